@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) Kimi Delta Attention layer: a C-ABI CUDA library plus a thin binding.
+
+    from gated_delta_rule_34_gb300 import chunk_prefill, decode_step, gate
+
+The binding loads ``_build/libkda.so`` on first use (build it with
+``python -m gated_delta_rule_34_gb300.build``); importing the package loads
+nothing, so the seeded input generator (``.inputs``) can be used without a GPU.
+"""
+from .api import (KDAError, chunk_prefill, decode_step, gate, lib, library_path,  # noqa: F401
+                  prefill_path, workspace_size)
+
+__all__ = ["KDAError", "chunk_prefill", "decode_step", "gate", "lib", "library_path",
+           "prefill_path", "workspace_size"]

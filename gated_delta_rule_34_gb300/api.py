@@ -1,0 +1,165 @@
+"""Thin Python binding of the KDA C ABI (include/kda.h).
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, and their data pointers plus the current CUDA stream are handed
+to ``libkda.so``.  Every step of the layer runs in the library's kernels; there
+is no fallback of any kind, and calling an op without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_LIB = None
+
+KDA_DTYPE_F32 = 0
+KDA_DTYPE_BF16 = 1
+PATH_NAMES = {0: "recurrent", 1: "chunked_tc"}
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+          4: "KDA_ERR_WORKSPACE"}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _declare(lib):
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.kda_status_string.argtypes = [i32]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_last_error.argtypes = []
+    lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_gate.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp]
+    lib.kda_gate.restype = i32
+    lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
+                                      i32, i32, i32, i32, i32, vp, sz, vp]
+    lib.kda_chunk_prefill.restype = i32
+    lib.kda_chunk_prefill_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32, i32]
+    lib.kda_chunk_prefill_workspace_size.restype = sz
+    lib.kda_chunk_prefill_path.argtypes = [i32, i32, i32, i32]
+    lib.kda_chunk_prefill_path.restype = i32
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.kda_decode_step.restype = i32
+    return lib
+
+
+def lib():
+    """The loaded ``libkda.so``; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"KDA CUDA library not found at {path}; build it with "
+                "`python -m gated_delta_rule_34_gb300.build` (there is no fallback path)")
+        _LIB = _declare(ctypes.CDLL(path))
+    return _LIB
+
+
+def _check(status: int):
+    if status != 0:
+        raise KDAError(status, lib().kda_last_error().decode())
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return KDA_DTYPE_F32
+    if t == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    raise TypeError(f"KDA inputs must be float32 or bfloat16, got {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("KDA ops take CUDA tensors")
+            if not t.is_contiguous():
+                raise ValueError("KDA ops take contiguous tensors")
+
+
+def gate(z: torch.Tensor, A: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """g = clamp(-5 * sigmoid(exp(A) * z), -5, 0) in fp32; z is [..., H, d_k], A is [H, d_k]."""
+    H, dk = z.shape[-2], z.shape[-1]
+    n_tokens = z.numel() // (H * dk) if z.numel() else 0
+    if out is None:
+        out = torch.empty(z.shape, dtype=torch.float32, device=z.device)
+    _need_cuda(z, A, out)
+    _check(lib().kda_gate(_ptr(z), _ptr(A), _ptr(out), n_tokens, H, dk, _dtype_code(z.dtype),
+                          _stream(z.device)))
+    return out
+
+
+def prefill_path(d_k: int, d_v: int, chunk: int, dtype: torch.dtype) -> str:
+    """Name of the kernel path kda_chunk_prefill takes for these sizes."""
+    return PATH_NAMES[lib().kda_chunk_prefill_path(d_k, d_v, chunk, _dtype_code(dtype))]
+
+
+def workspace_size(n_seqs: int, B: int, T: int, H: int, d_k: int, d_v: int, chunk: int,
+                   dtype: torch.dtype) -> int:
+    return int(lib().kda_chunk_prefill_workspace_size(n_seqs, B, T, H, d_k, d_v, chunk,
+                                                      _dtype_code(dtype)))
+
+
+def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chunk: int = 64,
+                  output_final_state: bool = True, out=None, final_state=None, workspace=None):
+    """Prefill through kda_chunk_prefill.
+
+    q, k, z: [B, T, H, d_k]; v: [B, T, H, d_v]; beta: [B, T, H] (one dtype, fp32 or bf16);
+    A: [H, d_k] fp32; initial_state: [N, H, d_k, d_v] fp32 or None; cu_seqlens: int32
+    [N + 1] on the device for a packed batch (then B must be 1).
+    Returns (o, final_state or None).  A workspace of the required size is allocated
+    with torch if none is given.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    need = workspace_size(n_seqs, B, T, H, dk, dv, chunk, q.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, cu_seqlens, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+        _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
+        _dtype_code(q.dtype), _ptr(workspace), ws_bytes, _stream(q.device)))
+    return out, final_state
+
+
+def decode_step(q, k, v, z, beta, A, state, out=None):
+    """One token per sequence; updates ``state`` [B, H, d_k, d_v] fp32 in place, returns o."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, z, beta, A, state, out)
+    _check(lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                 _ptr(state), _ptr(out), B, H, dk, dv, _dtype_code(q.dtype),
+                                 _stream(q.device)))
+    return out

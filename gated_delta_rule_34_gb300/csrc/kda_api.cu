@@ -1,0 +1,192 @@
+// kda_api.cu -- the C ABI: argument validation, path choice and launches.
+//
+// Every check happens on the host before anything is launched; nothing here
+// reads device memory.  Each entry point returns a kda_status and records a
+// one-line reason for the last failure in thread-local storage.
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kda_status fail(kda_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+kda_status ok() {
+    g_last_error[0] = '\0';
+    return KDA_OK;
+}
+
+kda_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 148;
+    return sms > 0 ? sms : 148;
+}
+
+bool valid_dtype(kda_dtype d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16; }
+
+// A pointer that must be present and 16-byte aligned.
+#define KDA_REQUIRE_PTR(p)                                                              \
+    do {                                                                                \
+        if ((p) == nullptr) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", #p);         \
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+    } while (0)
+
+#define KDA_OPTIONAL_PTR(p)                                                             \
+    do {                                                                                \
+        if ((p) != nullptr && !aligned16(p))                                            \
+            return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);          \
+    } while (0)
+
+constexpr bool kChunkedTcBuilt = false;
+
+bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
+    return kChunkedTcBuilt && dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && chunk == 64;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error(void) { return g_last_error; }
+
+kda_status kda_gate(const void* z, const float* A, float* g, int64_t n_tokens, int H, int d_k,
+                    kda_dtype z_dtype, cudaStream_t stream) {
+    if (!valid_dtype(z_dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)z_dtype);
+    if (n_tokens < 0 || H <= 0 || d_k <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes n_tokens=%lld H=%d d_k=%d",
+                    (long long)n_tokens, H, d_k);
+    if (n_tokens == 0) return ok();
+    KDA_REQUIRE_PTR(z);
+    KDA_REQUIRE_PTR(A);
+    KDA_REQUIRE_PTR(g);
+    return cuda_status(kda::run_gate(z, A, g, n_tokens, H, d_k, z_dtype == KDA_DTYPE_BF16, stream,
+                                     device_sm_count()),
+                       "kda_gate launch");
+}
+
+kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype dtype) {
+    return use_chunked_tc(d_k, d_v, chunk, dtype) ? KDA_PATH_CHUNKED_TC : KDA_PATH_RECURRENT;
+}
+
+size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int d_k, int d_v,
+                                        int chunk, kda_dtype dtype) {
+    if (n_seqs <= 0 || B <= 0 || T < 0 || H <= 0) return 0;
+    if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
+    return kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * T, H);
+}
+
+kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* z,
+                             const void* beta, const float* A, void* o,
+                             const float* initial_state, float* final_state,
+                             const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                             int d_k, int d_v, int chunk, kda_dtype dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B <= 0 || T < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || n_seqs <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%lld H=%d d_k=%d d_v=%d n_seqs=%d", B,
+                    (long long)T, H, d_k, d_v, n_seqs);
+    if (chunk != 16 && chunk != 64)
+        return fail(KDA_ERR_INVALID_ARG, "chunk must be 16 or 64, got %d", chunk);
+    if (cu_seqlens) {
+        if (B != 1) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens requires B == 1 (got %d)", B);
+        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is not 4-byte aligned");
+    } else if (n_seqs != B) {
+        return fail(KDA_ERR_INVALID_ARG, "without cu_seqlens n_seqs must equal B (%d vs %d)",
+                    n_seqs, B);
+    }
+    if (d_k > 128 || d_v > 128)
+        return fail(KDA_ERR_UNSUPPORTED, "head sizes above 128 are not supported (d_k=%d d_v=%d)",
+                    d_k, d_v);
+    if (H > 65535 || n_seqs > 65535)
+        return fail(KDA_ERR_UNSUPPORTED, "H and n_seqs must be <= 65535");
+    const int64_t T_total = (int64_t)B * T;
+    if (T_total > 0) {
+        KDA_REQUIRE_PTR(q);
+        KDA_REQUIRE_PTR(k);
+        KDA_REQUIRE_PTR(v);
+        KDA_REQUIRE_PTR(z);
+        KDA_REQUIRE_PTR(beta);
+        KDA_REQUIRE_PTR(o);
+    }
+    KDA_REQUIRE_PTR(A);
+    KDA_OPTIONAL_PTR(initial_state);
+    KDA_OPTIONAL_PTR(final_state);
+    const bool bf16 = dtype == KDA_DTYPE_BF16;
+
+    if (use_chunked_tc(d_k, d_v, chunk, dtype)) {
+        const size_t need = kda::chunked_tc_workspace_bytes(n_seqs, T_total, H);
+        if (need > 0) {
+            if (workspace == nullptr || workspace_bytes < need)
+                return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu at %p",
+                            need, workspace_bytes, workspace);
+            if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+                return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+        }
+        return cuda_status(kda::run_chunked_tc(q, k, v, z, beta, A, o, initial_state,
+                                               final_state, cu_seqlens, n_seqs, T, T_total, H,
+                                               workspace, stream, device_sm_count()),
+                           "kda_chunk_prefill (chunked tensor-core path)");
+    }
+    return cuda_status(kda::run_recurrent(q, k, v, z, beta, A, o, initial_state, final_state,
+                                          cu_seqlens, n_seqs, T, T_total, H, d_k, d_v, bf16,
+                                          stream),
+                       "kda_chunk_prefill (recurrent path)");
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* z,
+                           const void* beta, const float* A, float* state, void* o, int B, int H,
+                           int d_k, int d_v, kda_dtype dtype, cudaStream_t stream) {
+    if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 0 || H <= 0 || d_k <= 0 || d_v <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d H=%d d_k=%d d_v=%d", B, H, d_k, d_v);
+    if (d_k > 128 || d_v > 128 || d_v % 4 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "decode needs d_k <= 128 and d_v <= 128, d_v %% 4 == 0 "
+                    "(d_k=%d d_v=%d)", d_k, d_v);
+    if ((int64_t)B * H > 0x7fffffffLL)
+        return fail(KDA_ERR_UNSUPPORTED, "B*H too large");
+    if (B == 0) return ok();
+    KDA_REQUIRE_PTR(q);
+    KDA_REQUIRE_PTR(k);
+    KDA_REQUIRE_PTR(v);
+    KDA_REQUIRE_PTR(z);
+    KDA_REQUIRE_PTR(beta);
+    KDA_REQUIRE_PTR(A);
+    KDA_REQUIRE_PTR(state);
+    KDA_REQUIRE_PTR(o);
+    return cuda_status(kda::run_decode(q, k, v, z, beta, A, state, o, B, H, d_k, d_v,
+                                       dtype == KDA_DTYPE_BF16, stream),
+                       "kda_decode_step launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// kda_internal.h -- host-side launchers behind the C ABI (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+cudaError_t run_gate(const void* z, const float* A, float* g, int64_t n_tokens, int H, int dk,
+                     bool bf16, cudaStream_t stream, int num_sms);
+
+cudaError_t run_decode(const void* q, const void* k, const void* v, const void* z,
+                       const void* beta, const float* A, float* state, void* o, int B, int H,
+                       int dk, int dv, bool bf16, cudaStream_t stream);
+
+// Token-by-token SIMT path (fp32 arithmetic), any d_k, d_v <= 128.
+cudaError_t run_recurrent(const void* q, const void* k, const void* v, const void* z,
+                          const void* beta, const float* A, void* o, const float* S0, float* S1,
+                          const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
+                          int dk, int dv, bool bf16, cudaStream_t stream);
+
+// Chunked tensor-core path (bf16, d_k = d_v = 128, chunk 64).
+size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H);
+cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
+                           const void* beta, const float* A, void* o, const float* S0,
+                           float* S1, const int32_t* cu, int n_seqs, int64_t T,
+                           int64_t T_total, int H, void* workspace, cudaStream_t stream,
+                           int num_sms);
+
+}  // namespace kda

@@ -1,0 +1,177 @@
+// kda_recurrent.cu -- token-by-token prefill in fp32 SIMT arithmetic.
+//
+// The path for fp32 inputs (tf32 tensor cores cannot meet a 1e-4 relative
+// bound) and for head sizes the tensor-core path does not cover.  It runs the
+// delta rule of "Kimi K3 architecture review" with the per-channel gate of
+// "How Kimi K3 is built" exactly as written, one token after another:
+//
+//   S' = Diag(a_t) S,  u = b_t (v_t - S'^T k_t),  S <- S' + k_t u^T,
+//   o_t = S'^T q_t + u (k_t^T q_t)
+//
+// Columns of S evolve independently (column j only sees k, a, b and v[:, j]),
+// so the work splits over (sequence, head, 32-column group).  A CTA of eight
+// warps owns 32 columns; warp w owns 4 of them, lane l holds rows l, l+32,
+// l+64, l+96 of each (16 fp32 registers).  Tiles of 16 tokens are staged in
+// shared memory (q, k, the gate-derived decay a, beta, v for the 32 columns),
+// the decay is computed once per CTA per token and channel, and the d_k
+// reductions are warp butterflies.  The chunk size does not enter: the result
+// is the exact recurrence up to fp32 rounding.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+constexpr int kRecThreads = 256;
+constexpr int kRecTile = 16;     // tokens staged per shared-memory tile
+constexpr int kRecCols = 32;     // state columns per CTA (4 per warp)
+
+template <typename T>
+__global__ void __launch_bounds__(kRecThreads)
+recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                 const T* __restrict__ z, const T* __restrict__ beta,
+                 const float* __restrict__ A, T* __restrict__ o,
+                 const float* __restrict__ S0, float* __restrict__ S1,
+                 const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H,
+                 int dk, int dv) {
+    const int cgrp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int col0 = cgrp * kRecCols;           // first column of this CTA
+    const int wcol = warp * 4;                  // first column of this warp (CTA-local)
+
+    __shared__ float s_q[kRecTile][128], s_k[kRecTile][128], s_a[kRecTile][128];
+    __shared__ float s_v[kRecTile][kRecCols], s_o[kRecTile][kRecCols];
+    __shared__ float s_b[kRecTile], s_kq[kRecTile];
+    __shared__ float s_expA[128];
+
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_len, T_total, bos, eos);
+
+    for (int c = tid; c < 128; c += kRecThreads)
+        s_expA[c] = c < dk ? expf(A[(size_t)h * dk + c]) : 0.f;
+
+    // State registers: st[i][c] = S[lane + 32 i][col0 + wcol + c].
+    float st[4][4];
+    const size_t sbase = ((size_t)n * H + h) * dk * dv;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int j = col0 + wcol + c;
+            st[i][c] = (S0 && r < dk && j < dv) ? S0[sbase + (size_t)r * dv + j] : 0.f;
+        }
+    }
+
+    for (int64_t t0 = bos; t0 < eos; t0 += kRecTile) {
+        const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
+        __syncthreads();   // previous tile fully consumed; s_expA visible
+        for (int idx = tid; idx < kRecTile * 128; idx += kRecThreads) {
+            const int tt = idx >> 7, c = idx & 127;
+            float qq = 0.f, kk = 0.f, aa = 1.f;
+            if (tt < nt && c < dk) {
+                const size_t e = ((size_t)(t0 + tt) * H + h) * dk + c;
+                qq = to_f32(q[e]);
+                kk = to_f32(k[e]);
+                aa = expf(gate_accurate(s_expA[c], to_f32(z[e])));
+            }
+            s_q[tt][c] = qq;
+            s_k[tt][c] = kk;
+            s_a[tt][c] = aa;
+        }
+        for (int idx = tid; idx < kRecTile * kRecCols; idx += kRecThreads) {
+            const int tt = idx / kRecCols, jj = idx % kRecCols;
+            const int j = col0 + jj;
+            s_v[tt][jj] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j])
+                                              : 0.f;
+        }
+        if (tid < kRecTile)
+            s_b[tid] = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+        __syncthreads();
+        // k^T q per token: warp w handles tokens w and w + 8.
+        for (int tt = warp; tt < kRecTile; tt += kRecThreads / 32) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc += s_k[tt][lane + 32 * m] * s_q[tt][lane + 32 * m];
+            acc = warp_sum(acc);
+            if (lane == 0) s_kq[tt] = acc;
+        }
+        __syncthreads();
+
+        for (int tt = 0; tt < nt; ++tt) {
+            float a[4], kk[4], qq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = s_a[tt][lane + 32 * i];
+                kk[i] = s_k[tt][lane + 32 * i];
+                qq[i] = s_q[tt][lane + 32 * i];
+            }
+            float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    st[i][c] *= a[i];
+                    pk[c] = fmaf(st[i][c], kk[i], pk[c]);
+                    pq[c] = fmaf(st[i][c], qq[i], pq[c]);
+                }
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
+                    pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
+                }
+            }
+            const float b = s_b[tt], kq = s_kq[tt];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float u = b * (s_v[tt][wcol + c] - pk[c]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) st[i][c] = fmaf(kk[i], u, st[i][c]);
+                if (lane == c) s_o[tt][wcol + c] = fmaf(u, kq, pq[c]);
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nt * kRecCols; idx += kRecThreads) {
+            const int tt = idx / kRecCols, jj = idx % kRecCols;
+            const int j = col0 + jj;
+            if (j < dv) o[((size_t)(t0 + tt) * H + h) * dv + j] = from_f32<T>(s_o[tt][jj]);
+        }
+    }
+
+    if (S1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = col0 + wcol + c;
+                if (r < dk && j < dv) S1[sbase + (size_t)r * dv + j] = st[i][c];
+            }
+        }
+    }
+}
+
+cudaError_t run_recurrent(const void* q, const void* k, const void* v, const void* z,
+                          const void* beta, const float* A, void* o, const float* S0, float* S1,
+                          const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
+                          int dk, int dv, bool bf16, cudaStream_t stream) {
+    dim3 grid((unsigned)((dv + kRecCols - 1) / kRecCols), (unsigned)H, (unsigned)n_seqs);
+    if (bf16) {
+        using Tb = __nv_bfloat16;
+        recurrent_kernel<Tb><<<grid, kRecThreads, 0, stream>>>(
+            static_cast<const Tb*>(q), static_cast<const Tb*>(k), static_cast<const Tb*>(v),
+            static_cast<const Tb*>(z), static_cast<const Tb*>(beta), A, static_cast<Tb*>(o),
+            S0, S1, cu, T, T_total, H, dk, dv);
+    } else {
+        recurrent_kernel<float><<<grid, kRecThreads, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k),
+            static_cast<const float*>(v), static_cast<const float*>(z),
+            static_cast<const float*>(beta), A, static_cast<float*>(o), S0, S1, cu, T, T_total,
+            H, dk, dv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,147 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention layer library.
+ *
+ * The layer (per sequence n and head h; S is a d_k x d_v state):
+ *
+ *   g_t   = -5 * sigmoid(exp(A_h) (.) z_t)          (per channel, g_min = -5)
+ *   a_t   = exp(g_t)                                 (forget factor in [e^-5, 1])
+ *   S_t   = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T
+ *   o_t   = S_t^T q_t
+ *
+ * Sources: the gate is the forget-coefficient parametrisation of "How Kimi K3
+ * is built" (g = g_min*sigmoid(exp(A)*z), alpha = exp(g), g_min = -5); the
+ * state update is the delta rule of "Kimi K3 architecture review" (section on
+ * holding a million tokens of context: a fixed state that each token partly
+ * erases and then writes, beta the write strength, alpha the forget factor,
+ * alpha bounded to [e^-5, 1]); the per-channel forget gate is from both.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers owned by the caller, unless stated.
+ *     The library allocates no device memory, keeps no pointer after a call
+ *     returns, and launches its kernels asynchronously on `stream`.
+ *   - Layouts are row-major and dense:
+ *       q, k, z      [tokens, H, d_k]      (tokens = B*T, or packed T_total)
+ *       v, o         [tokens, H, d_v]
+ *       beta         [tokens, H]           (a scalar write strength in (0,1))
+ *       A            [H, d_k] fp32
+ *       states       [N, H, d_k, d_v] fp32 (d_v contiguous)
+ *     q, k, v, z, beta and o share one dtype (KDA_DTYPE_F32 or KDA_DTYPE_BF16).
+ *     The caller L2-normalises q and k if it wants unit keys; there is no
+ *     query scale.
+ *   - Every tensor pointer must be 16-byte aligned.
+ *   - Argument errors are reported before anything is launched.  Launch
+ *     failures are reported as KDA_ERR_CUDA.  Kernels never trap or assert;
+ *     kda_last_error() gives a one-line description of the last failure on
+ *     the calling thread.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or layout    */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d_k > 128)     */
+    KDA_ERR_CUDA = 3,          /* a CUDA call or kernel launch failed            */
+    KDA_ERR_WORKSPACE = 4      /* workspace missing or smaller than required     */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/* Which kernels kda_chunk_prefill runs for a given shape. */
+typedef enum {
+    KDA_PATH_RECURRENT = 0,    /* SIMT fp32, token by token, any d_k, d_v <= 128     */
+    KDA_PATH_CHUNKED_TC = 1    /* chunked WY/UT form on tcgen05 (bf16, d=128, C=64)  */
+} kda_prefill_path;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_string(kda_status s);
+
+/* Description of the last non-OK status returned on this thread ("" if none). */
+const char *kda_last_error(void);
+
+/*
+ * kda_gate -- the forget gate on its own.
+ *   g[t, h, c] = clamp(-5 * sigmoid(exp(A[h, c]) * z[t, h, c]), -5, 0)   (fp32 out)
+ * Defined by the gate formula of "How Kimi K3 is built" (g_min = -5); the clamp
+ * only guards the rounding of sigmoid and never moves an exact value.
+ *   z        [n_tokens, H, d_k] in z_dtype
+ *   A        [H, d_k] fp32
+ *   g        [n_tokens, H, d_k] fp32 (written)
+ * n_tokens may be 0 (nothing is launched).  Prefill and decode compute the gate
+ * inline from z and never read g.
+ */
+kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, int H, int d_k,
+                    kda_dtype z_dtype, cudaStream_t stream);
+
+/*
+ * kda_chunk_prefill -- o and (optionally) the final state for a batch of
+ * sequences, by the chunked form: tokens of one chunk in parallel, then the
+ * state passed from chunk to chunk ("Kimi K3 architecture review", chip-level
+ * FlashKDA section; the g_min bound that keeps every causal block a dense
+ * product is from "How Kimi K3 is built").
+ *
+ * Fixed-length batch: cu_seqlens == NULL, inputs [B, T, H, d], N = B = n_seqs.
+ * Packed batch:       cu_seqlens != NULL (device int32 [n_seqs + 1], rising
+ *                     from 0 to T), B must be 1, inputs [1, T, H, d],
+ *                     N = n_seqs.  Chunk boundaries restart at every sequence.
+ *                     Malformed offsets are clamped into [0, T] on the device:
+ *                     results are then unspecified but no access leaves the
+ *                     buffers.
+ *   initial_state  nullable; [N, H, d_k, d_v] fp32 (read).  NULL means zeros.
+ *   final_state    nullable; [N, H, d_k, d_v] fp32 (written).
+ *   o              [B, T, H, d_v] in `dtype` (written).
+ *   chunk          16 or 64 (the exact result does not depend on it).
+ *   workspace      device scratch of at least kda_chunk_prefill_workspace_size()
+ *                  bytes (may be NULL when that size is 0); 256-byte aligned;
+ *                  contents on entry are ignored.
+ * T == 0 (or every sequence empty) writes only the final states (copies of the
+ * initial ones, or zeros).
+ */
+kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
+                             const void *beta, const float *A, void *o,
+                             const float *initial_state, float *final_state,
+                             const int32_t *cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                             int d_k, int d_v, int chunk, kda_dtype dtype, void *workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of workspace kda_chunk_prefill needs for these sizes (0 if none).
+ * For packed batches pass B = 1, T = total tokens and the sequence count; the
+ * bound does not depend on the individual lengths.
+ */
+size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int d_k, int d_v,
+                                        int chunk, kda_dtype dtype);
+
+/* The kernel path kda_chunk_prefill takes for these sizes. */
+kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype dtype);
+
+/*
+ * kda_decode_step -- one token for each of B independent sequences, updating
+ * the state in place (the fixed-size state replaces a KV cache; "How Kimi K3
+ * is built" notes that reading this state is the cost of decoding):
+ *   S' = Diag(a) S,  u = b (v - S'^T k),  S <- S' + k u^T,  o = S'^T q + u (k^T q)
+ * which equals o = S_new^T q.
+ *   q, k, z  [B, H, d_k];  v, o [B, H, d_v];  beta [B, H]  (dtype)
+ *   A        [H, d_k] fp32
+ *   state    [B, H, d_k, d_v] fp32, read and overwritten
+ * Supports d_k <= 128 and d_v <= 128 with d_v a multiple of 4.  B == 0 is a
+ * no-op.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                           const void *beta, const float *A, float *state, void *o, int B, int H,
+                           int d_k, int d_v, kda_dtype dtype, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: exported symbols and host-side argument checks.
+
+Every call here is rejected by validation before anything is launched, so the
+tests run on a machine without a CUDA device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_delta_rule_34_gb300 as kda
+from gated_delta_rule_34_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 4
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gated_delta_rule_34_gb300 import build
+    build.build()
+    return kda.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kda_gate", "kda_chunk_prefill", "kda_decode_step", "kda_status_string",
+                 "kda_chunk_prefill_workspace_size", "kda_chunk_prefill_path", "kda_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", api.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(kda_\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(L, n)
+
+
+def test_status_strings(L):
+    for code, name in api.STATUS.items():
+        assert L.kda_status_string(code).decode() == name
+    assert L.kda_status_string(99).decode() == "KDA_ERR_UNKNOWN"
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def _prefill(L, **kw):
+    a = dict(q=_fake(), k=_fake(), v=_fake(), z=_fake(), beta=_fake(), A=_fake(), o=_fake(),
+             s0=None, s1=None, cu=None, n_seqs=1, B=1, T=8, H=2, dk=16, dv=16, chunk=16, dtype=0,
+             ws=None, ws_bytes=0)
+    a.update(kw)
+    return L.kda_chunk_prefill(a["q"], a["k"], a["v"], a["z"], a["beta"], a["A"], a["o"],
+                               a["s0"], a["s1"], a["cu"], a["n_seqs"], a["B"], a["T"], a["H"],
+                               a["dk"], a["dv"], a["chunk"], a["dtype"], a["ws"], a["ws_bytes"],
+                               None)
+
+
+def test_prefill_rejects_bad_arguments(L):
+    assert _prefill(L, q=None) == INVALID
+    assert b"q is NULL" in L.kda_last_error()
+    assert _prefill(L, k=_fake(0x10004)) == INVALID            # misaligned
+    assert b"16-byte" in L.kda_last_error()
+    assert _prefill(L, chunk=32) == INVALID
+    assert _prefill(L, dtype=7) == INVALID
+    assert _prefill(L, H=0) == INVALID
+    assert _prefill(L, T=-1) == INVALID
+    assert _prefill(L, n_seqs=2) == INVALID                     # != B without cu_seqlens
+    assert _prefill(L, cu=_fake(), B=2, n_seqs=3) == INVALID    # packed needs B == 1
+    assert _prefill(L, cu=_fake(0x10002)) == INVALID            # misaligned offsets
+    assert _prefill(L, dk=256) == UNSUPPORTED
+    assert _prefill(L, s0=_fake(0x10008)) == INVALID
+
+
+def test_prefill_tc_path_requires_workspace(L):
+    if L.kda_chunk_prefill_path(128, 128, 64, 1) != 1:
+        pytest.skip("chunked tensor-core path not built")
+    need = L.kda_chunk_prefill_workspace_size(1, 1, 4096, 2, 128, 128, 64, 1)
+    assert need > 0
+    rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=None, ws_bytes=0)
+    assert rc == WORKSPACE
+    rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=_fake(0x100000),
+                  ws_bytes=need - 1)
+    assert rc == WORKSPACE
+    rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=_fake(0x100010),
+                  ws_bytes=need)
+    assert rc == INVALID                                        # not 256-byte aligned
+
+
+def test_workspace_size_query(L):
+    assert L.kda_chunk_prefill_workspace_size(1, 1, 64, 1, 16, 16, 16, 0) == 0   # SIMT path
+    assert L.kda_chunk_prefill_workspace_size(0, 1, 64, 1, 128, 128, 64, 1) == 0
+
+
+def test_path_query(L):
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(16, 16, 16, 0)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 64, 0)] == "recurrent"   # fp32
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(64, 64, 64, 1)] == "recurrent"
+
+
+def test_gate_rejects_bad_arguments(L):
+    assert L.kda_gate(None, _fake(), _fake(), 4, 2, 16, 0, None) == INVALID
+    assert L.kda_gate(_fake(), _fake(), _fake(0x10004), 4, 2, 16, 0, None) == INVALID
+    assert L.kda_gate(_fake(), _fake(), _fake(), -1, 2, 16, 0, None) == INVALID
+    assert L.kda_gate(_fake(), _fake(), _fake(), 4, 2, 16, 5, None) == INVALID
+    assert L.kda_gate(None, None, None, 0, 2, 16, 0, None) == 0           # empty: no launch
+
+
+def test_decode_rejects_bad_arguments(L):
+    f = _fake()
+    assert L.kda_decode_step(None, f, f, f, f, f, f, f, 4, 2, 128, 128, 1, None) == INVALID
+    assert L.kda_decode_step(f, f, f, f, f, f, _fake(0x10004), f, 4, 2, 128, 128, 1,
+                             None) == INVALID
+    assert L.kda_decode_step(f, f, f, f, f, f, f, f, 4, 2, 256, 128, 1, None) == UNSUPPORTED
+    assert L.kda_decode_step(f, f, f, f, f, f, f, f, 4, 2, 128, 126, 1, None) == UNSUPPORTED
+    assert L.kda_decode_step(f, f, f, f, f, f, f, f, -1, 2, 128, 128, 1, None) == INVALID
+    assert L.kda_decode_step(None, None, None, None, None, None, None, None, 0, 2, 128, 128, 1,
+                             None) == 0                                     # empty: no launch
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(api, "_LIB", None)
+    monkeypatch.setattr(api, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        api.lib()
