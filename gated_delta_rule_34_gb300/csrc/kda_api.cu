@@ -56,10 +56,8 @@ bool valid_dtype(kda_dtype d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16
             return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);          \
     } while (0)
 
-constexpr bool kChunkedTcBuilt = false;
-
 bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
-    return kChunkedTcBuilt && dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && chunk == 64;
+    return dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && chunk == 64;
 }
 
 }  // namespace
