@@ -1,0 +1,409 @@
+"""Benchmark of the KDA layer on one GB300 (or N replicas under torchrun).
+
+One step is one pass of the whole hot path on synthetic inputs that are
+already resident in HBM:
+  prefill  B=1, H=32, T=65536, d_k=d_v=128, bf16 inputs, fp32 initial and final
+           state, chunk 64 (the long-context workload the headline metric names)
+  decode   one token for B=256 sequences, H=32, d=128, fp32 state in place
+Both inputs exceed the 129 MB L2 (2.15 GB of prefill inputs, 0.54 GB of decode
+state), so no flush is needed between steps.
+
+The JSON line reports prefill tokens/s as `value`, the tensor-core fraction of
+the prefill, decode GB/s, the roofline of the dominant prefill kernel, an
+end-to-end number through the C ABI with pinned host buffers, clocks sampled
+during the timed region, and the fp64 oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this layer
+has) on a bounded sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & % BF16 tensor peak (H=32,d=128); decode-step HBM GB/s"
+# Work per token-head of prefill at d_k = d_v = 128, chunk 64 (causal count):
+# C (3 d_k + 2 d_v) + 6 d_k d_v + C^2 / 3 FLOP, and 1,282 algorithmic bytes
+# (q, k, v, z, o in bf16 plus beta).  States add 64 KiB read + 64 KiB written
+# per (sequence, head).
+PREFILL_FLOP_PER_TH = 64 * (3 * 128 + 2 * 128) + 6 * 128 * 128 + 64 * 64 / 3
+PREFILL_FLOP_DENSE_PER_TH = 2 * 64 * (3 * 128 + 2 * 128) + 6 * 128 * 128 + 64 * 64 / 3
+PREFILL_BYTES_PER_TH = 1282
+STATE_BYTES = 128 * 128 * 4
+DECODE_BYTES_PER_BH = 2 * STATE_BYTES + 4 * 256 + 2 + 256
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, local):
+    import torch
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(seconds_budget: float = 20.0):
+    """Times the fp64 oracle on a bounded sample of the prefill workload.
+
+    The sample is the first L tokens of all 32 heads of the long-prefill inputs
+    (same seed and distributions), with L grown until the run takes a few
+    seconds, then scaled to about the budget.  Returns (tokens/s over all heads,
+    threads, description).
+    """
+    import oracle
+    from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[2]
+    threads = oracle.default_threads()
+    L = 256
+    while True:
+        x = make_inputs(w, T=L)
+        t0 = time.perf_counter()
+        oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"],
+                         n_threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_budget / 2 or L >= 65536:
+            break
+        L = min(65536, int(L * max(2.0, min(8.0, (seconds_budget / 2) / max(dt, 1e-3)))))
+    desc = (f"fp64 recurrence, first {L} tokens x {w.H} heads of the long-prefill workload "
+            f"(seed {w.seed}), {dt:.1f} s")
+    return L / dt, threads, desc
+
+
+def run_reference(args):
+    """The oracle arm: same metric and unit, on the host cores."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    import oracle
+    from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[2]
+    threads = oracle.default_threads()
+    L = int(os.environ.get("KDA_REF_SAMPLE_TOKENS", "2048"))
+    x = make_inputs(w, T=L)
+    run = lambda: oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],  # noqa
+                                   S0=x["S0"], n_threads=threads)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "long-prefill-h32-t65536 (bounded sample)", "B": 1,
+                       "T": L, "H": w.H, "d_k": 128, "d_v": 128, "chunk": 64},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"first {L} tokens x {w.H} heads per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, local)
+    import gated_delta_rule_34_gb300 as kda
+    from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs, token_heads
+
+    kda.lib()
+    peaks = load_peaks()
+    wp, wd = WORKLOADS[2], WORKLOADS[3]
+    xp = make_inputs(wp, device="cuda")
+    xd = make_inputs(wd, device="cuda")
+    B, T, H, dk = xp["q"].shape
+    dv = xp["v"].shape[-1]
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    S1 = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.workspace_size(B, B, T, H, dk, dv, wp.chunk, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    state = xd["S0"].clone()
+    od = torch.empty((wd.B, wd.H, wd.dv), dtype=torch.bfloat16, device="cuda")
+    path = kda.prefill_path(dk, dv, wp.chunk, torch.bfloat16)
+    n_prefill_kernels = 2 if path == "chunked_tc" else 1
+
+    def prefill():
+        kda.chunk_prefill(xp["q"], xp["k"], xp["v"], xp["z"], xp["beta"], xp["A"],
+                          initial_state=xp["S0"], chunk=wp.chunk, out=o, final_state=S1,
+                          workspace=ws)
+
+    def decode():
+        kda.decode_step(xd["q"], xd["k"], xd["v"], xd["z"], xd["beta"], xd["A"], state, out=od)
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    pre_ev = [[ev() for _ in range(n_prefill_kernels + 1)] for _ in range(K)]
+    dec_ev = [[ev(), ev()] for _ in range(K)]
+    start, end = ev(), ev()
+    for e in [x for evs in pre_ev + dec_ev for x in evs] + [start, end]:
+        e.record()                      # creates the CUDA events before their handles are used
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        kda.set_profile_events(pre_ev[i])
+        prefill()
+        kda.set_profile_events(dec_ev[i])
+        decode()
+    kda.set_profile_events(None)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    time.sleep(0.2)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(dist, start.elapsed_time(end))
+    status = int(ws[:4].view(torch.int32).item()) if ws.numel() >= 4 else 0
+
+    pre_ms = [e[0].elapsed_time(e[-1]) for e in pre_ev]
+    kern_ms = [[e[j].elapsed_time(e[j + 1]) for e in pre_ev] for j in range(n_prefill_kernels)]
+    dec_ms = [e[0].elapsed_time(e[1]) for e in dec_ev]
+    pre_avg = max_over_ranks(dist, sum(pre_ms) / K)
+    dec_avg = max_over_ranks(dist, sum(dec_ms) / K)
+    kern_avg = [sum(k) / K for k in kern_ms]
+
+    th = token_heads(wp, xp)                            # token-heads per prefill
+    tokens = B * T
+    value = world * tokens / (pre_avg * 1e-3)
+    flops = th * PREFILL_FLOP_PER_TH
+    flops_dense = th * PREFILL_FLOP_DENSE_PER_TH
+    pbytes = th * PREFILL_BYTES_PER_TH + 2 * B * H * STATE_BYTES
+    tflops = flops / (pre_avg * 1e-3) / 1e12
+    dbytes = wd.B * wd.H * DECODE_BYTES_PER_BH
+    dec_gbs = dbytes / (dec_avg * 1e-3) / 1e9
+
+    # Dominant prefill kernel and its roofline (HBM-bound: intensity < ridge).
+    names = ["chunk_prep", "state_pass"] if n_prefill_kernels == 2 else ["recurrent"]
+    dom = max(range(n_prefill_kernels), key=lambda j: kern_avg[j])
+    achieved = pbytes / (kern_avg[dom] * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            tr = json.load(f)
+        traffic = tr.get(names[dom])
+    except (OSError, ValueError):
+        pass
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": names[dom], "kernel_ms": kern_avg[dom],
+                "peak_source": peaks["source"],
+                "per_kernel_ms": {n: t for n, t in zip(names, kern_avg)}}
+
+    # End to end through the C ABI with pinned host buffers (copies inside the timing).
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = e2e_prefill(kda, xp, wp, steps=max(1, min(K, 3)))
+        e2e["value"] *= world
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        v, cores, desc = oracle_sample(args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; distributions of the layer's workloads)",
+            "config": {"workload": "long-prefill-h32-t65536 + decode-b256-h32", "B": B, "T": T,
+                       "H": H, "d_k": dk, "d_v": dv, "chunk": wp.chunk, "prefill_path": path,
+                       "decode_B": wd.B, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "prefill": {"ms": pre_avg, "tokens_per_s": value, "tflops_causal": tflops,
+                        "tensor_peak_frac_causal": tflops / peaks["bf16_tflops"],
+                        "tensor_peak_frac_dense_count": flops_dense / (pre_avg * 1e-3) / 1e12
+                        / peaks["bf16_tflops"],
+                        "hbm_gbs_algorithmic": pbytes / (pre_avg * 1e-3) / 1e9,
+                        "hbm_frac_algorithmic": pbytes / (pre_avg * 1e-3) / 1e9
+                        / peaks["hbm_gbs"],
+                        "device_status": status},
+            "decode": {"ms": dec_avg, "value": dec_gbs * world, "unit": "GB/s",
+                       "frac": dec_gbs / peaks["hbm_gbs"], "bytes_per_step": dbytes},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * (n_prefill_kernels + 1), "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_prefill(kda, xp, wp, steps: int):
+    """Prefill through the C ABI from pinned host buffers: H2D inputs, kernels, D2H o and S."""
+    import torch
+    host = {n: xp[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta", "A", "S0")}
+    dev = {n: torch.empty_like(xp[n]) for n in host}
+    B, T, H, dk = xp["q"].shape
+    dv = xp["v"].shape[-1]
+    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    S1 = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S1.shape, dtype=S1.dtype).pin_memory()
+    ws = torch.empty(kda.workspace_size(B, B, T, H, dk, dv, wp.chunk, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o.numel() * o.element_size() + S1.numel() * S1.element_size()
+
+    def step():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        kda.chunk_prefill(dev["q"], dev["k"], dev["v"], dev["z"], dev["beta"], dev["A"],
+                          initial_state=dev["S0"], chunk=wp.chunk, out=o, final_state=S1,
+                          workspace=ws)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S1, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": B * T / (ms * 1e-3), "unit": "tokens/s", "ms": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

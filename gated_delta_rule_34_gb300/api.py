@@ -50,6 +50,8 @@ def _declare(lib):
     lib.kda_chunk_prefill_path.restype = i32
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.kda_decode_step.restype = i32
+    lib.kda_set_profile_events.argtypes = [vp, i32]
+    lib.kda_set_profile_events.restype = i32
     return lib
 
 
@@ -163,3 +165,14 @@ def decode_step(q, k, v, z, beta, A, state, out=None):
                                  _ptr(state), _ptr(out), B, H, dk, dv, _dtype_code(q.dtype),
                                  _stream(q.device)))
     return out
+
+
+def set_profile_events(events) -> None:
+    """Makes later calls on this thread record ``events[0]`` before their first kernel and
+    ``events[i]`` after their i-th kernel (torch.cuda.Event objects); None switches it off."""
+    if events is None:
+        _check(lib().kda_set_profile_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    set_profile_events._keep = arr
+    _check(lib().kda_set_profile_events(arr, len(events)))

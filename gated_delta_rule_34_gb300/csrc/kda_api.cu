@@ -12,6 +12,8 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+thread_local cudaEvent_t* g_prof_events = nullptr;
+thread_local int g_prof_n = 0;
 
 kda_status fail(kda_status s, const char* fmt, ...) {
     va_list ap;
@@ -62,7 +64,20 @@ bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
 
 }  // namespace
 
+namespace kda {
+void profile_event(int i, cudaStream_t stream) {
+    if (g_prof_events && i < g_prof_n) cudaEventRecord(g_prof_events[i], stream);
+}
+}  // namespace kda
+
 extern "C" {
+
+kda_status kda_set_profile_events(cudaEvent_t* events, int n_events) {
+    if (n_events < 0) return fail(KDA_ERR_INVALID_ARG, "n_events must be >= 0");
+    g_prof_events = n_events > 0 ? events : nullptr;
+    g_prof_n = events ? n_events : 0;
+    return ok();
+}
 
 const char* kda_status_string(kda_status s) {
     switch (s) {
@@ -156,10 +171,12 @@ kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const 
                                                workspace, stream, device_sm_count()),
                            "kda_chunk_prefill (chunked tensor-core path)");
     }
-    return cuda_status(kda::run_recurrent(q, k, v, z, beta, A, o, initial_state, final_state,
-                                          cu_seqlens, n_seqs, T, T_total, H, d_k, d_v, bf16,
-                                          stream),
-                       "kda_chunk_prefill (recurrent path)");
+    kda::profile_event(0, stream);
+    const cudaError_t e = kda::run_recurrent(q, k, v, z, beta, A, o, initial_state, final_state,
+                                             cu_seqlens, n_seqs, T, T_total, H, d_k, d_v, bf16,
+                                             stream);
+    kda::profile_event(1, stream);
+    return cuda_status(e, "kda_chunk_prefill (recurrent path)");
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* z,
@@ -182,9 +199,11 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
     KDA_REQUIRE_PTR(A);
     KDA_REQUIRE_PTR(state);
     KDA_REQUIRE_PTR(o);
-    return cuda_status(kda::run_decode(q, k, v, z, beta, A, state, o, B, H, d_k, d_v,
-                                       dtype == KDA_DTYPE_BF16, stream),
-                       "kda_decode_step launch");
+    kda::profile_event(0, stream);
+    const cudaError_t e = kda::run_decode(q, k, v, z, beta, A, state, o, B, H, d_k, d_v,
+                                          dtype == KDA_DTYPE_BF16, stream);
+    kda::profile_event(1, stream);
+    return cuda_status(e, "kda_decode_step launch");
 }
 
 }  // extern "C"

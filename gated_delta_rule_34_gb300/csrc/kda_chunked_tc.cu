@@ -768,6 +768,7 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     if (e != cudaSuccess) return e;
     tc::SeqMap map{cu, T, T_total, n_seqs};
     using bf = __nv_bfloat16;
+    profile_event(0, stream);
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     if (T_total > 0) {
         dim3 grid_p((unsigned)slots, (unsigned)H);
@@ -777,10 +778,13 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    profile_event(1, stream);
     dim3 grid_s((unsigned)n_seqs, (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kThreads, tc::S_SMEM, stream>>>(
         ws, static_cast<bf*>(o), S0, S1, map, H);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    profile_event(2, stream);
+    return e;
 }
 
 }  // namespace kda

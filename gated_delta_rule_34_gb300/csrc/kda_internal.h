@@ -7,6 +7,9 @@
 
 namespace kda {
 
+// Records the caller-supplied profiling event i (if any) on `stream`.
+void profile_event(int i, cudaStream_t stream);
+
 cudaError_t run_gate(const void* z, const float* A, float* g, int64_t n_tokens, int H, int dk,
                      bool bf16, cudaStream_t stream, int num_sms);
 

@@ -104,10 +104,10 @@ def make_inputs(w: Workload, device: str = "cpu", T: int | None = None, B: int |
         lead = (1, int(cu[-1]))
         n_states = len(lengths)
     elif w.kind == "prefill":
-        lead = (B or w.B, T or w.T)
+        lead = (w.B if B is None else B, w.T if T is None else T)
         n_states = lead[0]
     else:
-        lead = (B or w.B,)
+        lead = (w.B if B is None else B,)
         n_states = lead[0]
     H, dk, dv = w.H, w.dk, w.dv
 

@@ -140,6 +140,17 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
                            const void *beta, const float *A, float *state, void *o, int B, int H,
                            int d_k, int d_v, kda_dtype dtype, cudaStream_t stream);
 
+/*
+ * Instrumentation (not part of the layer's arithmetic).  While `events` is
+ * non-NULL, every later kda_chunk_prefill / kda_decode_step call made on this
+ * thread records events[0] on its stream before its first kernel and
+ * events[i] after its i-th kernel, for i < n_events; the caller then reads
+ * per-kernel times with cudaEventElapsedTime.  The events stay owned by the
+ * caller.  Pass NULL to switch recording off.  Returns KDA_OK, or
+ * KDA_ERR_INVALID_ARG for n_events < 0.
+ */
+kda_status kda_set_profile_events(cudaEvent_t *events, int n_events);
+
 #ifdef __cplusplus
 }
 #endif
