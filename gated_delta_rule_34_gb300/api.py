@@ -50,6 +50,10 @@ def _declare(lib):
     lib.kda_chunk_prefill_path.restype = i32
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.kda_decode_step.restype = i32
+    lib.kda_chunk_prefill_static_workspace.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                       i32, i32, i64, i32, i32, i32, i32, i32,
+                                                       vp]
+    lib.kda_chunk_prefill_static_workspace.restype = i32
     lib.kda_set_profile_events.argtypes = [vp, i32]
     lib.kda_set_profile_events.restype = i32
     return lib
@@ -176,3 +180,28 @@ def set_profile_events(events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     set_profile_events._keep = arr
     _check(lib().kda_set_profile_events(arr, len(events)))
+
+
+def chunk_prefill_static_workspace(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
+                                   chunk: int = 64, output_final_state: bool = True, out=None,
+                                   final_state=None):
+    """chunk_prefill through kda_chunk_prefill_static_workspace: the library's own fixed
+    scratch array replaces the caller workspace, so nothing is allocated for it (the
+    outputs are still allocated here unless passed in)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    n_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((n_seqs, H, dk, dv), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, cu_seqlens)
+    _check(lib().kda_chunk_prefill_static_workspace(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+        _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
+        _dtype_code(q.dtype), _stream(q.device)))
+    return out, final_state

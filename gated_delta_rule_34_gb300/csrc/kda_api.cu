@@ -65,6 +65,14 @@ bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
 }  // namespace
 
 namespace kda {
+kda_status report(kda_status status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
 void profile_event(int i, cudaStream_t stream) {
     if (g_prof_events && i < g_prof_n) cudaEventRecord(g_prof_events[i], stream);
 }

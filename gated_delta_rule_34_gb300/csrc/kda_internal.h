@@ -5,7 +5,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/kda.h"
+
 namespace kda {
+
+// Records `status` with a printf-style reason for kda_last_error() and returns it.
+kda_status report(kda_status status, const char* fmt, ...);
 
 // Records the caller-supplied profiling event i (if any) on `stream`.
 void profile_event(int i, cudaStream_t stream);

@@ -141,6 +141,42 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
                            int d_k, int d_v, kda_dtype dtype, cudaStream_t stream);
 
 /*
+ * kda_chunk_prefill_static_workspace -- kda_chunk_prefill for callers that
+ * cannot allocate device memory.
+ *
+ * The pages describe no counterpart to this entry point; it exists for
+ * deployment.  The chunked tensor-core path needs device scratch, which
+ * kda_chunk_prefill takes from its caller.  Some callers cannot allocate it:
+ * a plugin hosted by a runtime that owns every device allocation and forbids
+ * its plugins from calling cudaMalloc, or a serving loop whose memory plan is
+ * fixed at start-up.  This entry point takes the same arguments minus the
+ * workspace and uses a library-owned __device__ array of
+ * KDA_STATIC_WORKSPACE_BYTES instead.  It allocates nothing.
+ *
+ *   - Every GPU that loads the library holds that array until the process exits.
+ *   - Sizes whose workspace (kda_chunk_prefill_workspace_size) exceeds
+ *     KDA_STATIC_WORKSPACE_BYTES are rejected with KDA_ERR_UNSUPPORTED before
+ *     any launch; kda_last_error() says how much they would need.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (the
+ *     kernels clear what must start at zero).  Calls whose kernels overlap on
+ *     the GPU -- concurrent streams, or several host threads -- race on it;
+ *     serialise them.
+ * Arguments, layouts and errors are otherwise those of kda_chunk_prefill.
+ */
+#define KDA_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+
+kda_status kda_chunk_prefill_static_workspace(const void *q, const void *k, const void *v,
+                                              const void *z, const void *beta, const float *A,
+                                              void *o, const float *initial_state,
+                                              float *final_state, const int32_t *cu_seqlens,
+                                              int n_seqs, int B, int64_t T, int H, int d_k,
+                                              int d_v, int chunk, kda_dtype dtype,
+                                              cudaStream_t stream);
+
+/*
  * Instrumentation (not part of the layer's arithmetic).  While `events` is
  * non-NULL, every later kda_chunk_prefill / kda_decode_step call made on this
  * thread records events[0] on its stream before its first kernel and
