@@ -70,6 +70,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
         : "memory");
 }
 
+// Asks L2 to fetch [src, src + bytes) ahead of a later bulk copy (16-byte
+// aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Shared -> global, tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),

@@ -9,7 +9,7 @@ import random
 
 import gated_delta_rule_34_gb300 as kda
 
-PKG_BYTES = 74752
+PKG_BYTES = 99328
 HEADER = 1024
 
 
