@@ -74,28 +74,33 @@ constexpr uint32_t kErrSmemAlign = 4u;
 
 // ---- chunk_prep ------------------------------------------------------------
 constexpr int kPrepThreads = 512;
-// shared memory (offsets from a 1024-byte aligned base)
+// shared memory (offsets from a 1024-byte aligned base).  The package image of
+// one item is staged in [0, PKG_BYTES) and stored asynchronously while the next
+// item starts: that range only holds buffers the next item first writes after
+// its scan (A-stack, K^(i), (b K^g)^T, (b V)^T), so the store has time to drain.
 constexpr uint32_t R_AST = 0;          // A-stack [128][128] swizzled (k rows, then q rows)
 constexpr uint32_t R_KV = 32768;       // K^(i) variants, 40 KB
-constexpr uint32_t R_G = 73728;        // L = block-local cumulative gate, fp32 [64][132]
+constexpr uint32_t R_BKT = 73728;      // (b K^g)^T [128 c][64 s] swizzled
+constexpr uint32_t R_BVT = 90112;      // (b V)^T  [128 j][64 s] swizzled
+constexpr uint32_t R_G = 106496;       // L = block-local cumulative gate, fp32 [64][132];
+                                       // also raw z and q of the next item (prefetched)
 constexpr uint32_t G_LD = 132;
-constexpr uint32_t R_K = 108544;       // raw k [64][128] bf16
-constexpr uint32_t R_V = 124928;       // raw v [64][128] bf16
-constexpr uint32_t R_BKT = 141312;     // (b K^g)^T [128 c][64 s] swizzled
-constexpr uint32_t R_BVT = 157696;     // (b V)^T  [128 j][64 s] swizzled
+constexpr uint32_t R_K = 141312;       // raw k [64][128] bf16
+constexpr uint32_t R_V = 157696;       // raw v [64][128] bf16
 constexpr uint32_t R_KC = 174080;      // (K^C)^T  [128 c][64 s] swizzled
 constexpr uint32_t R_P = 190464;       // P        [64 t][64 s] swizzled (follows K^C)
 constexpr uint32_t R_QG = 198656;      // Q^g      [64 t][128 c] swizzled, two K-blocks
 constexpr uint32_t R_SMALL = 215040;   // per-channel constants, beta
+constexpr uint32_t R_ZQ = R_G;         // raw z [64][128] bf16, then raw q, of the next item
 // reuse after the A/P products
 constexpr uint32_t R_AF = 0;           // A fp32 [64][65]
 constexpr uint32_t R_TF = 16896;       // T fp32 [64][65]
 constexpr uint32_t R_TB = 34816;       // T bf16 [64][64] swizzled
 constexpr uint32_t R_XS = 43008;       // solve scratch [3][16][16] fp32
 constexpr uint32_t F_LD = 65;
-// reuse after W / U~
-constexpr uint32_t R_WT = R_G;         // W^T  [128 c][64 s] swizzled
-constexpr uint32_t R_UT = R_G + 16384; // U~^T [128 j][64 s] swizzled
+// reuse after W / U~ (the solve's buffers and the A/P operands are dead)
+constexpr uint32_t R_WT = 0;           // W^T  [128 c][64 s] swizzled
+constexpr uint32_t R_UT = 16384;       // U~^T [128 j][64 s] swizzled
 constexpr uint32_t R_PKG = 0;          // package image, after the last products
 // small region, in floats
 constexpr uint32_t SM_TOT = 0;         // [4][128] block totals of g
@@ -104,7 +109,8 @@ constexpr uint32_t SM_EC = 1024;       // [4][128] e^{G_C - r_b}
 constexpr uint32_t SM_X = 1536;        // [6][128] e^{r_i - r_b}, i > b
 constexpr uint32_t SM_LAM = 2304;      // [128] e^{G_C}
 constexpr uint32_t SM_B = 2432;        // [64] beta
-constexpr uint32_t R_SMALL_BYTES = (2432 + 64) * 4;
+constexpr uint32_t SM_A = 2496;        // [128] A row of the next item (prefetched)
+constexpr uint32_t R_SMALL_BYTES = (2496 + 128) * 4;
 constexpr uint32_t R_BAR = R_SMALL + R_SMALL_BYTES;
 constexpr uint32_t P_SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
 
@@ -135,8 +141,9 @@ constexpr int kL2Ahead = 4;                        // packages prefetched into L
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
-static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 3 * 256 * 4 <= R_G, "solve scratch");
-static_assert(R_UT + 16384 <= R_K && R_PKG + PKG_BYTES <= R_KC, "reuse regions");
+static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 3 * 256 * 4 <= R_BKT, "solve scratch");
+static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions");
+static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
 struct SeqMap {
     const int32_t* cu;  // nullable
@@ -203,70 +210,53 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile_k
     }
 }
 
-// Row-block product readback: thread owns row t of block I; copies D_I's
-// 16 (I + 1) columns into row[] (columns beyond stay as they are).
-template <int I>
-__device__ __forceinline__ void load_block_row(uint32_t taddr_lane, bool mine, float (&row)[64]) {
-#pragma unroll
-    for (int q = 0; q <= I; ++q) {
-        float v[16];
-        tmem_ld16(taddr_lane + d_col(I) + 16u * q, v);
-        tmem_wait_ld();
-        if (mine) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) row[16 * q + e] = v[e];
-        }
-    }
-}
-
 // One distance of the blocked unit-lower inverse: for block pairs (i, j) with
-// i - j = d, X = sum_{m=j}^{i-1} A_im T_mj, then T_ij = -T_ii X.  Element
-// (pair p, row r, column col) is item tid + 512 k.
+// i - j = d, X = sum_{m=j}^{i-1} A_im T_mj, then T_ij = -T_ii X.  A thread
+// computes four adjacent columns of one row: item (pair p, row r, column
+// group c4), so each A element loaded feeds four FMAs.
 template <int d>
-__device__ __forceinline__ void solve_offdiag(const float* Af, float* Tf, float* Xs, int tid) {
-    constexpr int kItems = (4 - d) * 256;
-#pragma unroll
-    for (int it = tid; it < kItems; it += kPrepThreads) {
-        const int p = it >> 8, r = (it >> 4) & 15, col = it & 15;
+__device__ __forceinline__ void solve_offdiag(const float* __restrict__ Af, float* Tf,
+                                              float* Xs, int tid) {
+    constexpr int kItems = (4 - d) * 64;
+    if (tid < kItems) {
+        const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const int jb = p, ib = p + d;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int m = jb; m < ib; ++m) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                acc0 = fmaf(Af[(16 * ib + r) * F_LD + 16 * m + e],
-                            Tf[(16 * m + e) * F_LD + 16 * jb + col], acc0);
-                acc1 = fmaf(Af[(16 * ib + r) * F_LD + 16 * m + e + 1],
-                            Tf[(16 * m + e + 1) * F_LD + 16 * jb + col], acc1);
+        for (int mm = 0; mm < d; ++mm) {
+            const int m = jb + mm;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float a = Af[(16 * ib + r) * F_LD + 16 * m + e];
+                const float* tr = Tf + (16 * m + e) * F_LD + 16 * jb + c4;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) acc[cc] = fmaf(a, tr[cc], acc[cc]);
             }
         }
-        Xs[(p * 16 + r) * 16 + col] = acc0 + acc1;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) Xs[(p * 16 + r) * 16 + c4 + cc] = acc[cc];
     }
     __syncthreads();
-#pragma unroll
-    for (int it = tid; it < kItems; it += kPrepThreads) {
-        const int p = it >> 8, r = (it >> 4) & 15, col = it & 15;
+    if (tid < kItems) {
+        const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const int jb = p, ib = p + d;
-        float acc = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-            acc = fmaf(Tf[(16 * ib + r) * F_LD + 16 * ib + e], Xs[(p * 16 + e) * 16 + col], acc);
-        Tf[(16 * ib + r) * F_LD + 16 * jb + col] = -acc;
+        for (int e = 0; e < 16; ++e) {
+            const float tv = Tf[(16 * ib + r) * F_LD + 16 * ib + e];
+            const float* xr = Xs + (p * 16 + e) * 16 + c4;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) acc[cc] = fmaf(tv, xr[cc], acc[cc]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) Tf[(16 * ib + r) * F_LD + 16 * jb + c4 + cc] = -acc[cc];
     }
     __syncthreads();
 }
 
-// ============================================================================
-// chunk_prep: one CTA per (package slot, head).
-// ============================================================================
-__global__ void __launch_bounds__(kPrepThreads, 1)
-chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
-                  const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
-                  uint8_t* __restrict__ ws, SeqMap map, int H) {
-    const int slot = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // Which sequence and chunk this slot holds (binary search on slot bases).
+// Which chunk package slot `slot` holds: its first token t0 and length.
+// False for slots that hold no chunk (the slot space has a few spares).
+__device__ __forceinline__ bool slot_chunk(const SeqMap& map, int64_t slot, int64_t& t0, int& len) {
     int lo = 0, hi = map.n_seqs - 1;
     int64_t bos, eos;
     while (lo < hi) {
@@ -275,10 +265,80 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     }
     const int64_t chunk = slot - seq_slot_base(map, lo, bos, eos);
     const int64_t n_chunks = (eos - bos + kC - 1) / kC;
-    if (chunk < 0 || chunk >= n_chunks) return;   // empty slot: nothing allocated yet
-    const int64_t t0 = bos + chunk * kC;
-    const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
+    if (chunk < 0 || chunk >= n_chunks) return false;
+    t0 = bos + chunk * kC;
+    len = (int)((eos - t0) < kC ? (eos - t0) : kC);
+    return true;
+}
 
+// Writes row t of the A (warps holding key rows) or P (query rows) operand from
+// the row-block product D_I, once its 16 (I + 1) columns are loaded.
+template <int I>
+__device__ __forceinline__ void emit_block_row(uint32_t taddr_lane, bool mine, bool key_rows,
+                                               int t, float bt, float* Af, uint8_t* ptile) {
+    float v[16 * (I + 1)];
+#pragma unroll
+    for (int q = 0; q <= I; ++q) tmem_ld16(taddr_lane + d_col(I) + 16u * q,
+                                           *reinterpret_cast<float(*)[16]>(v + 16 * q));
+    tmem_wait_ld();
+    if (!mine) return;
+    if (key_rows) {
+#pragma unroll
+        for (int s = 0; s < 64; ++s) {
+            const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
+            Af[t * F_LD + s] = (s < t) ? bt * val : 0.f;
+        }
+    } else {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            float o8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s = ch * 8 + e;
+                const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
+                o8[e] = (s <= t) ? val : 0.f;
+            }
+            *reinterpret_cast<uint4*>(ptile + sw128(t, ch)) = pack8(o8);
+        }
+    }
+}
+
+// Issues the loads of one item's inputs: raw k, v (to R_K, R_V), z, q (to
+// R_ZQ) and the A row (to SM_A) as 16-byte async copies with zero fill past
+// `len`, plus beta into a register of threads < 64.  Completed by
+// cp_async_wait_all() in the item that consumes them.
+__device__ __forceinline__ void issue_item_loads(
+    uint8_t* sm, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
+    const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, int64_t t0, int len,
+    int h, int H, int tid, float& bt_reg) {
+    const size_t row0 = ((size_t)t0 * H + h) * kD;
+    const size_t rstride = (size_t)H * kD;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int i = it * kPrepThreads + tid;       // 0..4095
+        const int which = i >> 10, t = (i >> 4) & 63, ch = i & 15;
+        const __nv_bfloat16* base = which == 0 ? k : which == 1 ? v : which == 2 ? z : q;
+        const uint32_t dst = which == 0 ? R_K : which == 1 ? R_V : which == 2 ? R_ZQ : R_ZQ + 16384;
+        cp_async16(sm + dst + t * 256 + ch * 16,
+                   base + row0 + (size_t)(t < len ? t : 0) * rstride + ch * 8, t < len ? 16u : 0u);
+    }
+    if (tid < 32)
+        cp_async16(sm + R_SMALL + SM_A * 4 + tid * 16, A + (size_t)h * kD + tid * 4, 16u);
+    bt_reg = 0.f;
+    if (tid < kC && tid < len) bt_reg = __bfloat162float(beta[(size_t)(t0 + tid) * H + h]);
+}
+
+// ============================================================================
+// chunk_prep: persistent.  Each CTA walks the (package slot, head) items
+// blockIdx.x, blockIdx.x + gridDim.x, ... with item = slot * H + head.
+// ============================================================================
+__global__ void __launch_bounds__(kPrepThreads, 1)
+chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
+                  const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
+                  uint8_t* __restrict__ ws, SeqMap map, int H, int64_t n_items) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -287,45 +347,59 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 8);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-    uint8_t* pkg = ws + WS_HEADER + ((size_t)slot * H + h) * PKG_BYTES;
 
     if (warp == 0) tmem_alloc<512>(tslot);
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    uint32_t phase = 0;                      // parity of the next completion of `bar`
+    bool ok = true;
+    const int c8 = tid & 15;                 // channels 8 c8 .. 8 c8 + 7 in the row-side passes
 
-    // ---- prologue: raw k, v into shared memory (zero rows past len); z and q
-    //      for this thread's two (token, 8-channel) items into registers.
-    const size_t row0 = ((size_t)t0 * H + h) * kD;
-    const size_t rstride = (size_t)H * kD;
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int i = it * kPrepThreads + tid;       // 0..2047
-        const int which = i >> 10, t = (i >> 4) & 63, ch = i & 15;
-        const __nv_bfloat16* src =
-            (which ? v : k) + row0 + (size_t)(t < len ? t : 0) * rstride + ch * 8;
-        cp_async16(sm + (which ? R_V : R_K) + t * 256 + ch * 16, src, t < len ? 16u : 0u);
-    }
-    if (tid < kC)
-        small[SM_B + tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-    const int c8 = tid & 15;                 // this thread's channels: 8 c8 .. 8 c8 + 7
-    int tt[2];
-    uint4 zraw[2], qraw[2];
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        tt[it] = it * 32 + (tid >> 4);
-        const bool in = tt[it] < len;
-        const size_t off = row0 + (size_t)(in ? tt[it] : 0) * rstride + c8 * 8;
-        zraw[it] = in ? __ldg(reinterpret_cast<const uint4*>(z + off)) : make_uint4(0, 0, 0, 0);
-        qraw[it] = in ? __ldg(reinterpret_cast<const uint4*>(q + off)) : make_uint4(0, 0, 0, 0);
-    }
+    // The first item's inputs; later items' inputs are issued one item ahead.
+    int64_t item = blockIdx.x;
+    int64_t t0 = 0;
+    int len = 0;
+    float bt_reg = 0.f;
+    while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
+    if (item < n_items)
+        issue_item_loads(sm, q, k, v, z, beta, A, t0, len, (int)(item % H), H, tid, bt_reg);
 
-    // ---- gate g = -5 sigmoid(e^A z) into G (0 on padded rows)
-    {
+    while (item < n_items) {
+        const int h = (int)(item % H);
+        uint8_t* pkg = ws + WS_HEADER + (size_t)item * PKG_BYTES;
+        // The next item this CTA processes (skipping slots that hold no chunk).
+        int64_t nitem = item + gridDim.x, nt0 = 0;
+        int nlen = 0;
+        while (nitem < n_items && !slot_chunk(map, nitem / H, nt0, nlen)) nitem += gridDim.x;
+
+        // ---- inputs of this item (issued during the previous one) -> registers
+        cp_async_wait_all();
+        __syncthreads();
+        int tt[2];
+        uint4 zraw[2], qraw[2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            tt[it] = it * 32 + (tid >> 4);
+            zraw[it] = *reinterpret_cast<const uint4*>(sm + R_ZQ + tt[it] * 256 + c8 * 16);
+            qraw[it] = *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16);
+        }
         float eA[8];
+        {
+            float a8[8];
+            load8f(small + SM_A + c8 * 8, a8);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) eA[e] = __expf(__ldg(A + (size_t)h * kD + c8 * 8 + e));
+            for (int e = 0; e < 8; ++e) eA[e] = __expf(a8[e]);
+        }
+        if (tid < kC) small[SM_B + tid] = bt_reg;
+        __syncthreads();                         // raw z, q are read before G is written
+
+        // ---- gate g = -5 sigmoid(e^A z) into G (0 on padded rows)
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             float zf[8], g[8];
@@ -336,301 +410,315 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             dst[0] = make_float4(g[0], g[1], g[2], g[3]);
             dst[1] = make_float4(g[4], g[5], g[6], g[7]);
         }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-
-    // ---- block-local cumulative log-decay L_t = G_t - r_b (16-token scans), and
-    //      per-channel block factors from the block totals.
-    {
-        const int c = tid & 127, b = tid >> 7;
-        float run = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float* p = G + (16 * b + i) * G_LD + c;
-            run += *p;
-            *p = run;
-        }
-        small[SM_TOT + b * 128 + c] = run;
         __syncthreads();
-        const float t0v = small[SM_TOT + c], t1v = small[SM_TOT + 128 + c];
-        const float t2v = small[SM_TOT + 256 + c], t3v = small[SM_TOT + 384 + c];
-        const float r1 = t0v, r2 = t0v + t1v, r3 = r2 + t2v, rc = r3 + t3v;
-        if (b == 0) {
-            small[SM_ER + 0 * 128 + c] = 1.f;
-            small[SM_ER + 1 * 128 + c] = __expf(r1);
-            small[SM_ER + 2 * 128 + c] = __expf(r2);
-            small[SM_ER + 3 * 128 + c] = __expf(r3);
-        } else if (b == 1) {
-            small[SM_EC + 0 * 128 + c] = __expf(rc);
-            small[SM_EC + 1 * 128 + c] = __expf(rc - r1);
-            small[SM_EC + 2 * 128 + c] = __expf(rc - r2);
-            small[SM_EC + 3 * 128 + c] = __expf(rc - r3);
-        } else if (b == 2) {
-            small[SM_X + xidx(1, 0) * 128 + c] = __expf(r1);
-            small[SM_X + xidx(2, 0) * 128 + c] = __expf(r2);
-            small[SM_X + xidx(3, 0) * 128 + c] = __expf(r3);
-            small[SM_LAM + c] = __expf(rc);
-        } else {
-            small[SM_X + xidx(2, 1) * 128 + c] = __expf(r2 - r1);
-            small[SM_X + xidx(3, 1) * 128 + c] = __expf(r3 - r1);
-            small[SM_X + xidx(3, 2) * 128 + c] = __expf(r3 - r2);
-        }
-        __syncthreads();
-    }
 
-    // ---- row-side operands (thread = token t, 8 channels)
-    {
-        const int kb = c8 >> 3, chk = c8 & 7;
+        // ---- block-local cumulative log-decay L_t = G_t - r_b (16-token scans), and
+        //      per-channel block factors from the block totals.
+        {
+            const int c = tid & 127, b = tid >> 7;
+            float run = 0.f;
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int t = tt[it], b = t >> 4;
-            float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], o8[8];
-            load8f(G + t * G_LD + c8 * 8, Lt);
-            load8f(small + SM_ER + b * 128 + c8 * 8, er);
-            unpack8(*reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16), kf);
-            unpack8(qraw[it], qf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                E[e] = __expf(Lt[e]);                      // e^{G_t - r_b} in [e^-80, 1]
-                Rr[e] = __fdividef(1.0f, E[e]);            // e^{r_b - G_t} in [1, e^80]
+            for (int i = 0; i < 16; ++i) {
+                float* p = G + (16 * b + i) * G_LD + c;
+                run += *p;
+                *p = run;
             }
+            small[SM_TOT + b * 128 + c] = run;
+            __syncthreads();
+            const float t0v = small[SM_TOT + c], t1v = small[SM_TOT + 128 + c];
+            const float t2v = small[SM_TOT + 256 + c], t3v = small[SM_TOT + 384 + c];
+            const float r1 = t0v, r2 = t0v + t1v, r3 = r2 + t2v, rc = r3 + t3v;
+            if (b == 0) {
+                small[SM_ER + 0 * 128 + c] = 1.f;
+                small[SM_ER + 1 * 128 + c] = __expf(r1);
+                small[SM_ER + 2 * 128 + c] = __expf(r2);
+                small[SM_ER + 3 * 128 + c] = __expf(r3);
+            } else if (b == 1) {
+                small[SM_EC + 0 * 128 + c] = __expf(rc);
+                small[SM_EC + 1 * 128 + c] = __expf(rc - r1);
+                small[SM_EC + 2 * 128 + c] = __expf(rc - r2);
+                small[SM_EC + 3 * 128 + c] = __expf(rc - r3);
+            } else if (b == 2) {
+                small[SM_X + xidx(1, 0) * 128 + c] = __expf(r1);
+                small[SM_X + xidx(2, 0) * 128 + c] = __expf(r2);
+                small[SM_X + xidx(3, 0) * 128 + c] = __expf(r3);
+                small[SM_LAM + c] = __expf(rc);
+            } else {
+                small[SM_X + xidx(2, 1) * 128 + c] = __expf(r2 - r1);
+                small[SM_X + xidx(3, 1) * 128 + c] = __expf(r3 - r1);
+                small[SM_X + xidx(3, 2) * 128 + c] = __expf(r3 - r2);
+            }
+            // The previous item's package store must have read the staging area
+            // before the row-side pass overwrites it.
+            if (tid == 0) bulk_wait_read_all();
+            __syncthreads();
+        }
+
+        // ---- row-side operands (thread = token t, 8 channels); G keeps E = e^{L} after.
+        {
+            const int kb = c8 >> 3, chk = c8 & 7;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
-            *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(t, chk)) = pack8(o8);
+            for (int it = 0; it < 2; ++it) {
+                const int t = tt[it], b = t >> 4;
+                float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], o8[8];
+                load8f(G + t * G_LD + c8 * 8, Lt);
+                load8f(small + SM_ER + b * 128 + c8 * 8, er);
+                unpack8(*reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16), kf);
+                unpack8(qraw[it], qf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
-            *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(64 + t, chk)) = pack8(o8);
+                for (int e = 0; e < 8; ++e) {
+                    E[e] = __expf(Lt[e]);                      // e^{G_t - r_b} in [e^-80, 1]
+                    Rr[e] = __fdividef(1.0f, E[e]);            // e^{r_b - G_t} in [1, e^80]
+                }
+                float4* gp = reinterpret_cast<float4*>(G + t * G_LD + c8 * 8);
+                gp[0] = make_float4(E[0], E[1], E[2], E[3]);
+                gp[1] = make_float4(E[4], E[5], E[6], E[7]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e] * er[e];          // q e^{G_t}
-            *reinterpret_cast<uint4*>(sm + R_QG + kb * 8192 + sw128(t, chk)) = pack8(o8);
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+                *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(t, chk)) = pack8(o8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+                *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(64 + t, chk)) = pack8(o8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e] * er[e];          // q e^{G_t}
+                *reinterpret_cast<uint4*>(sm + R_QG + kb * 8192 + sw128(t, chk)) = pack8(o8);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (i < b) continue;
+                    float x[8];
+                    if (i == b) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = 1.f;
+                    } else {
+                        load8f(small + SM_X + xidx(i, b) * 128 + c8 * 8, x);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * x[e];  // k e^{r_i - G_t}
+                    *reinterpret_cast<uint4*>(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 +
+                                              sw128(t, chk)) = pack8(o8);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- A and P: four row-block products D_i = Astack * K^(i)^T into TMEM,
+        //      running while the column-side operands are built.
+        if (tid == 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (i < b) continue;
-                float x[8];
-                if (i == b) {
+                const uint32_t idesc = idesc_bf16(128, kv_rows(i));
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = 1.f;
-                } else {
-                    load8f(small + SM_X + xidx(i, b) * 128 + c8 * 8, x);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    const uint64_t ad = desc_sw128(smem_u32(sm + R_AST + kb * 16384 + off));
+                    const uint64_t bd = desc_sw128(
+                        smem_u32(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 + off));
+                    mma_bf16(tbase + d_col(i), ad, bd, idesc, ks > 0);
                 }
+            }
+            mma_commit(bar);
+        }
+
+        // ---- column-side operands, transposed (thread = channel c, tokens of block b)
+        {
+            const int c = tid & 127, b = tid >> 7;
+            const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
+            const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_V);
+            const float er = small[SM_ER + b * 128 + c], ec = small[SM_EC + b * 128 + c];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * x[e];    // k e^{r_i - G_t}
-                *reinterpret_cast<uint4*>(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 +
-                                          sw128(t, chk)) = pack8(o8);
+            for (int it = 0; it < 2; ++it) {
+                const int s8 = 2 * b + it;
+                float bk[8], kc[8], bv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s = s8 * 8 + e;
+                    const float bs = small[SM_B + s];
+                    const float kf = __bfloat162float(kraw[s * kD + c]);
+                    const float E = G[s * G_LD + c];
+                    bk[e] = bs * kf * E * er;                  // b_s k_s e^{G_s}
+                    kc[e] = kf * ec * __fdividef(1.0f, E);     // k_s e^{G_C - G_s}
+                    bv[e] = bs * __bfloat162float(vraw[s * kD + c]);
+                }
+                *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
+                *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
+                *reinterpret_cast<uint4*>(sm + R_BVT + sw128(c, s8)) = pack8(bv);
             }
         }
-    }
+        ok = mbar_wait(bar, phase) && ok;
+        phase ^= 1u;
+        tc_fence_after();
 
-    // ---- column-side operands, transposed (thread = channel c, tokens of block b)
-    {
-        const int c = tid & 127, b = tid >> 7;
-        const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
-        const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_V);
-        const float er = small[SM_ER + b * 128 + c], ec = small[SM_EC + b * 128 + c];
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int s8 = 2 * b + it;
-            float bk[8], kc[8], bv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = s8 * 8 + e;
-                const float bs = small[SM_B + s];
-                const float kf = __bfloat162float(kraw[s * kD + c]);
-                const float E = __expf(G[s * G_LD + c]);
-                bk[e] = bs * kf * E * er;                  // b_s k_s e^{G_s}
-                kc[e] = kf * ec * __fdividef(1.0f, E);     // k_s e^{G_C - G_s}
-                bv[e] = bs * __bfloat162float(vraw[s * kD + c]);
-            }
-            *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
-            *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
-            *reinterpret_cast<uint4*>(sm + R_BVT + sw128(c, s8)) = pack8(bv);
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tslot;
-
-    // ---- A and P: four row-block products D_i = Astack * K^(i)^T into TMEM
-    if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t idesc = idesc_bf16(128, kv_rows(i));
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                const uint64_t ad = desc_sw128(smem_u32(sm + R_AST + kb * 16384 + off));
-                const uint64_t bd =
-                    desc_sw128(smem_u32(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 + off));
-                mma_bf16(tbase + d_col(i), ad, bd, idesc, ks > 0);
-            }
-        }
-        mma_commit(bar);
-    }
-    bool ok = mbar_wait(bar, 0);
-    tc_fence_after();
-
-    // Readback: warps 0/1 hold key rows (-> A), warps 2/3 query rows (-> P).
-    if (warp < 4) {
-        const int lane_base = 32 * warp;
-        const int t = (lane_base + lane) & 63;
-        const int blk = t >> 4;
-        const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
-        float row[64];
-#pragma unroll
-        for (int s = 0; s < 64; ++s) row[s] = 0.f;
-        if ((warp & 1) == 0) {
-            load_block_row<0>(taddr, blk == 0, row);
-            load_block_row<1>(taddr, blk == 1, row);
-        } else {
-            load_block_row<2>(taddr, blk == 2, row);
-            load_block_row<3>(taddr, blk == 3, row);
-        }
-        if (warp < 2) {
+        // Readback: warps 0/1 hold key rows (-> A), warps 2/3 query rows (-> P).
+        if (warp < 4) {
+            const int lane_base = 32 * warp;
+            const int t = (lane_base + lane) & 63;
+            const int blk = t >> 4;
+            const bool key_rows = warp < 2;
+            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
             float* Af = reinterpret_cast<float*>(sm + R_AF);
             const float bt = small[SM_B + t];
+            if ((warp & 1) == 0) {
+                emit_block_row<0>(taddr, blk == 0, key_rows, t, bt, Af, sm + R_P);
+                emit_block_row<1>(taddr, blk == 1, key_rows, t, bt, Af, sm + R_P);
+            } else {
+                emit_block_row<2>(taddr, blk == 2, key_rows, t, bt, Af, sm + R_P);
+                emit_block_row<3>(taddr, blk == 3, key_rows, t, bt, Af, sm + R_P);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // Raw k, v and G are dead now: start loading the next item's inputs.
+        if (nitem < n_items)
+            issue_item_loads(sm, q, k, v, z, beta, A, nt0, nlen, (int)(nitem % H), H, tid, bt_reg);
+
+        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution,
+        //      then the off-diagonal blocks by distance.
+        {
+            const float* Af = reinterpret_cast<const float*>(sm + R_AF);
+            float* Tf = reinterpret_cast<float*>(sm + R_TF);
+            float* Xs = reinterpret_cast<float*>(sm + R_XS);
+            if (tid < 64) {
+                // Column j of the inverse of diagonal block blk, by forward substitution;
+                // rows of A are read before any T entry is written.
+                const int blk = tid >> 4, j = tid & 15;
+                const float* __restrict__ Ab = Af + 16 * blk * F_LD + 16 * blk;
+                float x[16];
 #pragma unroll
-            for (int s = 0; s < 64; ++s) Af[t * F_LD + s] = (s < t) ? bt * row[s] : 0.f;
-        } else {
+                for (int r = 0; r < 16; ++r) {
+                    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
+                    for (int m = 0; m + 1 < r; m += 2) {
+                        a0 = fmaf(Ab[r * F_LD + m], x[m], a0);
+                        a1 = fmaf(Ab[r * F_LD + m + 1], x[m + 1], a1);
+                    }
+                    if (r & 1) a0 = fmaf(Ab[r * F_LD + r - 1], x[r - 1], a0);
+                    x[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tf[(16 * blk + r) * F_LD + 16 * blk + j] = x[r];
+            }
+            __syncthreads();
+            solve_offdiag<1>(Af, Tf, Xs, tid);
+            solve_offdiag<2>(Af, Tf, Xs, tid);
+            solve_offdiag<3>(Af, Tf, Xs, tid);
+            // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
+            {
+                const int t = tid >> 3, ch = tid & 7;
                 float o8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = (ch * 8 + e <= t) ? row[ch * 8 + e] : 0.f;
-                *reinterpret_cast<uint4*>(sm + R_P + sw128(t, ch)) = pack8(o8);
+                for (int e = 0; e < 8; ++e) {
+                    const int s = ch * 8 + e;
+                    o8[e] = (s <= t) ? Tf[t * F_LD + s] : 0.f;
+                }
+                *reinterpret_cast<uint4*>(sm + R_TB + sw128(t, ch)) = pack8(o8);
             }
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution,
-    //      then the off-diagonal blocks by distance.
-    {
-        const float* Af = reinterpret_cast<const float*>(sm + R_AF);
-        float* Tf = reinterpret_cast<float*>(sm + R_TF);
-        float* Xs = reinterpret_cast<float*>(sm + R_XS);
-        if (tid < 64) {
-            const int blk = tid >> 4, j = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < r; ++m)
-                    acc = fmaf(Af[(16 * blk + r) * F_LD + 16 * blk + m], x[m], acc);
-                x[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
-                Tf[(16 * blk + r) * F_LD + 16 * blk + j] = x[r];
-            }
-        }
+        fence_async_smem();
+        tc_fence_before();
         __syncthreads();
-        solve_offdiag<1>(Af, Tf, Xs, tid);
-        solve_offdiag<2>(Af, Tf, Xs, tid);
-        solve_offdiag<3>(Af, Tf, Xs, tid);
-        // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
-        {
-            const int t = tid >> 3, ch = tid & 7;
-            float o8[8];
+        tc_fence_after();
+
+        // ---- W^T = (b K^g)^T T^T -> cols [0,64), U~^T = (b V)^T T^T -> cols [64,128)
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 64);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = ch * 8 + e;
-                o8[e] = (s <= t) ? Tf[t * F_LD + s] : 0.f;
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bd = desc_sw128(smem_u32(sm + R_TB + ks * 32));
+                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_BKT + ks * 32)), bd, idesc, ks > 0);
+                mma_bf16(tbase + 64, desc_sw128(smem_u32(sm + R_BVT + ks * 32)), bd, idesc, ks > 0);
             }
-            *reinterpret_cast<uint4*>(sm + R_TB + sw128(t, ch)) = pack8(o8);
+            mma_commit(bar);
         }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- W^T = (b K^g)^T T^T -> cols [0,64), U~^T = (b V)^T T^T -> cols [64,128)
-    if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = desc_sw128(smem_u32(sm + R_TB + ks * 32));
-            mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_BKT + ks * 32)), bd, idesc, ks > 0);
-            mma_bf16(tbase + 64, desc_sw128(smem_u32(sm + R_BVT + ks * 32)), bd, idesc, ks > 0);
+        ok = mbar_wait(bar, phase) && ok;
+        phase ^= 1u;
+        tc_fence_after();
+        // W^T and U~^T as bf16 K-major operands, thread = row (channel / column).
+        if (warp < 8) {
+            const int lane_base = 32 * (warp & 3);
+            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16) + (warp < 4 ? 0u : 64u);
+            tmem_row_to_tile<4>(taddr, sm + (warp < 4 ? R_WT : R_UT), 0, lane_base + lane);
         }
-        mma_commit(bar);
-    }
-    ok = mbar_wait(bar, 1) && ok;
-    tc_fence_after();
-    // W^T and U~^T as bf16 K-major operands, thread = row (channel / column).
-    if (warp < 8) {
-        const int lane_base = 32 * (warp & 3);
-        const uint32_t taddr = tbase + ((uint32_t)lane_base << 16) + (warp < 4 ? 0u : 64u);
-        tmem_row_to_tile<4>(taddr, sm + (warp < 4 ? R_WT : R_UT), 0, lane_base + lane);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
 
-    // ---- N = (K^C)^T W -> cols [0,128); [X^T | O'^T] = U~^T [K^C | P^T] -> [128,320);
-    //      (P W)^T = W^T P^T -> [320,384)
-    if (tid == 0) {
+        // ---- N = (K^C)^T W -> cols [0,128); [X^T | O'^T] = U~^T [K^C | P^T] -> [128,320);
+        //      P W -> [320,448): an M=128 product whose A rows 0..63 are P (rows 64..127
+        //      read the next tile and land in unused accumulator rows).
+        if (tid == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t off = ks * 32;
-            mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_KC + off)),
-                     desc_sw128(smem_u32(sm + R_WT + off)), idesc_bf16(128, 128), ks > 0);
-            mma_bf16(tbase + 128, desc_sw128(smem_u32(sm + R_UT + off)),
-                     desc_sw128(smem_u32(sm + R_KC + off)), idesc_bf16(128, 192), ks > 0);
-            mma_bf16(tbase + 320, desc_sw128(smem_u32(sm + R_WT + off)),
-                     desc_sw128(smem_u32(sm + R_P + off)), idesc_bf16(128, 64), ks > 0);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t off = ks * 32;
+                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_KC + off)),
+                         desc_sw128(smem_u32(sm + R_WT + off)), idesc_bf16(128, 128), ks > 0);
+                mma_bf16(tbase + 128, desc_sw128(smem_u32(sm + R_UT + off)),
+                         desc_sw128(smem_u32(sm + R_KC + off)), idesc_bf16(128, 192), ks > 0);
+                mma_bf16(tbase + 320, desc_sw128(smem_u32(sm + R_P + off)),
+                         desc_sw128(smem_u32(sm + R_WT + off)), idesc_bf16(128, 128), ks > 0);
+            }
+            mma_commit(bar);
         }
-        mma_commit(bar);
-    }
-    ok = mbar_wait(bar, 0) && ok;
-    tc_fence_after();
+        ok = mbar_wait(bar, phase) && ok;
+        phase ^= 1u;
+        tc_fence_after();
 
-    // ---- the package image, staged in shared memory
-    {
-        const int lane_base = 32 * (warp & 3);
-        const uint32_t row = lane_base + lane;
-        const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
-        const int role = warp >> 2;
-        if (role == 0) {            // N[c][c'] -> B rows c, both K-blocks
-            tmem_row_to_tile<8>(taddr + 0, sm + R_PKG + PKG_B0, PKG_BK, row);
-        } else if (role == 1) {     // Q'[t][c] = Q^g[t][c] - (P W)^T[c][t] -> B rows 128 + t
-            const uint32_t c = row, kb = c >> 6, cc = c & 63;
+        // ---- the package image, staged in shared memory
+        {
+            const int lane_base = 32 * (warp & 3);
+            const uint32_t row = lane_base + lane;
+            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
+            const int role = warp >> 2;
+            if (role == 0) {            // N[c][c' < 64] -> B rows c, K-block 0
+                tmem_row_to_tile<4>(taddr + 0, sm + R_PKG + PKG_B0, 0, row);
+            } else if (role == 1) {     // N[c][c' >= 64] -> B rows c, K-block 1
+                tmem_row_to_tile<4>(taddr + 64, sm + R_PKG + PKG_B0 + PKG_BK, 0, row);
+            } else if (role == 2) {     // X^T[j][c] -> two K-blocks
+                tmem_row_to_tile<8>(taddr + 128, sm + R_PKG + PKG_XT, 16384, row);
+            } else {                    // O'^T[j][t] -> one K-block
+                tmem_row_to_tile<4>(taddr + 256, sm + R_PKG + PKG_OT, 0, row);
+            }
+            // Q'[t][c] = Q^g[t][c] - (P W)[t][c] -> B rows 128 + t; lanes 0..63 hold rows t.
+            if ((warp & 3) < 2 && role < 2) {
+                const uint32_t t = row, kb = (uint32_t)role;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float pw[16];
-                tmem_ld16(taddr + 320 + 16 * q4, pw);
-                tmem_wait_ld();
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float pw[16];
+                    tmem_ld16(taddr + 320 + 64 * kb + 16 * q4, pw);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint32_t t = 16 * q4 + e;
-                    const float qg = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                        sm + R_QG + kb * 8192 + sw128(t, cc >> 3) + (cc & 7) * 2));
-                    *reinterpret_cast<__nv_bfloat16*>(sm + R_PKG + PKG_B0 + kb * PKG_BK +
-                                                      sw128(128 + t, cc >> 3) + (cc & 7) * 2) =
-                        __float2bfloat16_rn(qg - pw[e]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t ch = 2 * q4 + hh;
+                        float qg[8], o8[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + R_QG + kb * 8192 + sw128(t, ch)), qg);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o8[e] = qg[e] - pw[8 * hh + e];
+                        *reinterpret_cast<uint4*>(sm + R_PKG + PKG_B0 + kb * PKG_BK +
+                                                  sw128(128 + t, ch)) = pack8(o8);
+                    }
                 }
             }
-        } else if (role == 2) {     // X^T[j][c] -> two K-blocks
-            tmem_row_to_tile<8>(taddr + 128, sm + R_PKG + PKG_XT, 16384, row);
-        } else {                    // O'^T[j][t] -> one K-block
-            tmem_row_to_tile<4>(taddr + 256, sm + R_PKG + PKG_OT, 0, row);
+            if (tid < 128)
+                reinterpret_cast<float*>(sm + R_PKG + PKG_LAM)[tid] = small[SM_LAM + tid];
         }
-        if (tid < 128)
-            reinterpret_cast<float*>(sm + R_PKG + PKG_LAM)[tid] = small[SM_LAM + tid];
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(pkg, sm + R_PKG, 49152);
+            bulk_s2g(pkg + 49152, sm + R_PKG + 49152, PKG_BYTES - 49152);
+            bulk_commit();
+        }
+        item = nitem;
+        t0 = nt0;
+        len = nlen;
     }
     if (!ok) set_status(status, kErrPrepWait);
-    fence_async_smem();
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(pkg, sm + R_PKG, 49152);
-        bulk_s2g(pkg + 49152, sm + R_PKG + 49152, PKG_BYTES - 49152);
-        bulk_commit();
-        bulk_wait_all();
-    }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
@@ -838,7 +926,7 @@ size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0, float* S1,
                            const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                           void* workspace, cudaStream_t stream, int /*num_sms*/) {
+                           void* workspace, cudaStream_t stream, int num_sms) {
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -862,10 +950,11 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     profile_event(0, stream);
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     if (T_total > 0) {
-        dim3 grid_p((unsigned)slots, (unsigned)H);
-        tc::chunk_prep_kernel<<<grid_p, tc::kPrepThreads, tc::P_SMEM, stream>>>(
+        const int64_t n_items = slots * H;
+        const int64_t grid = n_items < num_sms ? n_items : num_sms;
+        tc::chunk_prep_kernel<<<(unsigned)grid, tc::kPrepThreads, tc::P_SMEM, stream>>>(
             static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-            static_cast<const bf*>(z), static_cast<const bf*>(beta), A, ws, map, H);
+            static_cast<const bf*>(z), static_cast<const bf*>(beta), A, ws, map, H, n_items);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
