@@ -8,7 +8,8 @@
 namespace kda {
 
 // Lower bound of the per-channel log-decay: g = g_min * sigmoid(exp(A) * z)
-// with g_min = -5 ("How Kimi K3 is built", forget-coefficient parametrisation).
+// with g_min = -5 ("How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens",
+// section "Sequence: three KDA to one global MLA").
 // The chunked kernels rely on it: across 16 tokens the decay spans at most
 // e^80, inside the fp32/bf16 exponent range.
 constexpr float kGMin = -5.0f;

@@ -6,9 +6,12 @@
 //   S  <- S' + k u^T                                  (= (I - b k k^T) S' + b k v^T)
 //   o  = S'^T q + u (k^T q)                           (= S_new^T q)
 //
-// The recurrence is the delta rule of "Kimi K3 architecture review" with the
-// gate of "How Kimi K3 is built"; the pages note that reading the large state
-// is what a decode step costs, so this kernel is built around one pass over S.
+// The recurrence is the delta rule of "Kimi K3 architecture: how an open model with a million-token context competes with market leaders"
+// (section "How the Kimi K3 architecture holds a million tokens of context") with
+// the gate of "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens"
+// (section "Sequence: three KDA to one global MLA").  The same page notes, in
+// "How to serve two different caches", that reading the large recurrent state
+// is what decoding costs, so this kernel is built around one pass over S.
 //
 // Design (HBM-bound; > 99% of the bytes are the fp32 state):
 //   one CTA of 256 threads per (b, h); warp w owns the 16-column slab

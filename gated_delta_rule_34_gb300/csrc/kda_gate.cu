@@ -2,7 +2,8 @@
 //
 //   g[t, h, c] = clamp(-5 * sigmoid(exp(A[h, c]) * z[t, h, c]), -5, 0)
 //
-// "How Kimi K3 is built", forget-coefficient parametrisation (g_min = -5).
+// "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens",
+// section "Sequence: three KDA to one global MLA" (g_min = -5).
 // Memory-bound: 2 (bf16) or 4 (fp32) bytes in and 4 bytes out per element.
 // Each thread handles one 16-byte vector of z when d_k allows it, so loads
 // and stores are 128-bit and fully coalesced.

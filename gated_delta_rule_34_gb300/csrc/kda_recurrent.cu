@@ -2,8 +2,10 @@
 //
 // The path for fp32 inputs (tf32 tensor cores cannot meet a 1e-4 relative
 // bound) and for head sizes the tensor-core path does not cover.  It runs the
-// delta rule of "Kimi K3 architecture review" with the per-channel gate of
-// "How Kimi K3 is built" exactly as written, one token after another:
+// delta rule of "Kimi K3 architecture: how an open model with a million-token context competes with market leaders"
+// (section "How the Kimi K3 architecture holds a million tokens of context") with the
+// per-channel gate of "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens"
+// (section "Sequence: three KDA to one global MLA") exactly as written, token by token:
 //
 //   S' = Diag(a_t) S,  u = b_t (v_t - S'^T k_t),  S <- S' + k_t u^T,
 //   o_t = S'^T q_t + u (k_t^T q_t)

@@ -8,12 +8,15 @@
  *   S_t   = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T
  *   o_t   = S_t^T q_t
  *
- * Sources: the gate is the forget-coefficient parametrisation of "How Kimi K3
- * is built" (g = g_min*sigmoid(exp(A)*z), alpha = exp(g), g_min = -5); the
- * state update is the delta rule of "Kimi K3 architecture review" (section on
- * holding a million tokens of context: a fixed state that each token partly
- * erases and then writes, beta the write strength, alpha the forget factor,
- * alpha bounded to [e^-5, 1]); the per-channel forget gate is from both.
+ * Sources: the gate is the forget-coefficient parametrisation of
+ * "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens",
+ * section "Sequence: three KDA to one global MLA" (g = g_min*sigmoid(exp(A)*z),
+ * alpha = exp(g), g_min = -5).  The state update is the delta rule of
+ * "Kimi K3 architecture: how an open model with a million-token context competes with market leaders",
+ * section "How the Kimi K3 architecture holds a million tokens of context": a
+ * fixed state that each token partly erases and then writes, beta the write
+ * strength, alpha the forget factor, alpha bounded to [e^-5, 1].  Both pages
+ * make the forget gate per channel.
  *
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers owned by the caller, unless stated.
@@ -71,7 +74,7 @@ const char *kda_last_error(void);
 /*
  * kda_gate -- the forget gate on its own.
  *   g[t, h, c] = clamp(-5 * sigmoid(exp(A[h, c]) * z[t, h, c]), -5, 0)   (fp32 out)
- * Defined by the gate formula of "How Kimi K3 is built" (g_min = -5); the clamp
+ * Defined by the gate formula of the first page above (g_min = -5); the clamp
  * only guards the rounding of sigmoid and never moves an exact value.
  *   z        [n_tokens, H, d_k] in z_dtype
  *   A        [H, d_k] fp32
@@ -85,9 +88,9 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
 /*
  * kda_chunk_prefill -- o and (optionally) the final state for a batch of
  * sequences, by the chunked form: tokens of one chunk in parallel, then the
- * state passed from chunk to chunk ("Kimi K3 architecture review", chip-level
- * FlashKDA section; the g_min bound that keeps every causal block a dense
- * product is from "How Kimi K3 is built").
+ * state passed from chunk to chunk (second page above, section "Chip level:
+ * the specialised FlashKDA kernel"; the g_min bound that keeps every causal
+ * block a dense product is from the first page, same section as the gate).
  *
  * Fixed-length batch: cu_seqlens == NULL, inputs [B, T, H, d], N = B = n_seqs.
  * Packed batch:       cu_seqlens != NULL (device int32 [n_seqs + 1], rising
@@ -126,8 +129,9 @@ kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype d
 
 /*
  * kda_decode_step -- one token for each of B independent sequences, updating
- * the state in place (the fixed-size state replaces a KV cache; "How Kimi K3
- * is built" notes that reading this state is the cost of decoding):
+ * the state in place.  The fixed-size state replaces a KV cache, and the first
+ * page above notes, in "How to serve two different caches", that reading this
+ * state is the cost of decoding:
  *   S' = Diag(a) S,  u = b (v - S'^T k),  S <- S' + k u^T,  o = S'^T q + u (k^T q)
  * which equals o = S_new^T q.
  *   q, k, z  [B, H, d_k];  v, o [B, H, d_v];  beta [B, H]  (dtype)

@@ -6,11 +6,12 @@ library and never imports it; the two meet only in the seeded input
 generator, which holds none of the layer's arithmetic.
 
 Contents
-  gate(z, A)            g = -5 * sigmoid(exp(A) * z), fp64 ("How Kimi K3 is built",
-                        forget-coefficient parametrisation).
-  recurrent(...)        the delta-rule recurrence token by token in fp64
-                        (kda_oracle.c; "Kimi K3 architecture review", delta-rule
-                        state update; "How Kimi K3 is built", channel-wise gate).
+  gate(z, A)            g = -5 * sigmoid(exp(A) * z), fp64 ("How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens",
+                        section "Sequence: three KDA to one global MLA").
+  recurrent(...)        the delta-rule recurrence token by token in fp64 (kda_oracle.c;
+                        the state update of "Kimi K3 architecture: how an open model with a million-token context competes with market leaders",
+                        section "How the Kimi K3 architecture holds a million tokens of
+                        context", with the channel-wise gate of the page above).
   chunked(...)          an independently written chunked form (oracle/chunked.py)
                         used to cross-check the recurrence.
 

@@ -3,9 +3,10 @@
 TEST INFRASTRUCTURE ONLY: it exists to cross-check the token-by-token oracle.
 
 The pages say the kernel runs the tokens of one chunk in parallel and then
-passes the state on ("Kimi K3 architecture review", section "Chip level: the
-FlashKDA kernel") but print no equations, so the algebra here is derived
-directly from the recurrence S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,
+passes the state on ("Kimi K3 architecture: how an open model with a
+million-token context competes with market leaders", section "Chip level: the
+specialised FlashKDA kernel") but print no equations, so the algebra here is
+derived directly from the recurrence S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,
 o_t = S_t^T q_t.  Inside a chunk with start state S0 and G_t = sum_{s<=t} g_s
 (per channel, cumulative log-decay from the chunk start):
 
@@ -26,7 +27,11 @@ import numpy as np
 
 
 def _gate64(z: np.ndarray, A: np.ndarray) -> np.ndarray:
-    """g = -5 * sigmoid(exp(A) * z) in fp64 ("How Kimi K3 is built", gate parametrisation)."""
+    """g = -5 * sigmoid(exp(A) * z) in fp64.
+
+    "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents
+    for a million tokens", section "Sequence: three KDA to one global MLA".
+    """
     x = np.exp(A) * z
     with np.errstate(over="ignore"):
         return -5.0 / (1.0 + np.exp(-x))

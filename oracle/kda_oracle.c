@@ -9,20 +9,22 @@
  * What it computes (plain definitions, no blocking, no reordering):
  *
  *   gate   g_t = g_min * sigmoid(exp(A) (.) z_t),  g_min = -5,  alpha_t = exp(g_t)
- *          -- "How Kimi K3 is built", section on the forget-coefficient
- *             parametrisation (g = g_min*sigmoid(exp(A)*z), alpha = exp(g),
- *             g_min = -5); the bound alpha in [e^-5, 1] is restated in
- *             "Kimi K3 architecture review", section "How the architecture
- *             holds a million tokens of context".
+ *          -- "How Kimi K3 is built: 2.8 trillion parameters, linear attention
+ *             and agents for a million tokens", section "Sequence: three KDA to
+ *             one global MLA"; the bound alpha in [e^-5, 1] is restated in
+ *             "Kimi K3 architecture: how an open model with a million-token
+ *             context competes with market leaders", section "How the Kimi K3
+ *             architecture holds a million tokens of context".
  *
  *   state  S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
  *   output o_t = S_t^T q_t
- *          -- the delta rule of "Kimi K3 architecture review" (fixed state S,
- *             each token partially erases and then writes; beta = write
- *             strength, alpha = forget factor applied before the write) with a
- *             per-channel forget gate ("How Kimi K3 is built": channel-wise
- *             forget coefficient kept before the new write).  Decay first,
- *             then erase, then write; o_t reads the state after the update.
+ *          -- the delta rule of the second page above, same section (a fixed
+ *             state S that each token partially erases and then writes; beta =
+ *             write strength, alpha = forget factor applied before the write),
+ *             with the per-channel forget gate of the first page above (the
+ *             channel-wise coefficient decides what is kept before the write).
+ *             Decay first, then erase, then write; o_t reads the state after
+ *             the update.
  *
  * Per (sequence, head) the recurrence is evaluated token by token in fp64.
  * Inputs are read in their stored type (fp32 or bf16) and converted exactly to

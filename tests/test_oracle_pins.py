@@ -246,7 +246,8 @@ def test_segment_split_equals_whole():
 
 def test_state_dependence_is_affine():
     # run(S0, x) = M S0 + run(0, x) for a linear M (the segment pair of the
-    # context-parallel decomposition in "How Kimi K3 is built").
+    # context-parallel decomposition: each segment is a pair of an accumulated
+    # transformation and a state built from zero, per the page "How Kimi K3 is built: 2.8 trillion para...").
     c = _rand_case(30, 5, 4, seed=8)
     args = [c[n] for n in ("q", "k", "v", "z", "beta")]
     Sa = c["S0"]
