@@ -44,6 +44,7 @@
 // rows.  All exponents are block-local: L_t = G_t - r_{b(t)} comes from a
 // 16-token scan, and the block references only enter through per-channel
 // factors e^{r_i - r_b}, e^{r_b}, e^{G_C - r_b}.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "kda_common.cuh"
@@ -93,11 +94,11 @@ constexpr uint32_t R_QG = 198656;      // Q^g      [64 t][128 c] swizzled, two K
 constexpr uint32_t R_SMALL = 215040;   // per-channel constants, beta
 constexpr uint32_t R_ZQ = R_G;         // raw z [64][128] bf16, then raw q, of the next item
 // reuse after the A/P products
-constexpr uint32_t R_AF = 0;           // A fp32 [64][65]
-constexpr uint32_t R_TF = 16896;       // T fp32 [64][65]
+constexpr uint32_t R_AF = 0;           // A fp32 [64][68]
+constexpr uint32_t R_TF = 17408;       // T fp32 [64][68]
 constexpr uint32_t R_TB = 34816;       // T bf16 [64][64] swizzled
 constexpr uint32_t R_XS = 43008;       // solve scratch [3][16][16] fp32
-constexpr uint32_t F_LD = 65;
+constexpr uint32_t F_LD = 68;           // fp32 row stride: 16-byte aligned rows, 4-bank skew
 // reuse after W / U~ (the solve's buffers and the A/P operands are dead)
 constexpr uint32_t R_WT = 0;           // W^T  [128 c][64 s] swizzled
 constexpr uint32_t R_UT = 16384;       // U~^T [128 j][64 s] swizzled
@@ -111,6 +112,7 @@ constexpr uint32_t SM_LAM = 2304;      // [128] e^{G_C}
 constexpr uint32_t SM_B = 2432;        // [64] beta
 constexpr uint32_t SM_A = 2496;        // [128] A row of the next item (prefetched)
 constexpr uint32_t R_SMALL_BYTES = (2496 + 128) * 4;
+constexpr uint32_t kInputBytes = 4 * 16384 + 512;    // q, k, v, z tiles and the A row
 constexpr uint32_t R_BAR = R_SMALL + R_SMALL_BYTES;
 constexpr uint32_t P_SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
 
@@ -221,35 +223,44 @@ __device__ __forceinline__ void solve_offdiag(const float* __restrict__ Af, floa
     if (tid < kItems) {
         const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const int jb = p, ib = p + d;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int mm = 0; mm < d; ++mm) {
             const int m = jb + mm;
+            float a[16];
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+                const float4 av = *reinterpret_cast<const float4*>(Af + (16 * ib + r) * F_LD + 16 * m + 4 * e4);
+                a[4 * e4] = av.x; a[4 * e4 + 1] = av.y; a[4 * e4 + 2] = av.z; a[4 * e4 + 3] = av.w;
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const float a = Af[(16 * ib + r) * F_LD + 16 * m + e];
-                const float* tr = Tf + (16 * m + e) * F_LD + 16 * jb + c4;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) acc[cc] = fmaf(a, tr[cc], acc[cc]);
+                const float4 tv = *reinterpret_cast<const float4*>(Tf + (16 * m + e) * F_LD + 16 * jb + c4);
+                acc.x = fmaf(a[e], tv.x, acc.x); acc.y = fmaf(a[e], tv.y, acc.y);
+                acc.z = fmaf(a[e], tv.z, acc.z); acc.w = fmaf(a[e], tv.w, acc.w);
             }
         }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) Xs[(p * 16 + r) * 16 + c4 + cc] = acc[cc];
+        *reinterpret_cast<float4*>(Xs + (p * 16 + r) * 16 + c4) = acc;
     }
     __syncthreads();
     if (tid < kItems) {
         const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
         const int jb = p, ib = p + d;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float tr[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 tv = *reinterpret_cast<const float4*>(Tf + (16 * ib + r) * F_LD + 16 * ib + 4 * e4);
+            tr[4 * e4] = tv.x; tr[4 * e4 + 1] = tv.y; tr[4 * e4 + 2] = tv.z; tr[4 * e4 + 3] = tv.w;
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            const float tv = Tf[(16 * ib + r) * F_LD + 16 * ib + e];
-            const float* xr = Xs + (p * 16 + e) * 16 + c4;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) acc[cc] = fmaf(tv, xr[cc], acc[cc]);
+            const float4 xv = *reinterpret_cast<const float4*>(Xs + (p * 16 + e) * 16 + c4);
+            acc.x = fmaf(tr[e], xv.x, acc.x); acc.y = fmaf(tr[e], xv.y, acc.y);
+            acc.z = fmaf(tr[e], xv.z, acc.z); acc.w = fmaf(tr[e], xv.w, acc.w);
         }
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) Tf[(16 * ib + r) * F_LD + 16 * jb + c4 + cc] = -acc[cc];
+        *reinterpret_cast<float4*>(Tf + (16 * ib + r) * F_LD + 16 * jb + c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
 }
@@ -284,9 +295,15 @@ __device__ __forceinline__ void emit_block_row(uint32_t taddr_lane, bool mine, b
     if (!mine) return;
     if (key_rows) {
 #pragma unroll
-        for (int s = 0; s < 64; ++s) {
-            const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
-            Af[t * F_LD + s] = (s < t) ? bt * val : 0.f;
+        for (int s4 = 0; s4 < 16; ++s4) {
+            float o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = 4 * s4 + e;
+                const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
+                o4[e] = (s < t) ? bt * val : 0.f;
+            }
+            *reinterpret_cast<float4*>(Af + t * F_LD + 4 * s4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
     } else {
 #pragma unroll
@@ -303,28 +320,30 @@ __device__ __forceinline__ void emit_block_row(uint32_t taddr_lane, bool mine, b
     }
 }
 
-// Issues the loads of one item's inputs: raw k, v (to R_K, R_V), z, q (to
-// R_ZQ) and the A row (to SM_A) as 16-byte async copies with zero fill past
-// `len`, plus beta into a register of threads < 64.  Completed by
-// cp_async_wait_all() in the item that consumes them.
-__device__ __forceinline__ void issue_item_loads(
-    uint8_t* sm, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
-    const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A, int64_t t0, int len,
-    int h, int H, int tid, float& bt_reg) {
-    const size_t row0 = ((size_t)t0 * H + h) * kD;
-    const size_t rstride = (size_t)H * kD;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int i = it * kPrepThreads + tid;       // 0..4095
-        const int which = i >> 10, t = (i >> 4) & 63, ch = i & 15;
-        const __nv_bfloat16* base = which == 0 ? k : which == 1 ? v : which == 2 ? z : q;
-        const uint32_t dst = which == 0 ? R_K : which == 1 ? R_V : which == 2 ? R_ZQ : R_ZQ + 16384;
-        cp_async16(sm + dst + t * 256 + ch * 16,
-                   base + row0 + (size_t)(t < len ? t : 0) * rstride + ch * 8, t < len ? 16u : 0u);
+// Input tensor maps: q, k, v, z as 3-D tensors [T_total][H][128] bf16 with
+// boxes of 64 tokens x 1 head x 128 channels (16 KB, rows at 256-byte pitch
+// in shared memory); boxes past the last token read zeros.
+struct InputMaps {
+    CUtensorMap q, k, v, z;
+};
+
+// Issues the loads of one item's inputs: q, k, v, z tiles by TMA and the A row
+// by a bulk copy, all completing on `inbar`; beta into a register of threads
+// < 64.  Rows past the item's `len` belong to the next sequence (or are zero);
+// the consumers mask them.
+__device__ __forceinline__ void issue_item_loads(uint8_t* sm, const InputMaps& maps,
+                                                 const __nv_bfloat16* __restrict__ beta,
+                                                 const float* __restrict__ A, int64_t t0, int len,
+                                                 int h, int H, int tid, uint64_t* inbar,
+                                                 float& bt_reg) {
+    if (tid == 0) {
+        mbar_expect_tx(inbar, kInputBytes);
+        tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
+        tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, inbar);
+        tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, inbar);
+        tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
+        bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
     }
-    if (tid < 32)
-        cp_async16(sm + R_SMALL + SM_A * 4 + tid * 16, A + (size_t)h * kD + tid * 4, 16u);
     bt_reg = 0.f;
     if (tid < kC && tid < len) bt_reg = __bfloat162float(beta[(size_t)(t0 + tid) * H + h]);
 }
@@ -334,10 +353,9 @@ __device__ __forceinline__ void issue_item_loads(
 // blockIdx.x, blockIdx.x + gridDim.x, ... with item = slot * H + head.
 // ============================================================================
 __global__ void __launch_bounds__(kPrepThreads, 1)
-chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
-                  const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
-                  uint8_t* __restrict__ ws, SeqMap map, int H, int64_t n_items) {
+chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* __restrict__ beta,
+                  const float* __restrict__ A, uint8_t* __restrict__ ws, SeqMap map, int H,
+                  int64_t n_items) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -345,12 +363,14 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     float* G = reinterpret_cast<float*>(sm + R_G);
     float* small = reinterpret_cast<float*>(sm + R_SMALL);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 8);
+    uint64_t* inbar = bar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 16);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
 
     if (warp == 0) tmem_alloc<512>(tslot);
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(inbar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -358,6 +378,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     tc_fence_after();
     const uint32_t tbase = *tslot;
     uint32_t phase = 0;                      // parity of the next completion of `bar`
+    uint32_t in_phase = 0;                   // parity of the next completion of `inbar`
     bool ok = true;
     const int c8 = tid & 15;                 // channels 8 c8 .. 8 c8 + 7 in the row-side passes
 
@@ -368,7 +389,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     float bt_reg = 0.f;
     while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
     if (item < n_items)
-        issue_item_loads(sm, q, k, v, z, beta, A, t0, len, (int)(item % H), H, tid, bt_reg);
+        issue_item_loads(sm, maps, beta, A, t0, len, (int)(item % H), H, tid, inbar, bt_reg);
 
     while (item < n_items) {
         const int h = (int)(item % H);
@@ -379,15 +400,19 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         while (nitem < n_items && !slot_chunk(map, nitem / H, nt0, nlen)) nitem += gridDim.x;
 
         // ---- inputs of this item (issued during the previous one) -> registers
-        cp_async_wait_all();
+        ok = mbar_wait(inbar, in_phase) && ok;
+        in_phase ^= 1u;
         __syncthreads();
         int tt[2];
         uint4 zraw[2], qraw[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             tt[it] = it * 32 + (tid >> 4);
-            zraw[it] = *reinterpret_cast<const uint4*>(sm + R_ZQ + tt[it] * 256 + c8 * 16);
-            qraw[it] = *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16);
+            const bool in = tt[it] < len;
+            zraw[it] = in ? *reinterpret_cast<const uint4*>(sm + R_ZQ + tt[it] * 256 + c8 * 16)
+                          : make_uint4(0, 0, 0, 0);
+            qraw[it] = in ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
+                          : make_uint4(0, 0, 0, 0);
         }
         float eA[8];
         {
@@ -463,7 +488,8 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], o8[8];
                 load8f(G + t * G_LD + c8 * 8, Lt);
                 load8f(small + SM_ER + b * 128 + c8 * 8, er);
-                unpack8(*reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16), kf);
+                unpack8(t < len ? *reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16)
+                                : make_uint4(0, 0, 0, 0), kf);
                 unpack8(qraw[it], qf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -536,11 +562,11 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 for (int e = 0; e < 8; ++e) {
                     const int s = s8 * 8 + e;
                     const float bs = small[SM_B + s];
-                    const float kf = __bfloat162float(kraw[s * kD + c]);
+                    const float kf = s < len ? __bfloat162float(kraw[s * kD + c]) : 0.f;
                     const float E = G[s * G_LD + c];
                     bk[e] = bs * kf * E * er;                  // b_s k_s e^{G_s}
                     kc[e] = kf * ec * __fdividef(1.0f, E);     // k_s e^{G_C - G_s}
-                    bv[e] = bs * __bfloat162float(vraw[s * kD + c]);
+                    bv[e] = s < len ? bs * __bfloat162float(vraw[s * kD + c]) : 0.f;
                 }
                 *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
                 *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
@@ -572,7 +598,8 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         __syncthreads();
         // Raw k, v and G are dead now: start loading the next item's inputs.
         if (nitem < n_items)
-            issue_item_loads(sm, q, k, v, z, beta, A, nt0, nlen, (int)(nitem % H), H, tid, bt_reg);
+            issue_item_loads(sm, maps, beta, A, nt0, nlen, (int)(nitem % H), H, tid, inbar,
+                             bt_reg);
 
         // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution,
         //      then the off-diagonal blocks by distance.
@@ -588,13 +615,19 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
+                    float a[16];
+#pragma unroll
+                    for (int e4 = 0; e4 < (r + 3) / 4; ++e4) {
+                        const float4 av = *reinterpret_cast<const float4*>(Ab + r * F_LD + 4 * e4);
+                        a[4 * e4] = av.x; a[4 * e4 + 1] = av.y; a[4 * e4 + 2] = av.z; a[4 * e4 + 3] = av.w;
+                    }
                     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                     for (int m = 0; m + 1 < r; m += 2) {
-                        a0 = fmaf(Ab[r * F_LD + m], x[m], a0);
-                        a1 = fmaf(Ab[r * F_LD + m + 1], x[m + 1], a1);
+                        a0 = fmaf(a[m], x[m], a0);
+                        a1 = fmaf(a[m + 1], x[m + 1], a1);
                     }
-                    if (r & 1) a0 = fmaf(Ab[r * F_LD + r - 1], x[r - 1], a0);
+                    if (r & 1) a0 = fmaf(a[r - 1], x[r - 1], a0);
                     x[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
                 }
 #pragma unroll
@@ -608,11 +641,10 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             {
                 const int t = tid >> 3, ch = tid & 7;
                 float o8[8];
+                load8f(Tf + t * F_LD + ch * 8, o8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = ch * 8 + e;
-                    o8[e] = (s <= t) ? Tf[t * F_LD + s] : 0.f;
-                }
+                for (int e = 0; e < 8; ++e)
+                    if (ch * 8 + e > t) o8[e] = 0.f;
                 *reinterpret_cast<uint4*>(sm + R_TB + sw128(t, ch)) = pack8(o8);
             }
         }
@@ -918,6 +950,18 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
 
 }  // namespace tc
 
+// Tensor map of one [T_total][H][128] bf16 input with 64 x 1 x 128 boxes.
+static CUresult make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
+    cuuint32_t box[3] = {128, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     return tc::WS_HEADER + (size_t)slots * H * tc::PKG_BYTES;
@@ -950,11 +994,16 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     profile_event(0, stream);
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     if (T_total > 0) {
+        tc::InputMaps maps;
+        if (make_input_map(&maps.q, q, T_total, H) != CUDA_SUCCESS ||
+            make_input_map(&maps.k, k, T_total, H) != CUDA_SUCCESS ||
+            make_input_map(&maps.v, v, T_total, H) != CUDA_SUCCESS ||
+            make_input_map(&maps.z, z, T_total, H) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
         const int64_t n_items = slots * H;
         const int64_t grid = n_items < num_sms ? n_items : num_sms;
         tc::chunk_prep_kernel<<<(unsigned)grid, tc::kPrepThreads, tc::P_SMEM, stream>>>(
-            static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-            static_cast<const bf*>(z), static_cast<const bf*>(beta), A, ws, map, H, n_items);
+            maps, static_cast<const bf*>(beta), A, ws, map, H, n_items);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

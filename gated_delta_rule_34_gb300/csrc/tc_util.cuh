@@ -70,6 +70,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32
         : "memory");
 }
 
+// Tiled TMA load of a 3-D box described by a tensor map (kernel parameter
+// declared const __grid_constant__) into shared memory; completion counted on
+// `bar` in bytes.  Coordinates are in elements, innermost first; boxes that
+// reach past the tensor's end are zero-filled.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Asks L2 to fetch [src, src + bytes) ahead of a later bulk copy (16-byte
 // aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
