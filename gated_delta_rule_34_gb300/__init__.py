@@ -7,7 +7,7 @@ The binding loads ``_build/libkda.so`` on first use (build it with
 nothing, so the seeded input generator (``.inputs``) can be used without a GPU.
 """
 from .api import (KDAError, chunk_prefill, decode_step, gate, lib, library_path,  # noqa: F401
-                  prefill_path, set_profile_events, workspace_size)
+                  prefill_path, set_profile_events, spec_commit, spec_verify, workspace_size)
 
 __all__ = ["KDAError", "chunk_prefill", "decode_step", "gate", "lib", "library_path",
-           "prefill_path", "set_profile_events", "workspace_size"]
+           "prefill_path", "set_profile_events", "spec_commit", "spec_verify", "workspace_size"]

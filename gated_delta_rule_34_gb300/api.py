@@ -44,6 +44,10 @@ def _declare(lib):
     lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
                                       i32, i32, i32, i32, i32, vp, sz, vp]
     lib.kda_chunk_prefill.restype = i32
+    lib.kda_chunk_prefill_checkpoints.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                  i32, i64, i32, i32, i32, i32, i32, vp, i64, i32,
+                                                  vp, sz, vp]
+    lib.kda_chunk_prefill_checkpoints.restype = i32
     lib.kda_chunk_prefill_workspace_size.argtypes = [i32, i32, i64, i32, i32, i32, i32, i32]
     lib.kda_chunk_prefill_workspace_size.restype = sz
     lib.kda_chunk_prefill_path.argtypes = [i32, i32, i32, i32]
@@ -54,6 +58,11 @@ def _declare(lib):
                                                        i32, i32, i64, i32, i32, i32, i32, i32,
                                                        vp]
     lib.kda_chunk_prefill_static_workspace.restype = i32
+    lib.kda_spec_verify.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                    vp]
+    lib.kda_spec_verify.restype = i32
+    lib.kda_spec_commit.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_spec_commit.restype = i32
     lib.kda_set_profile_events.argtypes = [vp, i32]
     lib.kda_set_profile_events.restype = i32
     return lib
@@ -126,14 +135,17 @@ def workspace_size(n_seqs: int, B: int, T: int, H: int, d_k: int, d_v: int, chun
 
 
 def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chunk: int = 64,
-                  output_final_state: bool = True, out=None, final_state=None, workspace=None):
+                  output_final_state: bool = True, out=None, final_state=None, workspace=None,
+                  checkpoints=None, checkpoint_every: int = 0):
     """Prefill through kda_chunk_prefill.
 
     q, k, z: [B, T, H, d_k]; v: [B, T, H, d_v]; beta: [B, T, H] (one dtype, fp32 or bf16);
     A: [H, d_k] fp32; initial_state: [N, H, d_k, d_v] fp32 or None; cu_seqlens: int32
     [N + 1] on the device for a packed batch (then B must be 1).
     Returns (o, final_state or None).  A workspace of the required size is allocated
-    with torch if none is given.
+    with torch if none is given.  With ``checkpoints`` (fp32 [N, H, n_slots, d_k, d_v])
+    the state after every ``checkpoint_every`` tokens of each sequence is written too
+    (kda_chunk_prefill_checkpoints).
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -149,12 +161,22 @@ def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chun
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
-    _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, cu_seqlens, workspace)
+    _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, cu_seqlens, workspace,
+               checkpoints)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().kda_chunk_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
-        _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
-        _dtype_code(q.dtype), _ptr(workspace), ws_bytes, _stream(q.device)))
+    if checkpoints is None:
+        _check(lib().kda_chunk_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
+            chunk, _dtype_code(q.dtype), _ptr(workspace), ws_bytes, _stream(q.device)))
+    else:
+        if checkpoints.dtype != torch.float32 or checkpoints.dim() != 5:
+            raise ValueError("checkpoints must be fp32 [N, H, max_checkpoints, d_k, d_v]")
+        _check(lib().kda_chunk_prefill_checkpoints(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
+            chunk, _dtype_code(q.dtype), _ptr(checkpoints), int(checkpoint_every),
+            checkpoints.shape[2], _ptr(workspace), ws_bytes, _stream(q.device)))
     return out, final_state
 
 
@@ -205,3 +227,32 @@ def chunk_prefill_static_workspace(q, k, v, z, beta, A, initial_state=None, cu_s
         _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
         _dtype_code(q.dtype), _stream(q.device)))
     return out, final_state
+
+
+def spec_verify(q, k, v, z, beta, A, state, out=None):
+    """Outputs of T draft tokens per sequence from ``state`` (not modified).
+
+    q, k, z: [B, T, H, d_k]; v: [B, T, H, d_v]; beta: [B, T, H]; state [B, H, d_k, d_v].
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, z, beta, A, state, out)
+    _check(lib().kda_spec_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                 _ptr(state), _ptr(out), B, T, H, dk, dv, _dtype_code(q.dtype),
+                                 _stream(q.device)))
+    return out
+
+
+def spec_commit(k, v, z, beta, A, state, n_accept):
+    """Advances ``state`` in place by the first n_accept[b] draft tokens of each sequence."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if n_accept.dtype != torch.int32:
+        raise TypeError("n_accept must be int32")
+    _need_cuda(k, v, z, beta, A, state, n_accept)
+    _check(lib().kda_spec_commit(_ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state),
+                                 _ptr(n_accept), B, T, H, dk, dv, _dtype_code(k.dtype),
+                                 _stream(k.device)))
+    return state

@@ -65,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     if force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"]
+        cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

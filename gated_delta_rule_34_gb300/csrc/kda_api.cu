@@ -126,12 +126,13 @@ size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int
     return kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * T, H);
 }
 
-kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* z,
-                             const void* beta, const float* A, void* o,
-                             const float* initial_state, float* final_state,
-                             const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
-                             int d_k, int d_v, int chunk, kda_dtype dtype, void* workspace,
-                             size_t workspace_bytes, cudaStream_t stream) {
+static kda_status prefill_impl(const void* q, const void* k, const void* v, const void* z,
+                               const void* beta, const float* A, void* o,
+                               const float* initial_state, float* final_state,
+                               const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                               int d_k, int d_v, int chunk, kda_dtype dtype, void* workspace,
+                               size_t workspace_bytes, const kda::CheckpointSpec& ck,
+                               cudaStream_t stream) {
     if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B <= 0 || T < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || n_seqs <= 0)
         return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%lld H=%d d_k=%d d_v=%d n_seqs=%d", B,
@@ -176,15 +177,55 @@ kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const 
         }
         return cuda_status(kda::run_chunked_tc(q, k, v, z, beta, A, o, initial_state,
                                                final_state, cu_seqlens, n_seqs, T, T_total, H,
-                                               workspace, stream, device_sm_count()),
+                                               workspace, ck, stream, device_sm_count()),
                            "kda_chunk_prefill (chunked tensor-core path)");
     }
     kda::profile_event(0, stream);
     const cudaError_t e = kda::run_recurrent(q, k, v, z, beta, A, o, initial_state, final_state,
                                              cu_seqlens, n_seqs, T, T_total, H, d_k, d_v, bf16,
-                                             stream);
+                                             ck, stream);
     kda::profile_event(1, stream);
     return cuda_status(e, "kda_chunk_prefill (recurrent path)");
+}
+
+kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const void* z,
+                             const void* beta, const float* A, void* o,
+                             const float* initial_state, float* final_state,
+                             const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
+                             int d_k, int d_v, int chunk, kda_dtype dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    return prefill_impl(q, k, v, z, beta, A, o, initial_state, final_state, cu_seqlens, n_seqs, B,
+                        T, H, d_k, d_v, chunk, dtype, workspace, workspace_bytes,
+                        kda::CheckpointSpec{}, stream);
+}
+
+kda_status kda_chunk_prefill_checkpoints(const void* q, const void* k, const void* v,
+                                         const void* z, const void* beta, const float* A, void* o,
+                                         const float* initial_state, float* final_state,
+                                         const int32_t* cu_seqlens, int n_seqs, int B, int64_t T,
+                                         int H, int d_k, int d_v, int chunk, kda_dtype dtype,
+                                         float* checkpoints, int64_t checkpoint_every,
+                                         int max_checkpoints, void* workspace,
+                                         size_t workspace_bytes, cudaStream_t stream) {
+    kda::CheckpointSpec ck;
+    if (checkpoints != nullptr) {
+        if (!aligned16(checkpoints))
+            return fail(KDA_ERR_INVALID_ARG, "checkpoints is not 16-byte aligned");
+        if (chunk != 16 && chunk != 64)
+            return fail(KDA_ERR_INVALID_ARG, "chunk must be 16 or 64, got %d", chunk);
+        if (checkpoint_every <= 0 || checkpoint_every % chunk != 0)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "checkpoint_every must be a positive multiple of the chunk (%lld, chunk %d)",
+                        (long long)checkpoint_every, chunk);
+        if (max_checkpoints <= 0)
+            return fail(KDA_ERR_INVALID_ARG, "max_checkpoints must be positive (got %d)",
+                        max_checkpoints);
+        ck.out = checkpoints;
+        ck.every = checkpoint_every;
+        ck.max_count = max_checkpoints;
+    }
+    return prefill_impl(q, k, v, z, beta, A, o, initial_state, final_state, cu_seqlens, n_seqs, B,
+                        T, H, d_k, d_v, chunk, dtype, workspace, workspace_bytes, ck, stream);
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* z,
@@ -212,6 +253,66 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
                                           dtype == KDA_DTYPE_BF16, stream);
     kda::profile_event(1, stream);
     return cuda_status(e, "kda_decode_step launch");
+}
+
+}  // extern "C"
+
+extern "C" {
+
+static kda_status spec_checks(int B, int T, int H, int d_k, int d_v, kda_dtype dtype) {
+    if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || T <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d d_k=%d d_v=%d", B, T, H, d_k,
+                    d_v);
+    if (T > 16) return fail(KDA_ERR_UNSUPPORTED, "at most 16 draft tokens per call (got %d)", T);
+    if (d_k > 128 || d_v > 128 || d_v % 4 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "needs d_k <= 128 and d_v <= 128, d_v %% 4 == 0 "
+                    "(d_k=%d d_v=%d)", d_k, d_v);
+    if ((int64_t)B * H > 0x7fffffffLL) return fail(KDA_ERR_UNSUPPORTED, "B*H too large");
+    return KDA_OK;
+}
+
+kda_status kda_spec_verify(const void* q, const void* k, const void* v, const void* z,
+                           const void* beta, const float* A, const float* state, void* o, int B,
+                           int T, int H, int d_k, int d_v, kda_dtype dtype, cudaStream_t stream) {
+    const kda_status st = spec_checks(B, T, H, d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (B == 0) return ok();
+    KDA_REQUIRE_PTR(q);
+    KDA_REQUIRE_PTR(k);
+    KDA_REQUIRE_PTR(v);
+    KDA_REQUIRE_PTR(z);
+    KDA_REQUIRE_PTR(beta);
+    KDA_REQUIRE_PTR(A);
+    KDA_REQUIRE_PTR(state);
+    KDA_REQUIRE_PTR(o);
+    kda::profile_event(0, stream);
+    const cudaError_t e = kda::run_spec(q, k, v, z, beta, A, const_cast<float*>(state), o, nullptr,
+                                        B, T, H, d_k, d_v, dtype == KDA_DTYPE_BF16, true, stream);
+    kda::profile_event(1, stream);
+    return cuda_status(e, "kda_spec_verify launch");
+}
+
+kda_status kda_spec_commit(const void* k, const void* v, const void* z, const void* beta,
+                           const float* A, float* state, const int32_t* n_accept, int B, int T,
+                           int H, int d_k, int d_v, kda_dtype dtype, cudaStream_t stream) {
+    const kda_status st = spec_checks(B, T, H, d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (B == 0) return ok();
+    KDA_REQUIRE_PTR(k);
+    KDA_REQUIRE_PTR(v);
+    KDA_REQUIRE_PTR(z);
+    KDA_REQUIRE_PTR(beta);
+    KDA_REQUIRE_PTR(A);
+    KDA_REQUIRE_PTR(state);
+    if (n_accept == nullptr) return fail(KDA_ERR_INVALID_ARG, "n_accept is NULL");
+    if ((reinterpret_cast<uintptr_t>(n_accept) & 3u) != 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_accept is not 4-byte aligned");
+    kda::profile_event(0, stream);
+    const cudaError_t e = kda::run_spec(nullptr, k, v, z, beta, A, state, nullptr, n_accept, B, T,
+                                        H, d_k, d_v, dtype == KDA_DTYPE_BF16, false, stream);
+    kda::profile_event(1, stream);
+    return cuda_status(e, "kda_spec_commit launch");
 }
 
 }  // extern "C"

@@ -45,7 +45,10 @@
 // 16-token scan, and the block references only enter through per-channel
 // factors e^{r_i - r_b}, e^{r_b}, e^{G_C - r_b}.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -765,7 +768,8 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 // ============================================================================
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
-                  const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H) {
+                  const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
+                  CheckpointSpec ck) {
     const int n = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lane_base = 32 * (warp & 3);
@@ -925,6 +929,16 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 *reinterpret_cast<uint4*>(sm + S_ST + g * 16384 + sw128(j, ch)) = pack8(o8);
             }
         }
+        // Checkpoint: the state after every `ck.every` tokens of this sequence.
+        if (ck.out) {
+            const int64_t done = (int64_t)(c + 1) * kC;
+            if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count) {
+                float* dst = ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
+                                          kD * kD;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) dst[(size_t)(64 * g + e) * kD + j] = st[e];
+            }
+        }
         if (!ok && tid == 0) {
             set_status(status, kErrStateWait);
             *s_abort = 1;
@@ -950,16 +964,34 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
 
 }  // namespace tc
 
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point so
+// that the library does not link against the driver library directly.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 // Tensor map of one [T_total][H][128] bf16 input with 64 x 1 x 128 boxes.
-static CUresult make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
     cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
     cuuint32_t box[3] = {128, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
-    return cuTensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
@@ -970,7 +1002,8 @@ size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0, float* S1,
                            const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                           void* workspace, cudaStream_t stream, int num_sms) {
+                           void* workspace, const CheckpointSpec& ck, cudaStream_t stream,
+                           int num_sms) {
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -995,10 +1028,8 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     if (T_total > 0) {
         tc::InputMaps maps;
-        if (make_input_map(&maps.q, q, T_total, H) != CUDA_SUCCESS ||
-            make_input_map(&maps.k, k, T_total, H) != CUDA_SUCCESS ||
-            make_input_map(&maps.v, v, T_total, H) != CUDA_SUCCESS ||
-            make_input_map(&maps.z, z, T_total, H) != CUDA_SUCCESS)
+        if (!make_input_map(&maps.q, q, T_total, H) || !make_input_map(&maps.k, k, T_total, H) ||
+            !make_input_map(&maps.v, v, T_total, H) || !make_input_map(&maps.z, z, T_total, H))
             return cudaErrorInvalidValue;
         const int64_t n_items = slots * H;
         const int64_t grid = n_items < num_sms ? n_items : num_sms;
@@ -1010,7 +1041,7 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     profile_event(1, stream);
     dim3 grid_s((unsigned)n_seqs, (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
-        ws, static_cast<bf*>(o), S0, S1, map, H);
+        ws, static_cast<bf*>(o), S0, S1, map, H, ck);
     e = cudaGetLastError();
     profile_event(2, stream);
     return e;

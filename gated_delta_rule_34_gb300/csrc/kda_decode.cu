@@ -148,3 +148,157 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
 }
 
 }  // namespace kda
+
+// ---------------------------------------------------------------------------
+// Speculative decoding: verify a span of draft tokens, then commit the
+// accepted prefix.  "How Kimi K3 is built" (section "How to serve two
+// different caches") describes K3 keeping the small input projections of the
+// draft tokens instead of a copy of the state after each one, and recomputing
+// the accepted span on chip.  Both kernels read S once into registers (same
+// thread layout as decode_kernel) and step through up to kSpecMaxT tokens:
+//   verify  o_t for every draft token; S is not written.
+//   commit  S advanced by the first n_accept[b] tokens, written once in place.
+// ---------------------------------------------------------------------------
+namespace kda {
+
+constexpr int kSpecMaxT = 16;
+
+template <typename T, bool kVerify>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+            const T* __restrict__ z, const T* __restrict__ beta, const float* __restrict__ A,
+            float* __restrict__ state, T* __restrict__ o, const int32_t* __restrict__ n_accept,
+            int Tn, int H, int dk, int dv) {
+    const int bh = blockIdx.x;
+    const int b = bh / H, h = bh % H;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int rg = lane >> 2, cg = lane & 3;
+    const int j0 = warp * 16 + cg * 4;
+    const bool col_ok = j0 < dv;
+    float* Sbh = state + (size_t)bh * dk * dv;
+    int n_steps = Tn;
+    if (!kVerify) {
+        const int na = n_accept[b];
+        n_steps = na < 0 ? 0 : (na > Tn ? Tn : na);
+        if (n_steps == 0) return;                       // nothing accepted: S unchanged
+    }
+
+    float4 s[kDecodeRows];
+#pragma unroll
+    for (int i = 0; i < kDecodeRows; ++i) {
+        const int r = rg + 8 * i;
+        s[i] = (col_ok && r < dk)
+                   ? __ldcs(reinterpret_cast<const float4*>(Sbh + (size_t)r * dv + j0))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    // Per-token vectors of the span: decay a (gate inline), k, q, v, beta.
+    __shared__ float s_a[kSpecMaxT][128], s_k[kSpecMaxT][128], s_q[kSpecMaxT][128];
+    __shared__ float s_v[kSpecMaxT][128], s_b[kSpecMaxT];
+    for (int idx = tid; idx < n_steps * 128; idx += kDecodeThreads) {
+        const int t = idx >> 7, c = idx & 127;
+        const size_t row = ((size_t)b * Tn + t) * H + h;
+        float kk = 0.f, qq = 0.f, aa = 1.f, vv = 0.f;
+        if (c < dk) {
+            kk = to_f32(k[row * dk + c]);
+            if (kVerify) qq = to_f32(q[row * dk + c]);
+            aa = expf(gate_accurate(expf(A[(size_t)h * dk + c]), to_f32(z[row * dk + c])));
+        }
+        if (c < dv) vv = to_f32(v[row * dv + c]);
+        s_a[t][c] = aa;
+        s_k[t][c] = kk;
+        s_q[t][c] = qq;
+        s_v[t][c] = vv;
+    }
+    if (tid < n_steps) s_b[tid] = to_f32(beta[((size_t)b * Tn + tid) * H + h]);
+    __syncthreads();
+
+    for (int t = 0; t < n_steps; ++t) {
+        float kq = 0.f;
+        if (kVerify) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) kq += s_k[t][lane + 32 * m] * s_q[t][lane + 32 * m];
+            kq = warp_sum(kq);
+        }
+        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) {
+            const int r = rg + 8 * i;
+            const float a = s_a[t][r], kr = s_k[t][r];
+            s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+            pk[0] = fmaf(s[i].x, kr, pk[0]); pk[1] = fmaf(s[i].y, kr, pk[1]);
+            pk[2] = fmaf(s[i].z, kr, pk[2]); pk[3] = fmaf(s[i].w, kr, pk[3]);
+            if (kVerify) {
+                const float qr = s_q[t][r];
+                pq[0] = fmaf(s[i].x, qr, pq[0]); pq[1] = fmaf(s[i].y, qr, pq[1]);
+                pq[2] = fmaf(s[i].z, qr, pq[2]); pq[3] = fmaf(s[i].w, qr, pq[3]);
+            }
+        }
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
+                if (kVerify) pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
+            }
+        }
+        const float bt = s_b[t];
+        float u[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u[c] = bt * ((col_ok ? s_v[t][j0 + c] : 0.f) - pk[c]);
+        if (kVerify && col_ok && rg == 0) {
+            T* ob = o + (((size_t)b * Tn + t) * H + h) * dv + j0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ob[c] = from_f32<T>(fmaf(u[c], kq, pq[c]));
+        }
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) {
+            const float kr = s_k[t][rg + 8 * i];
+            s[i].x = fmaf(kr, u[0], s[i].x); s[i].y = fmaf(kr, u[1], s[i].y);
+            s[i].z = fmaf(kr, u[2], s[i].z); s[i].w = fmaf(kr, u[3], s[i].w);
+        }
+    }
+    if (!kVerify) {
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) {
+            const int r = rg + 8 * i;
+            if (col_ok && r < dk) __stcs(reinterpret_cast<float4*>(Sbh + (size_t)r * dv + j0), s[i]);
+        }
+    }
+}
+
+cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z, const void* beta,
+                     const float* A, float* state, void* o, const int32_t* n_accept, int B, int Tn,
+                     int H, int dk, int dv, bool bf16, bool verify, cudaStream_t stream) {
+    const unsigned grid = (unsigned)((int64_t)B * H);
+    if (bf16) {
+        using Tb = __nv_bfloat16;
+        auto kq = static_cast<const Tb*>(q);
+        auto kk = static_cast<const Tb*>(k);
+        auto kv = static_cast<const Tb*>(v);
+        auto kz = static_cast<const Tb*>(z);
+        auto kb = static_cast<const Tb*>(beta);
+        if (verify)
+            spec_kernel<Tb, true><<<grid, kDecodeThreads, 0, stream>>>(
+                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
+        else
+            spec_kernel<Tb, false><<<grid, kDecodeThreads, 0, stream>>>(
+                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
+    } else {
+        auto kq = static_cast<const float*>(q);
+        auto kk = static_cast<const float*>(k);
+        auto kv = static_cast<const float*>(v);
+        auto kz = static_cast<const float*>(z);
+        auto kb = static_cast<const float*>(beta);
+        if (verify)
+            spec_kernel<float, true><<<grid, kDecodeThreads, 0, stream>>>(
+                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
+        else
+            spec_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
+                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -22,18 +22,33 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
                        const void* beta, const float* A, float* state, void* o, int B, int H,
                        int dk, int dv, bool bf16, cudaStream_t stream);
 
+// Speculative decoding over Tn <= 16 draft tokens per sequence: verify (outputs,
+// state untouched) or commit (state advanced by n_accept[b] tokens, in place).
+cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z, const void* beta,
+                     const float* A, float* state, void* o, const int32_t* n_accept, int B, int Tn,
+                     int H, int dk, int dv, bool bf16, bool verify, cudaStream_t stream);
+
+// Optional emission of intermediate states: for each sequence, the state after
+// (i + 1) * every tokens goes to out[((n * H + h) * max_count + i)], i < max_count.
+struct CheckpointSpec {
+    float* out = nullptr;       // [N, H, max_count, d_k, d_v] fp32, or null
+    int64_t every = 0;          // tokens between checkpoints (a multiple of the chunk)
+    int max_count = 0;
+};
+
 // Token-by-token SIMT path (fp32 arithmetic), any d_k, d_v <= 128.
 cudaError_t run_recurrent(const void* q, const void* k, const void* v, const void* z,
                           const void* beta, const float* A, void* o, const float* S0, float* S1,
                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                          int dk, int dv, bool bf16, cudaStream_t stream);
+                          int dk, int dv, bool bf16, const CheckpointSpec& ck,
+                          cudaStream_t stream);
 
 // Chunked tensor-core path (bf16, d_k = d_v = 128, chunk 64).
 size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H);
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0,
                            float* S1, const int32_t* cu, int n_seqs, int64_t T,
-                           int64_t T_total, int H, void* workspace, cudaStream_t stream,
-                           int num_sms);
+                           int64_t T_total, int H, void* workspace, const CheckpointSpec& ck,
+                           cudaStream_t stream, int num_sms);
 
 }  // namespace kda

@@ -34,7 +34,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  const float* __restrict__ A, T* __restrict__ o,
                  const float* __restrict__ S0, float* __restrict__ S1,
                  const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H,
-                 int dk, int dv) {
+                 int dk, int dv, CheckpointSpec ck) {
     const int cgrp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int col0 = cgrp * kRecCols;           // first column of this CTA
@@ -140,6 +140,20 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
             const int j = col0 + jj;
             if (j < dv) o[((size_t)(t0 + tt) * H + h) * dv + j] = from_f32<T>(s_o[tt][jj]);
         }
+        // Checkpoint: the state after every `ck.every` tokens of this sequence.
+        const int64_t done = t0 + nt - bos;
+        if (ck.out && done % ck.every == 0 && done / ck.every <= ck.max_count) {
+            float* dst = ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = col0 + wcol + c;
+                    if (r < dk && j < dv) dst[(size_t)r * dv + j] = st[i][c];
+                }
+            }
+        }
     }
 
     if (S1) {
@@ -158,20 +172,21 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 cudaError_t run_recurrent(const void* q, const void* k, const void* v, const void* z,
                           const void* beta, const float* A, void* o, const float* S0, float* S1,
                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                          int dk, int dv, bool bf16, cudaStream_t stream) {
+                          int dk, int dv, bool bf16, const CheckpointSpec& ck,
+                          cudaStream_t stream) {
     dim3 grid((unsigned)((dv + kRecCols - 1) / kRecCols), (unsigned)H, (unsigned)n_seqs);
     if (bf16) {
         using Tb = __nv_bfloat16;
         recurrent_kernel<Tb><<<grid, kRecThreads, 0, stream>>>(
             static_cast<const Tb*>(q), static_cast<const Tb*>(k), static_cast<const Tb*>(v),
             static_cast<const Tb*>(z), static_cast<const Tb*>(beta), A, static_cast<Tb*>(o),
-            S0, S1, cu, T, T_total, H, dk, dv);
+            S0, S1, cu, T, T_total, H, dk, dv, ck);
     } else {
         recurrent_kernel<float><<<grid, kRecThreads, 0, stream>>>(
             static_cast<const float*>(q), static_cast<const float*>(k),
             static_cast<const float*>(v), static_cast<const float*>(z),
             static_cast<const float*>(beta), A, static_cast<float*>(o), S0, S1, cu, T, T_total,
-            H, dk, dv);
+            H, dk, dv, ck);
     }
     return cudaGetLastError();
 }

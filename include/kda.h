@@ -117,6 +117,34 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_chunk_prefill_checkpoints -- kda_chunk_prefill that also emits
+ * intermediate states ("checkpoint states") at fixed token boundaries.
+ *
+ * Serving with a prefix cache keeps states only at some boundaries and copies a
+ * saved state before continuing from it ("How Kimi K3 is built", section "How
+ * to serve two different caches": checkpoint states are immutable and copied
+ * into the request's own state before it continues).  This call writes, for
+ * every sequence n and head h, the state after (i + 1) * checkpoint_every of
+ * that sequence's tokens into checkpoints[n, h, i] for
+ * i < min(len_n / checkpoint_every, max_checkpoints).  Slots past that are not
+ * written.  Continuing a prefill from checkpoints[n, h, i] (as initial_state)
+ * gives the same result as the uninterrupted run.
+ *   checkpoints       nullable (then this is kda_chunk_prefill); [N, H,
+ *                     max_checkpoints, d_k, d_v] fp32, 16-byte aligned
+ *   checkpoint_every  tokens between checkpoints, a positive multiple of chunk
+ *   max_checkpoints   slots per (sequence, head), >= 1
+ * Everything else is as for kda_chunk_prefill.
+ */
+kda_status kda_chunk_prefill_checkpoints(const void *q, const void *k, const void *v,
+                                         const void *z, const void *beta, const float *A, void *o,
+                                         const float *initial_state, float *final_state,
+                                         const int32_t *cu_seqlens, int n_seqs, int B, int64_t T,
+                                         int H, int d_k, int d_v, int chunk, kda_dtype dtype,
+                                         float *checkpoints, int64_t checkpoint_every,
+                                         int max_checkpoints, void *workspace,
+                                         size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Bytes of workspace kda_chunk_prefill needs for these sizes (0 if none).
  * For packed batches pass B = 1, T = total tokens and the sequence count; the
  * bound does not depend on the individual lengths.
@@ -181,8 +209,34 @@ kda_status kda_chunk_prefill_static_workspace(const void *q, const void *k, cons
                                               cudaStream_t stream);
 
 /*
+ * kda_spec_verify / kda_spec_commit -- speculative decoding without a state
+ * copy per draft token.  "How Kimi K3 is built", section "How to serve two
+ * different caches": K3 keeps the small input projections of the draft tokens
+ * and recomputes the accepted span on chip, which is cheaper than reading the
+ * large recurrent state again for every draft token.
+ *
+ * kda_spec_verify runs T draft tokens per sequence from `state` and writes
+ * their outputs.  The state is read once and NOT modified:
+ *   q, k, z  [B, T, H, d_k];  v, o [B, T, H, d_v];  beta [B, T, H]  (dtype)
+ *   A        [H, d_k] fp32;   state [B, H, d_k, d_v] fp32 (read only)
+ * kda_spec_commit advances each sequence's state by its first n_accept[b]
+ * draft tokens (recomputed from k, v, z, beta) and writes it once, in place:
+ *   n_accept device int32 [B]; values are clamped into [0, T]; 0 leaves the
+ *   state untouched.
+ * Both take 1 <= T <= 16, d_k <= 128, d_v <= 128 with d_v a multiple of 4.
+ * verify followed by commit with n_accept = T equals T decode steps.
+ */
+kda_status kda_spec_verify(const void *q, const void *k, const void *v, const void *z,
+                           const void *beta, const float *A, const float *state, void *o, int B,
+                           int T, int H, int d_k, int d_v, kda_dtype dtype, cudaStream_t stream);
+
+kda_status kda_spec_commit(const void *k, const void *v, const void *z, const void *beta,
+                           const float *A, float *state, const int32_t *n_accept, int B, int T,
+                           int H, int d_k, int d_v, kda_dtype dtype, cudaStream_t stream);
+
+/*
  * Instrumentation (not part of the layer's arithmetic).  While `events` is
- * non-NULL, every later kda_chunk_prefill / kda_decode_step call made on this
+ * non-NULL, every later prefill, decode or speculative call made on this
  * thread records events[0] on its stream before its first kernel and
  * events[i] after its i-th kernel, for i < n_events; the caller then reads
  * per-kernel times with cudaEventElapsedTime.  The events stay owned by the

@@ -137,3 +137,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         api.lib()
+
+
+def test_spec_rejects_bad_arguments(L):
+    f = _fake()
+    assert L.kda_spec_verify(f, f, f, f, f, f, f, f, 2, 17, 2, 128, 128, 1, None) == UNSUPPORTED
+    assert L.kda_spec_verify(f, f, f, f, f, f, f, f, 2, 0, 2, 128, 128, 1, None) == INVALID
+    assert L.kda_spec_verify(None, f, f, f, f, f, f, f, 2, 4, 2, 128, 128, 1, None) == INVALID
+    assert L.kda_spec_verify(f, f, f, f, f, f, f, f, 2, 4, 2, 256, 128, 1, None) == UNSUPPORTED
+    assert L.kda_spec_commit(f, f, f, f, f, f, None, 2, 4, 2, 128, 128, 1, None) == INVALID
+    assert L.kda_spec_commit(f, f, f, f, f, f, _fake(0x10002), 2, 4, 2, 128, 128, 1,
+                             None) == INVALID
+    assert L.kda_spec_commit(None, None, None, None, None, None, None, 0, 4, 2, 128, 128, 1,
+                             None) == 0                                   # empty: no launch
