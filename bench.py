@@ -332,6 +332,8 @@ def run_ours(args):
         e2e = e2e_prefill(kda, xp, wp, steps=max(1, min(K, 3)))
         e2e["value"] *= world
 
+    next_rows = measure_next_rows(kda, xp, wp, xd, wd, peaks) if not args.no_extras else None
+
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         v, cores, desc = oracle_sample(args.cpu_seconds)
@@ -358,13 +360,66 @@ def run_ours(args):
             "decode": {"ms": dec_avg, "value": dec_gbs * world, "unit": "GB/s",
                        "frac": dec_gbs / peaks["hbm_gbs"], "bytes_per_step": dbytes,
                        "traffic": recorded_traffic("decode")},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "next_rows": next_rows,
             "gpu_launches": K * (n_prefill_kernels + 1), "clocks": clocks,
         }
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def _time_ms(fn, iters=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def measure_next_rows(kda, xp, wp, xd, wd, peaks):
+    """Timings of the rows beyond the base path (outside the timed step):
+    speculative verify / commit on the decode workload's states with T draft
+    tokens, and long-context prefill with a checkpoint every 512 tokens."""
+    import torch
+    from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs
+    out = {}
+    B, H, d = wd.B, wd.H, wd.dk
+    for T in (4, 16):
+        from dataclasses import replace
+        w = replace(WORKLOADS[1], H=H, seed=100 + T)
+        x = make_inputs(w, device="cuda", B=B, T=T)
+        state = xd["S0"].clone()
+        o = torch.empty((B, T, H, d), dtype=torch.bfloat16, device="cuda")
+        n_acc = torch.full((B,), T, dtype=torch.int32, device="cuda")
+        tv = _time_ms(lambda: kda.spec_verify(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                                              state, out=o))
+        tc = _time_ms(lambda: kda.spec_commit(x["k"], x["v"], x["z"], x["beta"], x["A"], state,
+                                              n_acc))
+        vbytes = B * H * (STATE_BYTES + T * (4 * 256 + 2 + 256))
+        cbytes = B * H * (2 * STATE_BYTES + T * (3 * 256 + 2))
+        out[f"spec_T{T}"] = {"verify_ms": tv, "verify_gbs": vbytes / (tv * 1e-3) / 1e9,
+                             "commit_ms": tc, "commit_gbs": cbytes / (tc * 1e-3) / 1e9,
+                             "draft_tokens_per_s": B * T / (tv * 1e-3)}
+    Bp, Tp, Hp, dk = xp["q"].shape
+    every = 512
+    slots = Tp // every
+    ck = torch.empty((Bp, Hp, slots, dk, dk), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.workspace_size(Bp, Bp, Tp, Hp, dk, dk, wp.chunk, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    tck = _time_ms(lambda: kda.chunk_prefill(xp["q"], xp["k"], xp["v"], xp["z"], xp["beta"],
+                                             xp["A"], initial_state=xp["S0"], chunk=wp.chunk,
+                                             workspace=ws, checkpoints=ck, checkpoint_every=every),
+                   iters=3, warm=1)
+    out["prefill_checkpoint_every_512"] = {"ms": tck, "tokens_per_s": Bp * Tp / (tck * 1e-3),
+                                           "checkpoint_bytes": ck.numel() * 4}
+    return out
 
 
 def e2e_prefill(kda, xp, wp, steps: int):
@@ -445,6 +500,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the speculative-decoding and checkpoint timings")
     ap.add_argument("--ncu-case", choices=["prefill", "decode"],
                     help="run a short fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)

@@ -61,12 +61,15 @@ constexpr int kC = 64;        // chunk length
 constexpr int kD = 128;       // d_k = d_v
 
 // ---- package: one per (chunk, head), byte offsets -------------------------
-// B operand of the state-pass MMA, per K-block kb (channels 64 kb .. 64 kb + 63
-// of the contraction): rows 0..127 = N[c][c'], rows 128..191 = Q'[t][c'].
+// B operand of the state-pass products, per K-block kb (channels 64 kb ..
+// 64 kb + 63 of the contraction): rows 0..127 = N[c][c'], rows 128..191 =
+// Q'[t][c'].  X and O' are split into four 32-column tiles, one per state
+// column tile, each [rows][32] bf16 with 16-byte chunks XOR-permuted by
+// (row / 2) mod 4 (see jtile_off).
 constexpr uint32_t PKG_B0 = 0;
 constexpr uint32_t PKG_BK = 24576;   // bytes per K-block (192 rows x 128 B)
-constexpr uint32_t PKG_XT = 49152;   // X^T [j][c], two swizzled K-blocks (c < 64, c >= 64)
-constexpr uint32_t PKG_OT = 81920;   // O'^T [j][t], one swizzled K-block
+constexpr uint32_t PKG_X = 49152;    // X[c][j]: tile r at PKG_X + 8192 r, [128 c][32 j]
+constexpr uint32_t PKG_OP = 81920;   // O'[t][j]: tile r at PKG_OP + 4096 r, [64 t][32 j]
 constexpr uint32_t PKG_LAM = 98304;  // lam [c] fp32
 constexpr uint32_t PKG_BYTES = 99328;
 constexpr uint32_t WS_HEADER = 1024;  // word 0: device status (0 = ok)
@@ -134,15 +137,24 @@ __host__ __device__ constexpr int xidx(int i, int b) {
 }
 
 // ---- state_pass ------------------------------------------------------------
-constexpr int kStateThreads = 256;
-constexpr uint32_t S_STAGE0 = 0;
-constexpr uint32_t S_STAGE1 = PKG_BYTES;
-constexpr uint32_t S_ST = 2 * PKG_BYTES;           // S^T [128 j][128 c] swizzled, 2 K-blocks
-constexpr uint32_t S_BAR = S_ST + 32768;
-constexpr uint32_t S_SMEM = S_BAR + 64;            // the dynamic base is 1024-aligned
-constexpr uint32_t kDCols = 192;                   // accumulator columns per chunk
-constexpr uint32_t kDBuf = 256;                    // TMEM column offset of the second buffer
-constexpr int kL2Ahead = 4;                        // packages prefetched into L2 this far ahead
+// One CTA per (sequence, head, 32-column tile of S): columns of S evolve
+// independently, so four CTAs share a head and each streams only its tiles of
+// X and O' plus the shared [N ; Q'] operand.
+constexpr int kStateThreads = 128;
+constexpr int kTiles = 4;                          // column tiles per (sequence, head)
+constexpr int kJ = 32;                             // state columns per tile
+constexpr int kStages = 3;
+constexpr uint32_t ST_B = 0;                       // [N ; Q'], both K-blocks (48 KB)
+constexpr uint32_t ST_X = 49152;                   // X tile [128 c][32 j]
+constexpr uint32_t ST_OP = 57344;                  // O' tile [64 t][32 j]
+constexpr uint32_t ST_LAM = 61440;                 // lam [128] fp32
+constexpr uint32_t ST_BYTES = 62464;               // per stage (61 KB, 1024-aligned)
+constexpr uint32_t ST_LOAD = 49152 + 8192 + 4096 + 512;
+constexpr uint32_t S_ST = kStages * ST_BYTES;      // S^T tile [32 j][128 c] bf16, 2 K-blocks of 4 KB
+constexpr uint32_t S_BAR = S_ST + 8192;
+constexpr uint32_t S_SMEM = S_BAR + 128;           // the dynamic base is 1024-aligned
+constexpr uint32_t kDBuf = 64;                     // TMEM columns per accumulator buffer
+constexpr int kL2Ahead = 6;                        // packages prefetched into L2 this far ahead
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
@@ -163,6 +175,11 @@ __device__ __forceinline__ int64_t seq_slot_base(const SeqMap& m, int n, int64_t
                                                  int64_t& eos) {
     seq_bounds(m.cu, n, m.T, m.T_total, bos, eos);
     return bos / kC + n;
+}
+
+// Byte offset of 16-byte chunk q (0..3) of row `row` in a [rows][32] bf16 tile.
+__host__ __device__ __forceinline__ uint32_t jtile_off(uint32_t row, uint32_t q) {
+    return row * 64u + (((q ^ (row >> 1)) & 3u) << 4);
 }
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
@@ -283,6 +300,28 @@ __device__ __forceinline__ bool slot_chunk(const SeqMap& map, int64_t slot, int6
     t0 = bos + chunk * kC;
     len = (int)((eos - t0) < kC ? (eos - t0) : kC);
     return true;
+}
+
+// Copies TMEM columns [col0, col0 + 128) of this thread's lane, as bf16, into
+// row `row` of four [rows][32] tiles `tile_bytes` apart (columns 32 r .. 32 r
+// + 31 go to tile r).
+__device__ __forceinline__ void tmem_row_to_jtiles(uint32_t taddr, uint8_t* tile0,
+                                                   uint32_t tile_bytes, uint32_t row) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float v[16];
+        tmem_ld16(taddr + 16u * q, v);
+        tmem_wait_ld();
+        uint4 lo, hi;
+        lo.x = pack_bf16x2(v[0], v[1]);   lo.y = pack_bf16x2(v[2], v[3]);
+        lo.z = pack_bf16x2(v[4], v[5]);   lo.w = pack_bf16x2(v[6], v[7]);
+        hi.x = pack_bf16x2(v[8], v[9]);   hi.y = pack_bf16x2(v[10], v[11]);
+        hi.z = pack_bf16x2(v[12], v[13]); hi.w = pack_bf16x2(v[14], v[15]);
+        uint8_t* t = tile0 + (q >> 1) * tile_bytes;            // 16 q .. 16 q + 15 in tile q / 2
+        const uint32_t c0 = (q & 1) * 2;
+        *reinterpret_cast<uint4*>(t + jtile_off(row, c0)) = lo;
+        *reinterpret_cast<uint4*>(t + jtile_off(row, c0 + 1)) = hi;
+    }
 }
 
 // Writes row t of the A (warps holding key rows) or P (query rows) operand from
@@ -681,19 +720,23 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         __syncthreads();
         tc_fence_after();
 
-        // ---- N = (K^C)^T W -> cols [0,128); [X^T | O'^T] = U~^T [K^C | P^T] -> [128,320);
-        //      P W -> [320,448): an M=128 product whose A rows 0..63 are P (rows 64..127
-        //      read the next tile and land in unused accumulator rows).
+        // ---- N = (K^C)^T W -> cols [0,128); X = (K^C)^T U~ -> [128,256);
+        //      P W -> [256,384); O' = P U~ -> [384,512).  The last two are M=128
+        //      products whose A rows 0..63 are P (rows 64..127 read the next tile
+        //      and land in unused accumulator rows).
         if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 128);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint32_t off = ks * 32;
-                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_KC + off)),
-                         desc_sw128(smem_u32(sm + R_WT + off)), idesc_bf16(128, 128), ks > 0);
-                mma_bf16(tbase + 128, desc_sw128(smem_u32(sm + R_UT + off)),
-                         desc_sw128(smem_u32(sm + R_KC + off)), idesc_bf16(128, 192), ks > 0);
-                mma_bf16(tbase + 320, desc_sw128(smem_u32(sm + R_P + off)),
-                         desc_sw128(smem_u32(sm + R_WT + off)), idesc_bf16(128, 128), ks > 0);
+                const uint64_t kc = desc_sw128(smem_u32(sm + R_KC + off));
+                const uint64_t pp = desc_sw128(smem_u32(sm + R_P + off));
+                const uint64_t wt = desc_sw128(smem_u32(sm + R_WT + off));
+                const uint64_t ut = desc_sw128(smem_u32(sm + R_UT + off));
+                mma_bf16(tbase + 0, kc, wt, idesc, ks > 0);
+                mma_bf16(tbase + 128, kc, ut, idesc, ks > 0);
+                mma_bf16(tbase + 256, pp, wt, idesc, ks > 0);
+                mma_bf16(tbase + 384, pp, ut, idesc, ks > 0);
             }
             mma_commit(bar);
         }
@@ -711,10 +754,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 tmem_row_to_tile<4>(taddr + 0, sm + R_PKG + PKG_B0, 0, row);
             } else if (role == 1) {     // N[c][c' >= 64] -> B rows c, K-block 1
                 tmem_row_to_tile<4>(taddr + 64, sm + R_PKG + PKG_B0 + PKG_BK, 0, row);
-            } else if (role == 2) {     // X^T[j][c] -> two K-blocks
-                tmem_row_to_tile<8>(taddr + 128, sm + R_PKG + PKG_XT, 16384, row);
-            } else {                    // O'^T[j][t] -> one K-block
-                tmem_row_to_tile<4>(taddr + 256, sm + R_PKG + PKG_OT, 0, row);
+            } else if (role == 2) {     // X[c][j] -> four column tiles
+                tmem_row_to_jtiles(taddr + 128, sm + R_PKG + PKG_X, 8192, row);
+            } else if ((warp & 3) < 2) {  // O'[t][j] (lanes 0..63) -> four column tiles
+                tmem_row_to_jtiles(taddr + 384, sm + R_PKG + PKG_OP, 4096, row);
             }
             // Q'[t][c] = Q^g[t][c] - (P W)[t][c] -> B rows 128 + t; lanes 0..63 hold rows t.
             if ((warp & 3) < 2 && role < 2) {
@@ -722,7 +765,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     float pw[16];
-                    tmem_ld16(taddr + 320 + 64 * kb + 16 * q4, pw);
+                    tmem_ld16(taddr + 256 + 64 * kb + 16 * q4, pw);
                     tmem_wait_ld();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
@@ -762,184 +805,177 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 }
 
 // ============================================================================
-// state_pass: one CTA per (sequence, head), sequential over its chunks.
-// Thread (warp w, lane l) owns state column j = 32 (w mod 4) + l and the
-// channel half c in [64 g, 64 g + 64), g = w / 4.
+// state_pass: one CTA per (sequence, head, column tile), sequential over the
+// sequence's chunks.  Thread c (0..127) owns row c of the tile: S[c][j0 .. j0+31]
+// in fp32 registers.  Per chunk, two tcgen05 products from the bf16 copy of
+// the tile's S^T: D_S[c][j] = (N S)[c][j] and D_O[t][j] = (Q' S)[t][j]
+// (M=128, N=32, K=128 each; the O product's A rows 64..127 are unused).
 // ============================================================================
+__device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, int tile,
+                                            uint64_t* full) {
+    mbar_expect_tx(full, ST_LOAD);
+    bulk_g2s(stg + ST_B, pkg + PKG_B0, 49152, full);
+    bulk_g2s(stg + ST_X, pkg + PKG_X + tile * 8192, 8192, full);
+    bulk_g2s(stg + ST_OP, pkg + PKG_OP + tile * 4096, 4096, full);
+    bulk_g2s(stg + ST_LAM, pkg + PKG_LAM, 512, full);
+}
+
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
                   CheckpointSpec ck) {
-    const int n = blockIdx.x, h = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int lane_base = 32 * (warp & 3);
-    const int j = lane_base + lane, g = warp >> 2;
+    const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int c = tid;                         // state row (channel) = TMEM lane
+    const int j0 = tile * kJ;
 
     int64_t bos, eos;
     const int64_t slot0 = seq_slot_base(map, n, bos, eos);
     const int nc = (int)((eos - bos + kC - 1) / kC);
     uint32_t* status = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(ws));
     const uint8_t* pkgs = ws + WS_HEADER;
+    auto pkg_of = [&](int chunk) { return pkgs + ((size_t)(slot0 + chunk) * H + h) * PKG_BYTES; };
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [2]
-    uint64_t* mmab = full + 2;                                         // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 4);
-    int* s_abort = reinterpret_cast<int*>(full + 5);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [kStages]
+    uint64_t* mmab = full + kStages;                                   // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mmab + 2);
+    int* s_abort = reinterpret_cast<int*>(mmab + 3);
 
-    const size_t sbase = ((size_t)n * H + h) * kD * kD;
-    float st[64];
+    // State row c of this tile.
+    const size_t srow = (((size_t)n * H + h) * kD + c) * kD + j0;
+    float st[kJ];
 #pragma unroll
-    for (int e = 0; e < 64; ++e)
-        st[e] = S0 ? S0[sbase + (size_t)(64 * g + e) * kD + j] : 0.f;
+    for (int q = 0; q < kJ / 4; ++q) {
+        const float4 v = S0 ? __ldg(reinterpret_cast<const float4*>(S0 + srow) + q)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        st[4 * q] = v.x; st[4 * q + 1] = v.y; st[4 * q + 2] = v.z; st[4 * q + 3] = v.w;
+    }
+    auto store_row = [&](float* dst) {
+#pragma unroll
+        for (int q = 0; q < kJ / 4; ++q)
+            reinterpret_cast<float4*>(dst)[q] =
+                make_float4(st[4 * q], st[4 * q + 1], st[4 * q + 2], st[4 * q + 3]);
+    };
 
-    // The layout below needs the dynamic base on a 1024-byte boundary.
     if (nc == 0 || (smem_u32(smem_raw) & 1023u) != 0) {
         if (nc != 0 && tid == 0) set_status(status, kErrSmemAlign);
-        if (S1) {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) S1[sbase + (size_t)(64 * g + e) * kD + j] = st[e];
-        }
+        if (S1) store_row(S1 + srow);
         return;
     }
 
-    if (warp == 0) tmem_alloc<512>(tslot);
+    if (warp == 0) tmem_alloc<128>(tslot);
     if (tid == 0) {
-        mbar_init(full + 0, 1);
-        mbar_init(full + 1, 1);
+        for (int p = 0; p < kStages; ++p) mbar_init(full + p, 1);
         mbar_init(mmab + 0, 1);
         mbar_init(mmab + 1, 1);
         fence_mbar_init();
         *s_abort = 0;
-        for (int p = 2; p < kL2Ahead && p < nc; ++p)
-            for (uint32_t off = 0; off < PKG_BYTES; off += 49664)
-                bulk_prefetch_l2(pkgs + ((size_t)(slot0 + p) * H + h) * PKG_BYTES + off,
-                                 off + 49664 <= PKG_BYTES ? 49664u : PKG_BYTES - off);
-        for (int p = 0; p < 2 && p < nc; ++p) {
-            const uint8_t* src = pkgs + ((size_t)(slot0 + p) * H + h) * PKG_BYTES;
-            uint8_t* dst = sm + (p ? S_STAGE1 : S_STAGE0);
-            mbar_expect_tx(full + p, PKG_BYTES);
-            bulk_g2s(dst, src, 49152, full + p);
-            bulk_g2s(dst + 49152, src + 49152, PKG_BYTES - 49152, full + p);
-        }
+        for (int p = 0; p < kStages && p < nc; ++p)
+            issue_stage(sm + p * ST_BYTES, pkg_of(p), tile, full + p);
+        for (int p = kStages; p < kL2Ahead && p < nc; ++p)
+            bulk_prefetch_l2(pkg_of(p), 49152);
     }
-    // S^T as the bf16 A operand: row j, K-block g.
+    // The tile's S^T as the bf16 B operand: column c of rows j (K-block c / 64).
+    auto write_st = [&]() {
+        __nv_bfloat16* kbase = reinterpret_cast<__nv_bfloat16*>(
+            sm + S_ST + (c >> 6) * 4096 + ((c & 7) * 2));
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        float o8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o8[e] = st[8 * ch + e];
-        *reinterpret_cast<uint4*>(sm + S_ST + g * 16384 + sw128(j, ch)) = pack8(o8);
-    }
+        for (int jj = 0; jj < kJ; ++jj)
+            *reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(kbase) +
+                                              sw128(jj, (c & 63) >> 3)) = __float2bfloat16_rn(st[jj]);
+    };
+    write_st();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    const uint32_t tl = tbase + ((uint32_t)lane_base << 16);
+    const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
     bool ok = true;
 
-    // Output of chunk c: O^T from TMEM buffer (c & 1) plus O'^T, staged as o rows
-    // [t][j] in the consumed N rows of its stage and written out with coalesced
-    // 128-bit stores (two 256-byte rows per warp instruction); the stage is then
-    // refilled with chunk c + 2.
-    auto epilogue = [&](int c) {
-        const int b = c & 1;
-        uint8_t* stg = sm + (b ? S_STAGE1 : S_STAGE0);
-        const int64_t t0 = bos + (int64_t)c * kC;
+    // Output rows of chunk cc: (Q' S)[t] from TMEM plus O'[t], written as 64
+    // contiguous bytes per token by threads t < 64; then the chunk's stage is
+    // refilled with chunk cc + kStages.
+    auto epilogue = [&](int cc) {
+        const int b = cc & 1;
+        uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
+        const int64_t t0 = bos + (int64_t)cc * kC;
         const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
-        float ov[32];
-        tmem_ld16(tl + b * kDBuf + 128 + 32 * g, *reinterpret_cast<float(*)[16]>(ov));
-        tmem_ld16(tl + b * kDBuf + 128 + 32 * g + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
-        tmem_wait_ld();
-        __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(stg + PKG_B0);  // [64 t][128 j]
+        if (warp < 2) {
+            const int t = tid;
+            float ov[32];
+            tmem_ld16(tl + b * kDBuf + 32, *reinterpret_cast<float(*)[16]>(ov));
+            tmem_ld16(tl + b * kDBuf + 48, *reinterpret_cast<float(*)[16]>(ov + 16));
+            tmem_wait_ld();
+            if (t < len) {
+                uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * kD + j0);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            float op[8];
-            unpack8(*reinterpret_cast<const uint4*>(stg + PKG_OT + sw128(j, 4 * g + q4)), op);
+                for (int q = 0; q < 4; ++q) {
+                    float op[8], o8[8];
+                    unpack8(*reinterpret_cast<const uint4*>(stg + ST_OP + jtile_off(t, q)), op);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = 32 * g + 8 * q4 + e;
-                ost[t * kD + j] = __float2bfloat16_rn(ov[8 * q4 + e] + op[e]);
+                    for (int e = 0; e < 8; ++e) o8[e] = ov[8 * q + e] + op[e];
+                    __stcs(dst + q, pack8(o8));
+                }
             }
         }
         tc_fence_before();
         __syncthreads();
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int i = it * kStateThreads + tid, t = i >> 4, ch = i & 15;
-            if (t < len)
-                __stcs(reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * kD) + ch,
-                       reinterpret_cast<const uint4*>(ost + t * kD)[ch]);
-        }
-        __syncthreads();
-        if (tid == 0 && c + 2 < nc) {
-            const uint8_t* src = pkgs + ((size_t)(slot0 + c + 2) * H + h) * PKG_BYTES;
-            mbar_expect_tx(full + b, PKG_BYTES);
-            bulk_g2s(stg, src, 49152, full + b);
-            bulk_g2s(stg + 49152, src + 49152, PKG_BYTES - 49152, full + b);
-        }
-        if (tid == 32 && c + kL2Ahead < nc)
-            for (uint32_t off = 0; off < PKG_BYTES; off += 49664)
-                bulk_prefetch_l2(pkgs + ((size_t)(slot0 + c + kL2Ahead) * H + h) * PKG_BYTES + off,
-                                 off + 49664 <= PKG_BYTES ? 49664u : PKG_BYTES - off);
+        if (tid == 0 && cc + kStages < nc) issue_stage(stg, pkg_of(cc + kStages), tile, full + cc % kStages);
+        if (tid == 32 && cc + kL2Ahead < nc) bulk_prefetch_l2(pkg_of(cc + kL2Ahead), 49152);
     };
 
-    for (int c = 0; c < nc; ++c) {
-        const int b = c & 1;
-        uint8_t* stg = sm + (b ? S_STAGE1 : S_STAGE0);
-        ok = mbar_wait(full + b, (c >> 1) & 1) && ok;
+    int cc = 0;
+    for (; cc < nc; ++cc) {
+        const int b = cc & 1;
+        uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
+        ok = mbar_wait(full + cc % kStages, (cc / kStages) & 1) && ok;
 
-        // [(N S)^T | (Q' S)^T] = S^T [N | Q']^T  -> TMEM buffer b (M=128, N=192, K=128)
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, kDCols);
+            const uint32_t idesc = idesc_bf16(128, kJ);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                mma_bf16(tbase + b * kDBuf, desc_sw128(smem_u32(sm + S_ST + kb * 16384 + off)),
-                         desc_sw128(smem_u32(stg + PKG_B0 + kb * PKG_BK + off)), idesc, ks > 0);
+                const uint64_t bd = desc_sw128(smem_u32(sm + S_ST + kb * 4096 + off));
+                mma_bf16(tbase + b * kDBuf, desc_sw128(smem_u32(stg + ST_B + kb * PKG_BK + off)),
+                         bd, idesc, ks > 0);
+                mma_bf16(tbase + b * kDBuf + 32,
+                         desc_sw128(smem_u32(stg + ST_B + kb * PKG_BK + 16384 + off)), bd, idesc,
+                         ks > 0);
             }
             mma_commit(mmab + b);
         }
-        if (c > 0) epilogue(c - 1);          // overlaps this chunk's MMA
+        if (cc > 0) epilogue(cc - 1);            // overlaps this chunk's products
 
-        ok = mbar_wait(mmab + b, (c >> 1) & 1) && ok;
+        ok = mbar_wait(mmab + b, (cc >> 1) & 1) && ok;
         tc_fence_after();
-        // S <- lam (.) S - (N S) + X, then refresh the bf16 operand copy of S^T.
+        // S <- lam (.) S - (N S) + X, then refresh the bf16 copy of the tile's S^T.
         {
-            const float* lam = reinterpret_cast<const float*>(stg + PKG_LAM) + 64 * g;
-            float d64[64];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                tmem_ld16(tl + b * kDBuf + 64 * g + 16 * q4,
-                          *reinterpret_cast<float(*)[16]>(d64 + 16 * q4));
+            float d32[32];
+            tmem_ld16(tl + b * kDBuf, *reinterpret_cast<float(*)[16]>(d32));
+            tmem_ld16(tl + b * kDBuf + 16, *reinterpret_cast<float(*)[16]>(d32 + 16));
             tmem_wait_ld();
+            const float lam = reinterpret_cast<const float*>(stg + ST_LAM)[c];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {                // chunk within K-block g
-                float x8[8], o8[8];
-                unpack8(*reinterpret_cast<const uint4*>(stg + PKG_XT + g * 16384 + sw128(j, ch)), x8);
+            for (int q = 0; q < 4; ++q) {
+                float x8[8];
+                unpack8(*reinterpret_cast<const uint4*>(stg + ST_X + jtile_off(c, q)), x8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int ce = 8 * ch + e;
-                    st[ce] = fmaf(lam[ce], st[ce], x8[e] - d64[ce]);
-                    o8[e] = st[ce];
-                }
-                *reinterpret_cast<uint4*>(sm + S_ST + g * 16384 + sw128(j, ch)) = pack8(o8);
+                for (int e = 0; e < 8; ++e) st[8 * q + e] = fmaf(lam, st[8 * q + e], x8[e] - d32[8 * q + e]);
             }
+            write_st();
         }
         // Checkpoint: the state after every `ck.every` tokens of this sequence.
         if (ck.out) {
-            const int64_t done = (int64_t)(c + 1) * kC;
-            if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count) {
-                float* dst = ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
-                                          kD * kD;
-#pragma unroll
-                for (int e = 0; e < 64; ++e) dst[(size_t)(64 * g + e) * kD + j] = st[e];
-            }
+            const int64_t done = (int64_t)(cc + 1) * kC;
+            if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
+                store_row(ck.out + ((((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
+                                        kD + c) * kD + j0);
         }
-        if (!ok && tid == 0) {
+        if (!ok) {
             set_status(status, kErrStateWait);
             *s_abort = 1;
         }
@@ -948,17 +984,21 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
         __syncthreads();
         if (*s_abort) break;
     }
-    if (!*s_abort) epilogue(nc - 1);
-
-    if (S1) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) S1[sbase + (size_t)(64 * g + e) * kD + j] = st[e];
+    if (!*s_abort) {
+        epilogue(nc - 1);
+    } else if (tid == 0) {
+        // A wait ran out: give the copies issued for chunks cc .. cc + 2 and
+        // this chunk's products a bounded chance to land before the CTA exits.
+        for (int m = cc; m < nc && m < cc + kStages; ++m) mbar_wait(full + m % kStages, (m / kStages) & 1);
+        mbar_wait(mmab + (cc & 1), (cc >> 1) & 1);
     }
+
+    if (S1) store_row(S1 + srow);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc<512>(tbase);
+        tmem_dealloc<128>(tbase);
     }
 }
 
@@ -1039,7 +1079,7 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         if (e != cudaSuccess) return e;
     }
     profile_event(1, stream);
-    dim3 grid_s((unsigned)n_seqs, (unsigned)H);
+    dim3 grid_s((unsigned)tc::kTiles, (unsigned)n_seqs, (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
         ws, static_cast<bf*>(o), S0, S1, map, H, ck);
     e = cudaGetLastError();
