@@ -139,8 +139,14 @@ __host__ __device__ constexpr int xidx(int i, int b) {
 // ---- state_pass ------------------------------------------------------------
 // One CTA per (sequence, head, 32-column tile of S): columns of S evolve
 // independently, so four CTAs share a head and each streams only its tiles of
-// X and O' plus the shared [N ; Q'] operand.
-constexpr int kStateThreads = 128;
+// X and O' plus the shared [N ; Q'] operand.  Warp roles: warps 0-3 update the
+// state (thread c owns row c), warps 4-5 write the outputs, warps 6 .. 6 +
+// kIssuers - 1 issue the tensor-core products (the contraction's eight K=16
+// steps are split between them, each into its own partial accumulator, since
+// a single thread issues one tcgen05.mma only every ~50 cycles); issuer 0
+// also issues the package copies.
+constexpr int kIssuers = 2;
+constexpr int kStateThreads = 32 * (6 + kIssuers);
 constexpr int kTiles = 4;                          // column tiles per (sequence, head)
 constexpr int kJ = 32;                             // state columns per tile
 constexpr int kStages = 3;
@@ -150,11 +156,15 @@ constexpr uint32_t ST_OP = 57344;                  // O' tile [64 t][32 j]
 constexpr uint32_t ST_LAM = 61440;                 // lam [128] fp32
 constexpr uint32_t ST_BYTES = 62464;               // per stage (61 KB, 1024-aligned)
 constexpr uint32_t ST_LOAD = 49152 + 8192 + 4096 + 512;
-constexpr uint32_t S_ST = kStages * ST_BYTES;      // S^T tile [32 j][128 c] bf16, 2 K-blocks of 4 KB
-constexpr uint32_t S_BAR = S_ST + 8192;
+constexpr uint32_t S_ST = kStages * ST_BYTES;      // 2 x S^T tile [32 j][128 c] bf16 (2 K-blocks of 4 KB)
+constexpr uint32_t S_BAR = S_ST + 2 * 8192;
 constexpr uint32_t S_SMEM = S_BAR + 128;           // the dynamic base is 1024-aligned
-constexpr uint32_t kDBuf = 64;                     // TMEM columns per accumulator buffer
+constexpr uint32_t kPart = 32 * kIssuers;          // TMEM columns of one product's partials
+constexpr uint32_t kDBuf = 2 * kPart;              // per accumulator buffer: S then O partials
+constexpr uint32_t kTmemCols = 2 * kDBuf;
 constexpr int kL2Ahead = 6;                        // packages prefetched into L2 this far ahead
+static_assert(kTmemCols == 256 || kTmemCols == 512, "state_pass TMEM allocation");
+static_assert(8 % kIssuers == 0, "K steps per issuer");
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
@@ -806,10 +816,19 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 
 // ============================================================================
 // state_pass: one CTA per (sequence, head, column tile), sequential over the
-// sequence's chunks.  Thread c (0..127) owns row c of the tile: S[c][j0 .. j0+31]
-// in fp32 registers.  Per chunk, two tcgen05 products from the bf16 copy of
-// the tile's S^T: D_S[c][j] = (N S)[c][j] and D_O[t][j] = (Q' S)[t][j]
-// (M=128, N=32, K=128 each; the O product's A rows 64..127 are unused).
+// sequence's chunks.  Thread c (0..127) of the update warps owns row c of the
+// tile, S[c][j0 .. j0+31], in fp32 registers.  Per chunk two tcgen05 products
+// read the bf16 copy of the tile's S^T: D_S[c][j] = (N S)[c][j] and D_O[t][j]
+// = (Q' S)[t][j] (M=128, N=32, K=128; the O product's A rows 64..127 are
+// unused).  S^T is double-buffered so that chunk m + 1's update can write the
+// next copy while chunk m's O product still reads the current one.
+//
+// Barriers (phase k of a per-chunk barrier belongs to the k-th chunk using it):
+//   full[m % 3]     package of chunk m landed            (1 arrival + bytes)
+//   sdone[m & 1]    chunk m's S product done             (kIssuers commits)
+//   odone[m & 1]    chunk m's O product done             (kIssuers commits)
+//   stready[p]      S^T copy p written by the update of the chunk before (4 warps)
+//   consumed[m & 1] chunk m's stage and accumulators read (6 warps)
 // ============================================================================
 __device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, int tile,
                                             uint64_t* full) {
@@ -820,13 +839,37 @@ __device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, in
     bulk_g2s(stg + ST_LAM, pkg + PKG_LAM, 512, full);
 }
 
+// Asks L2 for the parts of a package that one column-tile CTA copies.
+__device__ __forceinline__ void prefetch_stage(const uint8_t* pkg, int tile) {
+    bulk_prefetch_l2(pkg + PKG_B0, 49152);
+    bulk_prefetch_l2(pkg + PKG_X + tile * 8192, 8192);
+    bulk_prefetch_l2(pkg + PKG_OP + tile * 4096, 4096);
+    bulk_prefetch_l2(pkg + PKG_LAM, 512);
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has
+// raised `abort`.
+__device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < (1u << 30); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && (*abort || global_ns() - t0 > 2000000000ull)) break;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
+    tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+}
+
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
                   CheckpointSpec ck) {
     const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int c = tid;                         // state row (channel) = TMEM lane
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = tile * kJ;
 
     int64_t bos, eos;
@@ -838,78 +881,148 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [kStages]
-    uint64_t* mmab = full + kStages;                                   // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mmab + 2);
-    int* s_abort = reinterpret_cast<int*>(mmab + 3);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [3]
+    uint64_t* sdone = full + kStages;                                  // [2]
+    uint64_t* odone = sdone + 2;                                       // [2]
+    uint64_t* stready = odone + 2;                                     // [2]
+    uint64_t* consumed = stready + 2;                                  // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(consumed + 2);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
-    // State row c of this tile.
+    // State row c of this tile (update warps).
+    const int c = tid & 127;
     const size_t srow = (((size_t)n * H + h) * kD + c) * kD + j0;
     float st[kJ];
-#pragma unroll
-    for (int q = 0; q < kJ / 4; ++q) {
-        const float4 v = S0 ? __ldg(reinterpret_cast<const float4*>(S0 + srow) + q)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        st[4 * q] = v.x; st[4 * q + 1] = v.y; st[4 * q + 2] = v.z; st[4 * q + 3] = v.w;
-    }
     auto store_row = [&](float* dst) {
 #pragma unroll
         for (int q = 0; q < kJ / 4; ++q)
             reinterpret_cast<float4*>(dst)[q] =
                 make_float4(st[4 * q], st[4 * q + 1], st[4 * q + 2], st[4 * q + 3]);
     };
-
+    if (warp < 4) {
+#pragma unroll
+        for (int q = 0; q < kJ / 4; ++q) {
+            const float4 v = S0 ? __ldg(reinterpret_cast<const float4*>(S0 + srow) + q)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            st[4 * q] = v.x; st[4 * q + 1] = v.y; st[4 * q + 2] = v.z; st[4 * q + 3] = v.w;
+        }
+    }
     if (nc == 0 || (smem_u32(smem_raw) & 1023u) != 0) {
         if (nc != 0 && tid == 0) set_status(status, kErrSmemAlign);
-        if (S1) store_row(S1 + srow);
+        if (S1 && warp < 4) store_row(S1 + srow);
         return;
     }
 
-    if (warp == 0) tmem_alloc<128>(tslot);
-    if (tid == 0) {
-        for (int p = 0; p < kStages; ++p) mbar_init(full + p, 1);
-        mbar_init(mmab + 0, 1);
-        mbar_init(mmab + 1, 1);
-        fence_mbar_init();
-        *s_abort = 0;
-        for (int p = 0; p < kStages && p < nc; ++p)
-            issue_stage(sm + p * ST_BYTES, pkg_of(p), tile, full + p);
-        for (int p = kStages; p < kL2Ahead && p < nc; ++p)
-            bulk_prefetch_l2(pkg_of(p), 49152);
-    }
-    // The tile's S^T as the bf16 B operand: column c of rows j (K-block c / 64).
-    auto write_st = [&]() {
-        __nv_bfloat16* kbase = reinterpret_cast<__nv_bfloat16*>(
-            sm + S_ST + (c >> 6) * 4096 + ((c & 7) * 2));
+    // Copy p of the tile's S^T as the bf16 B operand: column c of rows j
+    // (K-block c / 64).
+    auto write_st = [&](int p) {
+        uint8_t* kbase = sm + S_ST + p * 8192 + (c >> 6) * 4096 + ((c & 7) * 2);
 #pragma unroll
         for (int jj = 0; jj < kJ; ++jj)
-            *reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(kbase) +
-                                              sw128(jj, (c & 63) >> 3)) = __float2bfloat16_rn(st[jj]);
+            *reinterpret_cast<__nv_bfloat16*>(kbase + sw128(jj, (c & 63) >> 3)) =
+                __float2bfloat16_rn(st[jj]);
     };
-    write_st();
+
+    if (warp == 0) tmem_alloc<kTmemCols>(tslot);
+    if (tid == 32) {
+        for (int p = 0; p < kStages; ++p) mbar_init(full + p, 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(sdone + p, kIssuers);
+            mbar_init(odone + p, kIssuers);
+            mbar_init(stready + p, 4);
+            mbar_init(consumed + p, 6);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp < 4) write_st(0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
     bool ok = true;
 
-    // Output rows of chunk cc: (Q' S)[t] from TMEM plus O'[t], written as 64
-    // contiguous bytes per token by threads t < 64; then the chunk's stage is
-    // refilled with chunk cc + kStages.
-    auto epilogue = [&](int cc) {
-        const int b = cc & 1;
-        uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
-        const int64_t t0 = bos + (int64_t)cc * kC;
-        const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
-        if (warp < 2) {
-            const int t = tid;
+    if (warp >= 6) {
+        // ---------------------------------------------------------- issuers
+        const int is = warp - 6;
+        if (lane == 0) {
+            int loaded = 0;                                // chunks whose copies were issued
+            if (is == 0) {
+                for (; loaded < kStages && loaded < nc; ++loaded)
+                    issue_stage(sm + loaded * ST_BYTES, pkg_of(loaded), tile, full + loaded);
+                for (int p = kStages; p < kL2Ahead && p < nc; ++p) prefetch_stage(pkg_of(p), tile);
+            }
+            const uint32_t idesc = idesc_bf16(128, kJ);
+            constexpr int kSteps = 8 / kIssuers;
+            int cc = 0;
+            for (; cc < nc; ++cc) {
+                const int b = cc & 1;
+                if (cc >= 2) {
+                    ok = role_wait(consumed + b, ((cc - 2) >> 1) & 1, abort) && ok;
+                    if (!ok) break;
+                    if (is == 0 && loaded < nc) {      // chunk cc + 1 into chunk cc - 2's stage
+                        issue_stage(sm + (loaded % kStages) * ST_BYTES, pkg_of(loaded), tile,
+                                    full + loaded % kStages);
+                        ++loaded;
+                    }
+                }
+                if (is == 0 && cc + kL2Ahead < nc) prefetch_stage(pkg_of(cc + kL2Ahead), tile);
+                ok = role_wait(full + cc % kStages, (cc / kStages) & 1, abort) && ok;
+                if (cc >= 1) ok = role_wait(stready + b, ((cc - 1) >> 1) & 1, abort) && ok;
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
+                const uint64_t bdesc0 = desc_sw128(smem_u32(sm + S_ST + b * 8192));
+                const uint64_t adesc0 = desc_sw128(smem_u32(stg + ST_B));
+                const uint32_t dS = tbase + b * kDBuf + 32 * is;
+#pragma unroll
+                for (int k = 0; k < kSteps; ++k) {
+                    const uint32_t ks = is * kSteps + k, kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(dS, adesc0 + ((kb * PKG_BK + off) >> 4), bdesc0 + ((kb * 4096 + off) >> 4),
+                             idesc, k > 0);
+                }
+                mma_commit(sdone + b);
+#pragma unroll
+                for (int k = 0; k < kSteps; ++k) {
+                    const uint32_t ks = is * kSteps + k, kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(dS + kPart, adesc0 + ((kb * PKG_BK + 16384 + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, k > 0);
+                }
+                mma_commit(odone + b);
+            }
+            if (!ok) {
+                *abort = 1;
+                set_status(status, kErrStateWait);
+                // Give the copies and products this CTA has in flight a bounded
+                // chance to land before it exits.
+                for (int m = cc; m < loaded; ++m) mbar_wait(full + m % kStages, (m / kStages) & 1);
+                if (cc > 0) mbar_wait(odone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1);
+            }
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------- outputs o = Q' S + O'
+        const int t = tid - 128;                           // token row = TMEM lane
+        const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+        for (int cc = 0; cc < nc; ++cc) {
+            const int b = cc & 1;
+            ok = role_wait(odone + b, (cc >> 1) & 1, abort) && ok;
+            if (!ok) break;
+            tc_fence_after();
             float ov[32];
-            tmem_ld16(tl + b * kDBuf + 32, *reinterpret_cast<float(*)[16]>(ov));
-            tmem_ld16(tl + b * kDBuf + 48, *reinterpret_cast<float(*)[16]>(ov + 16));
+            tmem_ld32(tl + b * kDBuf + kPart, ov);
             tmem_wait_ld();
-            if (t < len) {
+#pragma unroll
+            for (int i = 1; i < kIssuers; ++i) {
+                float pv[32];
+                tmem_ld32(tl + b * kDBuf + kPart + 32 * i, pv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] += pv[e];
+            }
+            const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
+            const int64_t t0 = bos + (int64_t)cc * kC;
+            if (t < eos - t0) {
                 uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * kD + j0);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -920,85 +1033,65 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                     __stcs(dst + q, pack8(o8));
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(consumed + b);
         }
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && cc + kStages < nc) issue_stage(stg, pkg_of(cc + kStages), tile, full + cc % kStages);
-        if (tid == 32 && cc + kL2Ahead < nc) bulk_prefetch_l2(pkg_of(cc + kL2Ahead), 49152);
-    };
-
-    int cc = 0;
-    for (; cc < nc; ++cc) {
-        const int b = cc & 1;
-        uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
-        ok = mbar_wait(full + cc % kStages, (cc / kStages) & 1) && ok;
-
-        if (tid == 0) {
+        if (!ok) *abort = 1;
+    } else {
+        // ------------------------------- state S <- lam (.) S - (N S) + X
+        const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
+        for (int cc = 0; cc < nc; ++cc) {
+            const int b = cc & 1;
+            ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
+            if (!ok) break;
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, kJ);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                const uint64_t bd = desc_sw128(smem_u32(sm + S_ST + kb * 4096 + off));
-                mma_bf16(tbase + b * kDBuf, desc_sw128(smem_u32(stg + ST_B + kb * PKG_BK + off)),
-                         bd, idesc, ks > 0);
-                mma_bf16(tbase + b * kDBuf + 32,
-                         desc_sw128(smem_u32(stg + ST_B + kb * PKG_BK + 16384 + off)), bd, idesc,
-                         ks > 0);
-            }
-            mma_commit(mmab + b);
-        }
-        if (cc > 0) epilogue(cc - 1);            // overlaps this chunk's products
-
-        ok = mbar_wait(mmab + b, (cc >> 1) & 1) && ok;
-        tc_fence_after();
-        // S <- lam (.) S - (N S) + X, then refresh the bf16 copy of the tile's S^T.
-        {
-            float d32[32];
-            tmem_ld16(tl + b * kDBuf, *reinterpret_cast<float(*)[16]>(d32));
-            tmem_ld16(tl + b * kDBuf + 16, *reinterpret_cast<float(*)[16]>(d32 + 16));
+            float d[32];
+            tmem_ld32(tl + b * kDBuf, d);
             tmem_wait_ld();
+#pragma unroll
+            for (int i = 1; i < kIssuers; ++i) {
+                float pv[32];
+                tmem_ld32(tl + b * kDBuf + 32 * i, pv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) d[e] += pv[e];
+            }
+            const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
             const float lam = reinterpret_cast<const float*>(stg + ST_LAM)[c];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float x8[8];
                 unpack8(*reinterpret_cast<const uint4*>(stg + ST_X + jtile_off(c, q)), x8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) st[8 * q + e] = fmaf(lam, st[8 * q + e], x8[e] - d32[8 * q + e]);
+                for (int e = 0; e < 8; ++e) st[8 * q + e] = fmaf(lam, st[8 * q + e], x8[e] - d[8 * q + e]);
             }
-            write_st();
+            if (cc + 1 < nc) write_st((cc + 1) & 1);
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (cc + 1 < nc) mbar_arrive(stready + ((cc + 1) & 1));
+                mbar_arrive(consumed + b);
+            }
+            // Checkpoint: the state after every `ck.every` tokens of this sequence.
+            if (ck.out) {
+                const int64_t done = (int64_t)(cc + 1) * kC;
+                if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
+                    store_row(ck.out + ((((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
+                                            kD + c) * kD + j0);
+            }
         }
-        // Checkpoint: the state after every `ck.every` tokens of this sequence.
-        if (ck.out) {
-            const int64_t done = (int64_t)(cc + 1) * kC;
-            if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
-                store_row(ck.out + ((((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
-                                        kD + c) * kD + j0);
-        }
-        if (!ok) {
-            set_status(status, kErrStateWait);
-            *s_abort = 1;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (*s_abort) break;
+        if (!ok) *abort = 1;
+        if (S1) store_row(S1 + srow);
     }
-    if (!*s_abort) {
-        epilogue(nc - 1);
-    } else if (tid == 0) {
-        // A wait ran out: give the copies issued for chunks cc .. cc + 2 and
-        // this chunk's products a bounded chance to land before the CTA exits.
-        for (int m = cc; m < nc && m < cc + kStages; ++m) mbar_wait(full + m % kStages, (m / kStages) & 1);
-        mbar_wait(mmab + (cc & 1), (cc >> 1) & 1);
-    }
+    if (!ok) set_status(status, kErrStateWait);
 
-    if (S1) store_row(S1 + srow);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc<128>(tbase);
+        tmem_dealloc<kTmemCols>(tbase);
     }
 }
 

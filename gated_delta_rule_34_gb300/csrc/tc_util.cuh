@@ -3,6 +3,7 @@
 // copies, and the 128-byte-swizzled K-major shared-memory operand layout.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace kda {
@@ -19,6 +20,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One arrival (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
