@@ -139,32 +139,32 @@ __host__ __device__ constexpr int xidx(int i, int b) {
 // ---- state_pass ------------------------------------------------------------
 // One CTA per (sequence, head, 32-column tile of S): columns of S evolve
 // independently, so four CTAs share a head and each streams only its tiles of
-// X and O' plus the shared [N ; Q'] operand.  Warp roles: warps 0-3 update the
-// state (thread c owns row c), warps 4-5 write the outputs, warps 6 .. 6 +
-// kIssuers - 1 issue the tensor-core products (the contraction's eight K=16
-// steps are split between them, each into its own partial accumulator, since
-// a single thread issues one tcgen05.mma only every ~50 cycles); issuer 0
-// also issues the package copies.
-constexpr int kIssuers = 2;
-constexpr int kStateThreads = 32 * (6 + kIssuers);
+// X and O' plus the shared [N ; Q'] operand.  Warp roles (a warp reaches the
+// TMEM lanes 32 (warp mod 4) .. + 31):
+//   warps 0-7            update the state: row c = 32 (w mod 4) + lane, columns
+//                        16 (w / 4) .. + 15 of the tile;
+//   warps 8-11           write the outputs: the O product is M=64, whose row t
+//                        sits in TMEM lane 32 (t / 16) + t mod 16, so lanes
+//                        0..15 of warp 8 + t / 16 hold token t;
+//   warp 12              issues the S product (on the chain from one chunk's
+//                        update to the next);
+//   warp 13              issues the O product once the S product is done, so
+//                        that it never delays the chain;
+//   warp 14              issues the package copies.
+// The tensor pipe accepts a small-N tcgen05.mma only every ~50 cycles, so the
+// chain's floor is about eight of those plus the update.
+constexpr int kStateThreads = 32 * 15;
+constexpr int kUpdWarps = 8, kOutWarps = 4;
 constexpr int kTiles = 4;                          // column tiles per (sequence, head)
 constexpr int kJ = 32;                             // state columns per tile
-constexpr int kStages = 3;
-constexpr uint32_t ST_B = 0;                       // [N ; Q'], both K-blocks (48 KB)
-constexpr uint32_t ST_X = 49152;                   // X tile [128 c][32 j]
-constexpr uint32_t ST_OP = 57344;                  // O' tile [64 t][32 j]
-constexpr uint32_t ST_LAM = 61440;                 // lam [128] fp32
-constexpr uint32_t ST_BYTES = 62464;               // per stage (61 KB, 1024-aligned)
-constexpr uint32_t ST_LOAD = 49152 + 8192 + 4096 + 512;
+constexpr int kStages = 4;
+constexpr uint32_t ST_BYTES = 49152;               // per stage: [N ; Q'], both K-blocks
 constexpr uint32_t S_ST = kStages * ST_BYTES;      // 2 x S^T tile [32 j][128 c] bf16 (2 K-blocks of 4 KB)
 constexpr uint32_t S_BAR = S_ST + 2 * 8192;
-constexpr uint32_t S_SMEM = S_BAR + 128;           // the dynamic base is 1024-aligned
-constexpr uint32_t kPart = 32 * kIssuers;          // TMEM columns of one product's partials
-constexpr uint32_t kDBuf = 2 * kPart;              // per accumulator buffer: S then O partials
+constexpr uint32_t S_SMEM = S_BAR + 256;           // the dynamic base is 1024-aligned
+constexpr uint32_t kDBuf = 64;                     // per accumulator buffer: D_S, then D_O at +32
 constexpr uint32_t kTmemCols = 2 * kDBuf;
 constexpr int kL2Ahead = 6;                        // packages prefetched into L2 this far ahead
-static_assert(kTmemCols == 256 || kTmemCols == 512, "state_pass TMEM allocation");
-static_assert(8 % kIssuers == 0, "K steps per issuer");
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
@@ -816,27 +816,25 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 
 // ============================================================================
 // state_pass: one CTA per (sequence, head, column tile), sequential over the
-// sequence's chunks.  Thread c (0..127) of the update warps owns row c of the
-// tile, S[c][j0 .. j0+31], in fp32 registers.  Per chunk two tcgen05 products
+// sequence's chunks.  The update warps hold the tile S[c][j0 .. j0+31] in fp32
+// registers, two threads per row c.  Per chunk two tcgen05 products
 // read the bf16 copy of the tile's S^T: D_S[c][j] = (N S)[c][j] and D_O[t][j]
-// = (Q' S)[t][j] (M=128, N=32, K=128; the O product's A rows 64..127 are
-// unused).  S^T is double-buffered so that chunk m + 1's update can write the
+// = (Q' S)[t][j] (N=32, K=128; M=128 and M=64).  S^T is double-buffered so that chunk m + 1's update can write the
 // next copy while chunk m's O product still reads the current one.
 //
 // Barriers (phase k of a per-chunk barrier belongs to the k-th chunk using it):
-//   full[m % 3]     package of chunk m landed            (1 arrival + bytes)
-//   sdone[m & 1]    chunk m's S product done             (kIssuers commits)
-//   odone[m & 1]    chunk m's O product done             (kIssuers commits)
-//   stready[p]      S^T copy p written by the update of the chunk before (4 warps)
-//   consumed[m & 1] chunk m's stage and accumulators read (6 warps)
+//   full[m % 4]     [N ; Q'] of chunk m landed            (1 arrival + bytes)
+//   sdone[m & 1]    chunk m's S product done              (1 commit)
+//   odone[m & 1]    chunk m's O product done              (1 commit)
+//   sfree[m % 4]    chunk m's products no longer read its stage (1 commit)
+//   stready[p]      S^T copy p written by the update of the chunk before (8 warps)
+//   dfree[m & 1]    chunk m's accumulators read           (12 warps)
+// X, O' and lam bypass shared memory: the warps that use them load their own
+// pieces straight into registers two chunks ahead.
 // ============================================================================
-__device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, int tile,
-                                            uint64_t* full) {
-    mbar_expect_tx(full, ST_LOAD);
-    bulk_g2s(stg + ST_B, pkg + PKG_B0, 49152, full);
-    bulk_g2s(stg + ST_X, pkg + PKG_X + tile * 8192, 8192, full);
-    bulk_g2s(stg + ST_OP, pkg + PKG_OP + tile * 4096, 4096, full);
-    bulk_g2s(stg + ST_LAM, pkg + PKG_LAM, 512, full);
+__device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, uint64_t* full) {
+    mbar_expect_tx(full, ST_BYTES);
+    bulk_g2s(stg, pkg + PKG_B0, ST_BYTES, full);
 }
 
 // Asks L2 for the parts of a package that one column-tile CTA copies.
@@ -859,11 +857,6 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
-    tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-}
-
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
@@ -881,27 +874,30 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [3]
-    uint64_t* sdone = full + kStages;                                  // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S_BAR);        // [4]
+    uint64_t* sfree = full + kStages;                                  // [4]
+    uint64_t* sdone = sfree + kStages;                                 // [2]
     uint64_t* odone = sdone + 2;                                       // [2]
     uint64_t* stready = odone + 2;                                     // [2]
-    uint64_t* consumed = stready + 2;                                  // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(consumed + 2);
+    uint64_t* dfree = stready + 2;                                     // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dfree + 2);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
-    // State row c of this tile (update warps).
-    const int c = tid & 127;
-    const size_t srow = (((size_t)n * H + h) * kD + c) * kD + j0;
-    float st[kJ];
+    // Update warps: row c, columns jh .. jh + 15 of the tile (jh = 0 or 16).
+    const int c = 32 * (warp & 3) + lane;
+    const int jh = 16 * ((warp >> 2) & 1);
+    const bool upd = warp < kUpdWarps;
+    const size_t srow = (((size_t)n * H + h) * kD + c) * kD + j0 + jh;
+    float st[16];
     auto store_row = [&](float* dst) {
 #pragma unroll
-        for (int q = 0; q < kJ / 4; ++q)
+        for (int q = 0; q < 4; ++q)
             reinterpret_cast<float4*>(dst)[q] =
                 make_float4(st[4 * q], st[4 * q + 1], st[4 * q + 2], st[4 * q + 3]);
     };
-    if (warp < 4) {
+    if (upd) {
 #pragma unroll
-        for (int q = 0; q < kJ / 4; ++q) {
+        for (int q = 0; q < 4; ++q) {
             const float4 v = S0 ? __ldg(reinterpret_cast<const float4*>(S0 + srow) + q)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
             st[4 * q] = v.x; st[4 * q + 1] = v.y; st[4 * q + 2] = v.z; st[4 * q + 3] = v.w;
@@ -909,33 +905,36 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     }
     if (nc == 0 || (smem_u32(smem_raw) & 1023u) != 0) {
         if (nc != 0 && tid == 0) set_status(status, kErrSmemAlign);
-        if (S1 && warp < 4) store_row(S1 + srow);
+        if (S1 && upd) store_row(S1 + srow);
         return;
     }
 
-    // Copy p of the tile's S^T as the bf16 B operand: column c of rows j
-    // (K-block c / 64).
+    // Copy p of the tile's S^T as the bf16 B operand: column c of rows
+    // jh .. jh + 15 (K-block c / 64).
     auto write_st = [&](int p) {
         uint8_t* kbase = sm + S_ST + p * 8192 + (c >> 6) * 4096 + ((c & 7) * 2);
 #pragma unroll
-        for (int jj = 0; jj < kJ; ++jj)
-            *reinterpret_cast<__nv_bfloat16*>(kbase + sw128(jj, (c & 63) >> 3)) =
+        for (int jj = 0; jj < 16; ++jj)
+            *reinterpret_cast<__nv_bfloat16*>(kbase + sw128(jh + jj, (c & 63) >> 3)) =
                 __float2bfloat16_rn(st[jj]);
     };
 
     if (warp == 0) tmem_alloc<kTmemCols>(tslot);
     if (tid == 32) {
-        for (int p = 0; p < kStages; ++p) mbar_init(full + p, 1);
+        for (int p = 0; p < kStages; ++p) {
+            mbar_init(full + p, 1);
+            mbar_init(sfree + p, 1);
+        }
         for (int p = 0; p < 2; ++p) {
-            mbar_init(sdone + p, kIssuers);
-            mbar_init(odone + p, kIssuers);
-            mbar_init(stready + p, 4);
-            mbar_init(consumed + p, 6);
+            mbar_init(sdone + p, 1);
+            mbar_init(odone + p, 1);
+            mbar_init(stready + p, kUpdWarps);
+            mbar_init(dfree + p, kUpdWarps + kOutWarps);
         }
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp < 4) write_st(0);
+    if (upd) write_st(0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -943,144 +942,182 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     const uint32_t tbase = *tslot;
     bool ok = true;
 
-    if (warp >= 6) {
-        // ---------------------------------------------------------- issuers
-        const int is = warp - 6;
+    if (warp == 14) {
+        // ---------------------------------------------------- package copies
         if (lane == 0) {
-            int loaded = 0;                                // chunks whose copies were issued
-            if (is == 0) {
-                for (; loaded < kStages && loaded < nc; ++loaded)
-                    issue_stage(sm + loaded * ST_BYTES, pkg_of(loaded), tile, full + loaded);
-                for (int p = kStages; p < kL2Ahead && p < nc; ++p) prefetch_stage(pkg_of(p), tile);
+            int m = 0;
+            for (; m < kStages && m < nc; ++m) issue_stage(sm + m * ST_BYTES, pkg_of(m), full + m);
+            for (int p = kStages; p < kL2Ahead && p < nc; ++p) prefetch_stage(pkg_of(p), tile);
+            for (; m < nc; ++m) {
+                // chunk m goes into chunk m - 4's stage once that chunk's products are done
+                ok = role_wait(sfree + m % kStages, ((m - kStages) / kStages) & 1, abort) && ok;
+                if (!ok) break;
+                issue_stage(sm + (m % kStages) * ST_BYTES, pkg_of(m), full + m % kStages);
+                if (m + kL2Ahead - kStages < nc) prefetch_stage(pkg_of(m + kL2Ahead - kStages), tile);
             }
+            if (!ok) {
+                *abort = 1;
+                // Let the copies in flight land (bounded) before the CTA exits.
+                for (int k = m > kStages ? m - kStages : 0; k < m; ++k)
+                    mbar_wait(full + k % kStages, (k / kStages) & 1);
+            }
+        }
+    } else if (warp == 12) {
+        // ------------------------------------------- S product D_S = N S^T'
+        if (lane == 0) {
             const uint32_t idesc = idesc_bf16(128, kJ);
-            constexpr int kSteps = 8 / kIssuers;
             int cc = 0;
             for (; cc < nc; ++cc) {
                 const int b = cc & 1;
-                if (cc >= 2) {
-                    ok = role_wait(consumed + b, ((cc - 2) >> 1) & 1, abort) && ok;
-                    if (!ok) break;
-                    if (is == 0 && loaded < nc) {      // chunk cc + 1 into chunk cc - 2's stage
-                        issue_stage(sm + (loaded % kStages) * ST_BYTES, pkg_of(loaded), tile,
-                                    full + loaded % kStages);
-                        ++loaded;
-                    }
-                }
-                if (is == 0 && cc + kL2Ahead < nc) prefetch_stage(pkg_of(cc + kL2Ahead), tile);
+                // accumulator buffer b was last read for chunk cc - 2
+                if (cc >= 2) ok = role_wait(dfree + b, ((cc - 2) >> 1) & 1, abort) && ok;
                 ok = role_wait(full + cc % kStages, (cc / kStages) & 1, abort) && ok;
                 if (cc >= 1) ok = role_wait(stready + b, ((cc - 1) >> 1) & 1, abort) && ok;
                 if (!ok) break;
                 tc_fence_after();
-                const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
                 const uint64_t bdesc0 = desc_sw128(smem_u32(sm + S_ST + b * 8192));
-                const uint64_t adesc0 = desc_sw128(smem_u32(stg + ST_B));
-                const uint32_t dS = tbase + b * kDBuf + 32 * is;
+                const uint64_t adesc0 = desc_sw128(smem_u32(sm + (cc % kStages) * ST_BYTES));
 #pragma unroll
-                for (int k = 0; k < kSteps; ++k) {
-                    const uint32_t ks = is * kSteps + k, kb = ks >> 2, off = (ks & 3) * 32;
-                    mma_bf16(dS, adesc0 + ((kb * PKG_BK + off) >> 4), bdesc0 + ((kb * 4096 + off) >> 4),
-                             idesc, k > 0);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + b * kDBuf, adesc0 + ((kb * PKG_BK + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, ks > 0);
                 }
                 mma_commit(sdone + b);
-#pragma unroll
-                for (int k = 0; k < kSteps; ++k) {
-                    const uint32_t ks = is * kSteps + k, kb = ks >> 2, off = (ks & 3) * 32;
-                    mma_bf16(dS + kPart, adesc0 + ((kb * PKG_BK + 16384 + off) >> 4),
-                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, k > 0);
-                }
-                mma_commit(odone + b);
             }
             if (!ok) {
                 *abort = 1;
-                set_status(status, kErrStateWait);
-                // Give the copies and products this CTA has in flight a bounded
-                // chance to land before it exits.
-                for (int m = cc; m < loaded; ++m) mbar_wait(full + m % kStages, (m / kStages) & 1);
+                if (cc > 0) mbar_wait(sdone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1);
+            }
+        }
+    } else if (warp == 13) {
+        // ------------------------- O product D_O = Q' S^T' (M=64), after D_S
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(64, kJ);
+            int cc = 0;
+            for (; cc < nc; ++cc) {
+                const int b = cc & 1;
+                ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t bdesc0 = desc_sw128(smem_u32(sm + S_ST + b * 8192));
+                const uint64_t adesc0 = desc_sw128(smem_u32(sm + (cc % kStages) * ST_BYTES + 16384));
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + b * kDBuf + 32, adesc0 + ((kb * PKG_BK + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, ks > 0);
+                }
+                mma_commit(odone + b);
+                mma_commit(sfree + cc % kStages);   // the S product finished before these began
+            }
+            if (!ok) {
+                *abort = 1;
                 if (cc > 0) mbar_wait(odone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1);
             }
         }
-    } else if (warp >= 4) {
-        // -------------------------------------------- outputs o = Q' S + O'
-        const int t = tid - 128;                           // token row = TMEM lane
+    } else if (!upd) {
+        // ------------------------------- outputs o = Q' S + O' (warps 8-11)
+        const int t = 16 * (warp & 3) + lane;              // token row, lanes 0..15
+        const bool act = lane < 16;
         const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-        for (int cc = 0; cc < nc; ++cc) {
+        // O'[t][0 .. 31] of chunk m, loaded two chunks ahead of its use
+        auto load_op = [&](int m, uint4 (&r)[4]) {
+            const uint8_t* tp = pkg_of(m) + PKG_OP + tile * 4096;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r[q] = __ldg(reinterpret_cast<const uint4*>(tp + jtile_off(t, q)));
+        };
+        auto step = [&](int cc, uint4 (&r)[4]) -> bool {
             const int b = cc & 1;
             ok = role_wait(odone + b, (cc >> 1) & 1, abort) && ok;
-            if (!ok) break;
+            if (!ok) return false;
             tc_fence_after();
             float ov[32];
-            tmem_ld32(tl + b * kDBuf + kPart, ov);
+            tmem_ld16(tl + b * kDBuf + 32, *reinterpret_cast<float(*)[16]>(ov));
+            tmem_ld16(tl + b * kDBuf + 48, *reinterpret_cast<float(*)[16]>(ov + 16));
             tmem_wait_ld();
-#pragma unroll
-            for (int i = 1; i < kIssuers; ++i) {
-                float pv[32];
-                tmem_ld32(tl + b * kDBuf + kPart + 32 * i, pv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] += pv[e];
-            }
-            const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dfree + b);
             const int64_t t0 = bos + (int64_t)cc * kC;
-            if (t < eos - t0) {
+            if (act && t < eos - t0) {
                 uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * kD + j0);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float op[8], o8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(stg + ST_OP + jtile_off(t, q)), op);
+                    unpack8(r[q], op);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o8[e] = ov[8 * q + e] + op[e];
                     __stcs(dst + q, pack8(o8));
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(consumed + b);
+            if (act && cc + 2 < nc) load_op(cc + 2, r);
+            return true;
+        };
+        uint4 ra[4], rb[4];
+        if (act) {
+            load_op(0, ra);
+            if (nc > 1) load_op(1, rb);
+        }
+        for (int cc = 0; cc < nc; cc += 2) {
+            if (!step(cc, ra)) break;
+            if (cc + 1 < nc && !step(cc + 1, rb)) break;
         }
         if (!ok) *abort = 1;
     } else {
         // ------------------------------- state S <- lam (.) S - (N S) + X
-        const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
-        for (int cc = 0; cc < nc; ++cc) {
+        const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + jh;
+        // X[c][jh .. jh + 15] and lam[c] of chunk m, loaded two chunks ahead of their use
+        auto load_x = [&](int m, uint4& a, uint4& b2, float& l) {
+            const uint8_t* pk = pkg_of(m);
+            a = __ldg(reinterpret_cast<const uint4*>(pk + PKG_X + tile * 8192 + jtile_off(c, jh >> 3)));
+            b2 = __ldg(reinterpret_cast<const uint4*>(pk + PKG_X + tile * 8192 + jtile_off(c, (jh >> 3) + 1)));
+            l = __ldg(reinterpret_cast<const float*>(pk + PKG_LAM) + c);
+        };
+        auto step = [&](int cc, uint4& x0, uint4& x1, float& lam) -> bool {
             const int b = cc & 1;
             ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
-            if (!ok) break;
+            if (!ok) return false;
             tc_fence_after();
-            float d[32];
-            tmem_ld32(tl + b * kDBuf, d);
+            float d[16];
+            tmem_ld16(tl + b * kDBuf, d);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 1; i < kIssuers; ++i) {
-                float pv[32];
-                tmem_ld32(tl + b * kDBuf + 32 * i, pv);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) d[e] += pv[e];
-            }
-            const uint8_t* stg = sm + (cc % kStages) * ST_BYTES;
-            const float lam = reinterpret_cast<const float*>(stg + ST_LAM)[c];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float x8[8];
-                unpack8(*reinterpret_cast<const uint4*>(stg + ST_X + jtile_off(c, q)), x8);
+                unpack8(q == 0 ? x0 : x1, x8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) st[8 * q + e] = fmaf(lam, st[8 * q + e], x8[e] - d[8 * q + e]);
             }
-            if (cc + 1 < nc) write_st((cc + 1) & 1);
+            if (cc + 1 < nc) {
+                // S^T copy (cc + 1) & 1 is still read by chunk cc - 1's O product
+                if (cc >= 1) ok = role_wait(odone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1, abort) && ok;
+                write_st((cc + 1) & 1);
+            }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 if (cc + 1 < nc) mbar_arrive(stready + ((cc + 1) & 1));
-                mbar_arrive(consumed + b);
+                mbar_arrive(dfree + b);
             }
+            if (cc + 2 < nc) load_x(cc + 2, x0, x1, lam);
             // Checkpoint: the state after every `ck.every` tokens of this sequence.
             if (ck.out) {
                 const int64_t done = (int64_t)(cc + 1) * kC;
                 if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
                     store_row(ck.out + ((((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
-                                            kD + c) * kD + j0);
+                                            kD + c) * kD + j0 + jh);
             }
+            return true;
+        };
+        uint4 xa0, xa1, xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+        float la, lb = 0.f;
+        load_x(0, xa0, xa1, la);
+        if (nc > 1) load_x(1, xb0, xb1, lb);
+        for (int cc = 0; cc < nc; cc += 2) {
+            if (!step(cc, xa0, xa1, la)) break;
+            if (cc + 1 < nc && !step(cc + 1, xb0, xb1, lb)) break;
         }
         if (!ok) *abort = 1;
         if (S1) store_row(S1 + srow);
