@@ -122,12 +122,13 @@ constexpr uint32_t kInputBytes = 4 * 16384 + 512;    // q, k, v, z tiles and the
 constexpr uint32_t R_BAR = R_SMALL + R_SMALL_BYTES;
 constexpr uint32_t P_SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
 
-// K^(i): variant i covers rows s < 16 (i + 1), two K-blocks of N_i * 128 bytes.
-__host__ __device__ constexpr uint32_t kv_base(int i) {
-    return i == 0 ? 0u : i == 1 ? 4096u : i == 2 ? 12288u : 24576u;
-}
-__host__ __device__ constexpr uint32_t kv_rows(int i) { return 16u * (uint32_t)(i + 1); }
-// TMEM columns of the row-block products D_i (width 16 (i + 1)).
+// K^(i): variant i covers rows s < 16 (i + 1).  The four variants are stacked
+// into one 160-row operand (variant i from row d_col(i)), two K-blocks of
+// 160 x 128 bytes, so that the four row-block products are one N=160 product.
+constexpr uint32_t KV_ROWS = 160;
+constexpr uint32_t KV_KB = KV_ROWS * 128;
+// TMEM columns of the row-block products D_i (width 16 (i + 1)), which are
+// also the first row of variant i in the stacked operand.
 __host__ __device__ constexpr uint32_t d_col(int i) {
     return i == 0 ? 0u : i == 1 ? 16u : i == 2 ? 48u : 96u;
 }
@@ -380,14 +381,15 @@ struct InputMaps {
 };
 
 // Issues the loads of one item's inputs: q, k, v, z tiles by TMA and the A row
-// by a bulk copy, all completing on `inbar`; beta into a register of threads
-// < 64.  Rows past the item's `len` belong to the next sequence (or are zero);
-// the consumers mask them.
+// by a bulk copy, all completing on `inbar`; beta's raw bits into a register
+// of threads < 64, converted only when the next item starts so that the load
+// stays in flight meanwhile.  Rows past the item's `len` belong to the next
+// sequence (or are zero); the consumers mask them.
 __device__ __forceinline__ void issue_item_loads(uint8_t* sm, const InputMaps& maps,
                                                  const __nv_bfloat16* __restrict__ beta,
                                                  const float* __restrict__ A, int64_t t0, int len,
                                                  int h, int H, int tid, uint64_t* inbar,
-                                                 float& bt_reg) {
+                                                 uint32_t& bt_raw) {
     if (tid == 0) {
         mbar_expect_tx(inbar, kInputBytes);
         tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
@@ -396,8 +398,9 @@ __device__ __forceinline__ void issue_item_loads(uint8_t* sm, const InputMaps& m
         tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
         bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
     }
-    bt_reg = 0.f;
-    if (tid < kC && tid < len) bt_reg = __bfloat162float(beta[(size_t)(t0 + tid) * H + h]);
+    bt_raw = 0u;
+    if (tid < kC && tid < len)
+        bt_raw = reinterpret_cast<const unsigned short*>(beta)[(size_t)(t0 + tid) * H + h];
 }
 
 // ============================================================================
@@ -438,10 +441,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     int64_t item = blockIdx.x;
     int64_t t0 = 0;
     int len = 0;
-    float bt_reg = 0.f;
+    uint32_t bt_raw = 0u;
     while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
     if (item < n_items)
-        issue_item_loads(sm, maps, beta, A, t0, len, (int)(item % H), H, tid, inbar, bt_reg);
+        issue_item_loads(sm, maps, beta, A, t0, len, (int)(item % H), H, tid, inbar, bt_raw);
 
     while (item < n_items) {
         const int h = (int)(item % H);
@@ -473,7 +476,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 #pragma unroll
             for (int e = 0; e < 8; ++e) eA[e] = __expf(a8[e]);
         }
-        if (tid < kC) small[SM_B + tid] = bt_reg;
+        if (tid < kC) small[SM_B + tid] = __uint_as_float(bt_raw << 16);   // bf16 -> fp32
         __syncthreads();                         // raw z, q are read before G is written
 
         // ---- gate g = -5 sigmoid(e^A z) into G (0 on padded rows)
@@ -572,8 +575,8 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * x[e];  // k e^{r_i - G_t}
-                    *reinterpret_cast<uint4*>(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 +
-                                              sw128(t, chk)) = pack8(o8);
+                    *reinterpret_cast<uint4*>(sm + R_KV + kb * KV_KB + sw128(d_col(i) + t, chk)) =
+                        pack8(o8);
                 }
             }
         }
@@ -582,20 +585,17 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         __syncthreads();
         tc_fence_after();
 
-        // ---- A and P: four row-block products D_i = Astack * K^(i)^T into TMEM,
-        //      running while the column-side operands are built.
+        // ---- A and P: the row-block products D_i = Astack * K^(i)^T, as one
+        //      N=160 product into TMEM columns [0, 160), running while the
+        //      column-side operands are built.
         if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, KV_ROWS);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t idesc = idesc_bf16(128, kv_rows(i));
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                    const uint64_t ad = desc_sw128(smem_u32(sm + R_AST + kb * 16384 + off));
-                    const uint64_t bd = desc_sw128(
-                        smem_u32(sm + R_KV + kv_base(i) + kb * kv_rows(i) * 128 + off));
-                    mma_bf16(tbase + d_col(i), ad, bd, idesc, ks > 0);
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                const uint64_t ad = desc_sw128(smem_u32(sm + R_AST + kb * 16384 + off));
+                const uint64_t bd = desc_sw128(smem_u32(sm + R_KV + kb * KV_KB + off));
+                mma_bf16(tbase, ad, bd, idesc, ks > 0);
             }
             mma_commit(bar);
         }
@@ -651,7 +651,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         // Raw k, v and G are dead now: start loading the next item's inputs.
         if (nitem < n_items)
             issue_item_loads(sm, maps, beta, A, nt0, nlen, (int)(nitem % H), H, tid, inbar,
-                             bt_reg);
+                             bt_raw);
 
         // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution,
         //      then the off-diagonal blocks by distance.
