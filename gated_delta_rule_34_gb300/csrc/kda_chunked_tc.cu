@@ -81,6 +81,7 @@ constexpr uint32_t kErrSmemAlign = 4u;
 
 // ---- chunk_prep ------------------------------------------------------------
 constexpr int kPrepThreads = 512;
+constexpr int kLoadThread = 480;       // lane 0 of the last warp issues the input copies
 // shared memory (offsets from a 1024-byte aligned base).  The package image of
 // one item is staged in [0, PKG_BYTES) and stored asynchronously while the next
 // item starts: that range only holds buffers the next item first writes after
@@ -103,7 +104,7 @@ constexpr uint32_t R_ZQ = R_G;         // raw z [64][128] bf16, then raw q, of t
 constexpr uint32_t R_AF = 0;           // A fp32 [64][68]
 constexpr uint32_t R_TF = 17408;       // T fp32 [64][68]
 constexpr uint32_t R_TB = 34816;       // T bf16 [64][64] swizzled
-constexpr uint32_t R_XS = 43008;       // solve scratch [3][16][16] fp32
+constexpr uint32_t R_XS = 43008;       // solve scratch, 1024 fp32
 constexpr uint32_t F_LD = 68;           // fp32 row stride: 16-byte aligned rows, 4-bank skew
 // reuse after W / U~ (the solve's buffers and the A/P operands are dead)
 constexpr uint32_t R_WT = 0;           // W^T  [128 c][64 s] swizzled
@@ -169,7 +170,7 @@ constexpr int kL2Ahead = 6;                        // packages prefetched into L
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
-static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 3 * 256 * 4 <= R_BKT, "solve scratch");
+static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 1024 * 4 <= R_BKT, "solve scratch");
 static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions");
 static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
@@ -243,57 +244,87 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile_k
     }
 }
 
-// One distance of the blocked unit-lower inverse: for block pairs (i, j) with
-// i - j = d, X = sum_{m=j}^{i-1} A_im T_mj, then T_ij = -T_ii X.  A thread
-// computes four adjacent columns of one row: item (pair p, row r, column
-// group c4), so each A element loaded feeds four FMAs.
-template <int d>
-__device__ __forceinline__ void solve_offdiag(const float* __restrict__ Af, float* Tf,
-                                              float* Xs, int tid) {
-    constexpr int kItems = (4 - d) * 64;
-    if (tid < kItems) {
-        const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const int jb = p, ib = p + d;
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A (fp32, row stride F_LD),
+// by blocked doubling so that every step spreads over many threads: the 4 x 4
+// diagonal blocks by forward substitution, then for n = 4, 8, 16, 32 each
+// 2n x 2n diagonal block [T11 0; T21 T22] from its halves by
+// T21 = -T22 (A21 T11), with the n x n scratch X = A21 T11.  Every T entry
+// that a later step reads is written first, zeros above the diagonal included.
+template <int n>
+__device__ __forceinline__ void solve_level(const float* __restrict__ Af, float* Tf, float* Xs,
+                                            int tid) {
+    // A thread computes four adjacent entries (row i, columns j .. j + 3):
+    // lane = (pair p, row i), warp = column group, so the T (or X) row that a
+    // warp reads at step m is the same for all lanes of a pair (a broadcast)
+    // and the rows of A (or T22) are spread over the lanes.
+    constexpr int kThreads = 8 * n;                      // n / 4 warps
+    const int lane = tid & 31;
+    const int p = lane / n, i = lane % n, j = 4 * (tid >> 5);
+    const int e0 = (p * n + i) * n + j;
+    const int base = 2 * n * p;
+    if (tid < kThreads) {
+        // X[i][j..j+3] = sum_m A21[i][m] T11[m][j..j+3]
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* arow = Af + (base + n + i) * F_LD + base;
 #pragma unroll
-        for (int mm = 0; mm < d; ++mm) {
-            const int m = jb + mm;
-            float a[16];
+        for (int m4 = 0; m4 < n; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(arow + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 av = *reinterpret_cast<const float4*>(Af + (16 * ib + r) * F_LD + 16 * m + 4 * e4);
-                a[4 * e4] = av.x; a[4 * e4 + 1] = av.y; a[4 * e4 + 2] = av.z; a[4 * e4 + 3] = av.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float4 tv = *reinterpret_cast<const float4*>(Tf + (16 * m + e) * F_LD + 16 * jb + c4);
-                acc.x = fmaf(a[e], tv.x, acc.x); acc.y = fmaf(a[e], tv.y, acc.y);
-                acc.z = fmaf(a[e], tv.z, acc.z); acc.w = fmaf(a[e], tv.w, acc.w);
+            for (int e = 0; e < 4; ++e) {
+                const float4 t = *reinterpret_cast<const float4*>(Tf + (base + m4 + e) * F_LD + base + j);
+                acc.x = fmaf(av[e], t.x, acc.x); acc.y = fmaf(av[e], t.y, acc.y);
+                acc.z = fmaf(av[e], t.z, acc.z); acc.w = fmaf(av[e], t.w, acc.w);
             }
         }
-        *reinterpret_cast<float4*>(Xs + (p * 16 + r) * 16 + c4) = acc;
+        *reinterpret_cast<float4*>(Xs + e0) = acc;
     }
     __syncthreads();
-    if (tid < kItems) {
-        const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        const int jb = p, ib = p + d;
-        float tr[16];
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 tv = *reinterpret_cast<const float4*>(Tf + (16 * ib + r) * F_LD + 16 * ib + 4 * e4);
-            tr[4 * e4] = tv.x; tr[4 * e4 + 1] = tv.y; tr[4 * e4 + 2] = tv.z; tr[4 * e4 + 3] = tv.w;
-        }
+    if (tid < kThreads) {
+        // T21[i][j..j+3] = -sum_m T22[i][m] X[m][j..j+3]; T12 = 0
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* trow = Tf + (base + n + i) * F_LD + base + n;
+        const float* xp = Xs + p * n * n + j;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float4 xv = *reinterpret_cast<const float4*>(Xs + (p * 16 + e) * 16 + c4);
-            acc.x = fmaf(tr[e], xv.x, acc.x); acc.y = fmaf(tr[e], xv.y, acc.y);
-            acc.z = fmaf(tr[e], xv.z, acc.z); acc.w = fmaf(tr[e], xv.w, acc.w);
+        for (int m4 = 0; m4 < n; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(trow + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 x = *reinterpret_cast<const float4*>(xp + (m4 + e) * n);
+                acc.x = fmaf(av[e], x.x, acc.x); acc.y = fmaf(av[e], x.y, acc.y);
+                acc.z = fmaf(av[e], x.z, acc.z); acc.w = fmaf(av[e], x.w, acc.w);
+            }
         }
-        *reinterpret_cast<float4*>(Tf + (16 * ib + r) * F_LD + 16 * jb + c4) =
+        *reinterpret_cast<float4*>(Tf + (base + n + i) * F_LD + base + j) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        *reinterpret_cast<float4*>(Tf + (base + i) * F_LD + base + n + j) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, float* Tf,
+                                                 float* Xs, int tid) {
+    if (tid < 64) {
+        // column j of the 4 x 4 diagonal block k by forward substitution
+        const int k = tid >> 2, j = tid & 3;
+        const float* ab = Af + 4 * k * F_LD + 4 * k;
+        float x[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) acc = fmaf(ab[r * F_LD + m], x[m], acc);
+            x[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) Tf[(4 * k + r) * F_LD + 4 * k + j] = x[r];
+    }
+    __syncthreads();
+    solve_level<4>(Af, Tf, Xs, tid);
+    solve_level<8>(Af, Tf, Xs, tid);
+    solve_level<16>(Af, Tf, Xs, tid);
+    solve_level<32>(Af, Tf, Xs, tid);
 }
 
 // Which chunk package slot `slot` holds: its first token t0 and length.
@@ -380,27 +411,28 @@ struct InputMaps {
     CUtensorMap q, k, v, z;
 };
 
-// Issues the loads of one item's inputs: q, k, v, z tiles by TMA and the A row
-// by a bulk copy, all completing on `inbar`; beta's raw bits into a register
-// of threads < 64, converted only when the next item starts so that the load
-// stays in flight meanwhile.  Rows past the item's `len` belong to the next
-// sequence (or are zero); the consumers mask them.
-__device__ __forceinline__ void issue_item_loads(uint8_t* sm, const InputMaps& maps,
-                                                 const __nv_bfloat16* __restrict__ beta,
-                                                 const float* __restrict__ A, int64_t t0, int len,
-                                                 int h, int H, int tid, uint64_t* inbar,
-                                                 uint32_t& bt_raw) {
-    if (tid == 0) {
-        mbar_expect_tx(inbar, kInputBytes);
-        tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
-        tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, inbar);
-        tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, inbar);
-        tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
-        bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
-    }
-    bt_raw = 0u;
-    if (tid < kC && tid < len)
-        bt_raw = reinterpret_cast<const unsigned short*>(beta)[(size_t)(t0 + tid) * H + h];
+// One thread issues the loads of an item's inputs: q, k, v, z tiles by TMA
+// and the A row by a bulk copy, all completing on `inbar`.  Rows past the
+// item's `len` belong to the next sequence (or are zero); the consumers mask
+// them.
+__device__ __forceinline__ void issue_item_tma(uint8_t* sm, const InputMaps& maps,
+                                               const float* __restrict__ A, int64_t t0, int h,
+                                               uint64_t* inbar) {
+    mbar_expect_tx(inbar, kInputBytes);
+    tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
+    tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, inbar);
+    tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, inbar);
+    tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
+    bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
+}
+
+// beta's raw bits for threads < 64, converted only when the item starts so
+// that the load stays in flight meanwhile.
+__device__ __forceinline__ uint32_t load_beta_raw(const __nv_bfloat16* __restrict__ beta,
+                                                  int64_t t0, int len, int h, int H, int tid) {
+    uint32_t r = 0u;
+    if (tid < kC && tid < len) r = reinterpret_cast<const unsigned short*>(beta)[(size_t)(t0 + tid) * H + h];
+    return r;
 }
 
 // ============================================================================
@@ -443,8 +475,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     int len = 0;
     uint32_t bt_raw = 0u;
     while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
-    if (item < n_items)
-        issue_item_loads(sm, maps, beta, A, t0, len, (int)(item % H), H, tid, inbar, bt_raw);
+    if (item < n_items) {
+        if (tid == kLoadThread) issue_item_tma(sm, maps, A, t0, (int)(item % H), inbar);
+        bt_raw = load_beta_raw(beta, t0, len, (int)(item % H), H, tid);
+    }
 
     while (item < n_items) {
         const int h = (int)(item % H);
@@ -648,47 +682,14 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         }
         tc_fence_before();
         __syncthreads();
-        // Raw k, v and G are dead now: start loading the next item's inputs.
-        if (nitem < n_items)
-            issue_item_loads(sm, maps, beta, A, nt0, nlen, (int)(nitem % H), H, tid, inbar,
-                             bt_raw);
+        if (nitem < n_items) bt_raw = load_beta_raw(beta, nt0, nlen, (int)(nitem % H), H, tid);
 
-        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution,
-        //      then the off-diagonal blocks by distance.
+        // ---- T = (I + A)^{-1}
         {
             const float* Af = reinterpret_cast<const float*>(sm + R_AF);
             float* Tf = reinterpret_cast<float*>(sm + R_TF);
             float* Xs = reinterpret_cast<float*>(sm + R_XS);
-            if (tid < 64) {
-                // Column j of the inverse of diagonal block blk, by forward substitution;
-                // rows of A are read before any T entry is written.
-                const int blk = tid >> 4, j = tid & 15;
-                const float* __restrict__ Ab = Af + 16 * blk * F_LD + 16 * blk;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float a[16];
-#pragma unroll
-                    for (int e4 = 0; e4 < (r + 3) / 4; ++e4) {
-                        const float4 av = *reinterpret_cast<const float4*>(Ab + r * F_LD + 4 * e4);
-                        a[4 * e4] = av.x; a[4 * e4 + 1] = av.y; a[4 * e4 + 2] = av.z; a[4 * e4 + 3] = av.w;
-                    }
-                    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                    for (int m = 0; m + 1 < r; m += 2) {
-                        a0 = fmaf(a[m], x[m], a0);
-                        a1 = fmaf(a[m + 1], x[m + 1], a1);
-                    }
-                    if (r & 1) a0 = fmaf(a[r - 1], x[r - 1], a0);
-                    x[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tf[(16 * blk + r) * F_LD + 16 * blk + j] = x[r];
-            }
-            __syncthreads();
-            solve_offdiag<1>(Af, Tf, Xs, tid);
-            solve_offdiag<2>(Af, Tf, Xs, tid);
-            solve_offdiag<3>(Af, Tf, Xs, tid);
+            solve_unit_lower(Af, Tf, Xs, tid);
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
             {
                 const int t = tid >> 3, ch = tid & 7;
@@ -716,6 +717,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             }
             mma_commit(bar);
         }
+        // Raw k, v, z, q and G are dead now: a thread idle in the solve's last
+        // steps starts loading the next item's inputs during this wait.
+        if (tid == kLoadThread && nitem < n_items)
+            issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
         ok = mbar_wait(bar, phase) && ok;
         phase ^= 1u;
         tc_fence_after();
