@@ -250,6 +250,39 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile_k
 // 2n x 2n diagonal block [T11 0; T21 T22] from its halves by
 // T21 = -T22 (A21 T11), with the n x n scratch X = A21 T11.  Every T entry
 // that a later step reads is written first, zeros above the diagonal included.
+// Run by the first kSolveThreads threads, which synchronise among themselves
+// on named barrier 1, so that the other warps are free meanwhile.
+constexpr int kSolveThreads = 256;
+
+// acc[0..3] += sum_{m < n} row[m] * M[m][0..3], with M's rows `ld` floats
+// apart; the row's values are loaded first and M's rows in batches of eight,
+// so that each batch's loads are in flight together.
+template <int n>
+__device__ __forceinline__ float4 row_times_block(const float* __restrict__ row,
+                                                  const float* __restrict__ M, int ld) {
+    float r[n];
+#pragma unroll
+    for (int m4 = 0; m4 < n; m4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(row + m4);
+        r[m4] = a.x; r[m4 + 1] = a.y; r[m4 + 2] = a.z; r[m4 + 3] = a.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kB = n < 8 ? n : 8;
+#pragma unroll
+    for (int m0 = 0; m0 < n; m0 += kB) {
+        float4 t[kB];
+#pragma unroll
+        for (int e = 0; e < kB; ++e) t[e] = *reinterpret_cast<const float4*>(M + (m0 + e) * ld);
+#pragma unroll
+        for (int e = 0; e < kB; ++e) {
+            const float a = r[m0 + e];
+            acc.x = fmaf(a, t[e].x, acc.x); acc.y = fmaf(a, t[e].y, acc.y);
+            acc.z = fmaf(a, t[e].z, acc.z); acc.w = fmaf(a, t[e].w, acc.w);
+        }
+    }
+    return acc;
+}
+
 template <int n>
 __device__ __forceinline__ void solve_level(const float* __restrict__ Af, float* Tf, float* Xs,
                                             int tid) {
@@ -258,49 +291,27 @@ __device__ __forceinline__ void solve_level(const float* __restrict__ Af, float*
     // warp reads at step m is the same for all lanes of a pair (a broadcast)
     // and the rows of A (or T22) are spread over the lanes.
     constexpr int kThreads = 8 * n;                      // n / 4 warps
+    static_assert(kThreads <= kSolveThreads, "solve threads");
     const int lane = tid & 31;
     const int p = lane / n, i = lane % n, j = 4 * (tid >> 5);
     const int e0 = (p * n + i) * n + j;
     const int base = 2 * n * p;
     if (tid < kThreads) {
         // X[i][j..j+3] = sum_m A21[i][m] T11[m][j..j+3]
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = Af + (base + n + i) * F_LD + base;
-#pragma unroll
-        for (int m4 = 0; m4 < n; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(arow + m4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 t = *reinterpret_cast<const float4*>(Tf + (base + m4 + e) * F_LD + base + j);
-                acc.x = fmaf(av[e], t.x, acc.x); acc.y = fmaf(av[e], t.y, acc.y);
-                acc.z = fmaf(av[e], t.z, acc.z); acc.w = fmaf(av[e], t.w, acc.w);
-            }
-        }
+        const float4 acc = row_times_block<n>(Af + (base + n + i) * F_LD + base,
+                                              Tf + base * F_LD + base + j, F_LD);
         *reinterpret_cast<float4*>(Xs + e0) = acc;
     }
-    __syncthreads();
+    named_bar_sync(1, kSolveThreads);
     if (tid < kThreads) {
         // T21[i][j..j+3] = -sum_m T22[i][m] X[m][j..j+3]; T12 = 0
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* trow = Tf + (base + n + i) * F_LD + base + n;
-        const float* xp = Xs + p * n * n + j;
-#pragma unroll
-        for (int m4 = 0; m4 < n; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(trow + m4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 x = *reinterpret_cast<const float4*>(xp + (m4 + e) * n);
-                acc.x = fmaf(av[e], x.x, acc.x); acc.y = fmaf(av[e], x.y, acc.y);
-                acc.z = fmaf(av[e], x.z, acc.z); acc.w = fmaf(av[e], x.w, acc.w);
-            }
-        }
+        const float4 acc = row_times_block<n>(Tf + (base + n + i) * F_LD + base + n,
+                                              Xs + p * n * n + j, n);
         *reinterpret_cast<float4*>(Tf + (base + n + i) * F_LD + base + j) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         *reinterpret_cast<float4*>(Tf + (base + i) * F_LD + base + n + j) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
+    named_bar_sync(1, kSolveThreads);
 }
 
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, float* Tf,
@@ -320,7 +331,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, f
 #pragma unroll
         for (int r = 0; r < 4; ++r) Tf[(4 * k + r) * F_LD + 4 * k + j] = x[r];
     }
-    __syncthreads();
+    named_bar_sync(1, kSolveThreads);
     solve_level<4>(Af, Tf, Xs, tid);
     solve_level<8>(Af, Tf, Xs, tid);
     solve_level<16>(Af, Tf, Xs, tid);
@@ -481,7 +492,6 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     }
 
     while (item < n_items) {
-        const int h = (int)(item % H);
         uint8_t* pkg = ws + WS_HEADER + (size_t)item * PKG_BYTES;
         // The next item this CTA processes (skipping slots that hold no chunk).
         int64_t nitem = item + gridDim.x, nt0 = 0;
@@ -689,7 +699,14 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             const float* Af = reinterpret_cast<const float*>(sm + R_AF);
             float* Tf = reinterpret_cast<float*>(sm + R_TF);
             float* Xs = reinterpret_cast<float*>(sm + R_XS);
-            solve_unit_lower(Af, Tf, Xs, tid);
+            if (tid < kSolveThreads) {
+                solve_unit_lower(Af, Tf, Xs, tid);
+            } else if (tid == kLoadThread && nitem < n_items) {
+                // Raw k, v, z, q and G are dead now: an idle warp starts loading
+                // the next item's inputs while the solve runs.
+                issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
+            }
+            __syncthreads();
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
             {
                 const int t = tid >> 3, ch = tid & 7;
@@ -717,10 +734,6 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             }
             mma_commit(bar);
         }
-        // Raw k, v, z, q and G are dead now: a thread idle in the solve's last
-        // steps starts loading the next item's inputs during this wait.
-        if (tid == kLoadThread && nitem < n_items)
-            issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
         ok = mbar_wait(bar, phase) && ok;
         phase ^= 1u;
         tc_fence_after();
