@@ -456,8 +456,9 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                   int64_t n_items) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Offset from the array (not an integer cast) so that the compiler keeps
+    // every access below in the shared window.
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* G = reinterpret_cast<float*>(sm + R_G);
     float* small = reinterpret_cast<float*>(sm + R_SMALL);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
