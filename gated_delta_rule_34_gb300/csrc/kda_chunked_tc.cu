@@ -377,44 +377,6 @@ __device__ __forceinline__ void tmem_row_to_jtiles(uint32_t taddr, uint8_t* tile
     }
 }
 
-// Writes row t of the A (warps holding key rows) or P (query rows) operand from
-// the row-block product D_I, once its 16 (I + 1) columns are loaded.
-template <int I>
-__device__ __forceinline__ void emit_block_row(uint32_t taddr_lane, bool mine, bool key_rows,
-                                               int t, float bt, float* Af, uint8_t* ptile) {
-    float v[16 * (I + 1)];
-#pragma unroll
-    for (int q = 0; q <= I; ++q) tmem_ld16(taddr_lane + d_col(I) + 16u * q,
-                                           *reinterpret_cast<float(*)[16]>(v + 16 * q));
-    tmem_wait_ld();
-    if (!mine) return;
-    if (key_rows) {
-#pragma unroll
-        for (int s4 = 0; s4 < 16; ++s4) {
-            float o4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = 4 * s4 + e;
-                const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
-                o4[e] = (s < t) ? bt * val : 0.f;
-            }
-            *reinterpret_cast<float4*>(Af + t * F_LD + 4 * s4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
-        }
-    } else {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            float o8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = ch * 8 + e;
-                const float val = (s < 16 * (I + 1)) ? v[s < 16 * (I + 1) ? s : 0] : 0.f;
-                o8[e] = (s <= t) ? val : 0.f;
-            }
-            *reinterpret_cast<uint4*>(ptile + sw128(t, ch)) = pack8(o8);
-        }
-    }
-}
-
 // Input tensor maps: q, k, v, z as 3-D tensors [T_total][H][128] bf16 with
 // boxes of 64 tokens x 1 head x 128 channels (16 KB, rows at 256-byte pitch
 // in shared memory); boxes past the last token read zeros.
@@ -463,13 +425,15 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     float* small = reinterpret_cast<float*>(sm + R_SMALL);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
     uint64_t* inbar = bar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 16);
+    uint64_t* bar2 = bar + 2;               // second half of the last products
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 32);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
 
     if (warp == 0) tmem_alloc<512>(tslot);
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(inbar, 1);
+        mbar_init(bar2, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -478,6 +442,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     const uint32_t tbase = *tslot;
     uint32_t phase = 0;                      // parity of the next completion of `bar`
     uint32_t in_phase = 0;                   // parity of the next completion of `inbar`
+    uint32_t phase2 = 0;                     // parity of the next completion of `bar2`
     bool ok = true;
     const int c8 = tid & 15;                 // channels 8 c8 .. 8 c8 + 7 in the row-side passes
 
@@ -514,15 +479,11 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             qraw[it] = in ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
                           : make_uint4(0, 0, 0, 0);
         }
-        float eA[8];
-        {
-            float a8[8];
-            load8f(small + SM_A + c8 * 8, a8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) eA[e] = __expf(a8[e]);
-        }
+        if (tid < kD) small[SM_A + tid] = __expf(small[SM_A + tid]);       // A -> e^A, in place
         if (tid < kC) small[SM_B + tid] = __uint_as_float(bt_raw << 16);   // bf16 -> fp32
         __syncthreads();                         // raw z, q are read before G is written
+        float eA[8];
+        load8f(small + SM_A + c8 * 8, eA);
 
         // ---- gate g = -5 sigmoid(e^A z) into G (0 on padded rows)
 #pragma unroll
@@ -674,21 +635,51 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         phase ^= 1u;
         tc_fence_after();
 
-        // Readback: warps 0/1 hold key rows (-> A), warps 2/3 query rows (-> P).
-        if (warp < 4) {
-            const int lane_base = 32 * warp;
-            const int t = (lane_base + lane) & 63;
-            const int blk = t >> 4;
-            const bool key_rows = warp < 2;
-            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
-            float* Af = reinterpret_cast<float*>(sm + R_AF);
-            const float bt = small[SM_B + t];
-            if ((warp & 1) == 0) {
-                emit_block_row<0>(taddr, blk == 0, key_rows, t, bt, Af, sm + R_P);
-                emit_block_row<1>(taddr, blk == 1, key_rows, t, bt, Af, sm + R_P);
+        // Readback of A (key rows, TMEM lanes 0..63) and P (query rows, lanes
+        // 64..127): warp w covers the lanes of quadrant w mod 4 and output
+        // columns 16 (w / 4) .. + 15.  Lanes 0..15 and 16..31 of a warp hold
+        // rows of two different 16-row blocks, so the warp loads both blocks'
+        // column slices and each lane keeps its own.
+        {
+            const int q = warp & 3, s0 = 16 * (warp >> 2);
+            const int t = (32 * q + lane) & 63, blk = t >> 4;
+            const int b0 = 2 * (q & 1), b1 = b0 + 1;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * q) << 16);
+            float v0[16], v1[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) { v0[e] = 0.f; v1[e] = 0.f; }
+            if (s0 < 16 * (b0 + 1)) tmem_ld16(taddr + d_col(b0) + s0, v0);   // D_b has 16 (b+1) columns
+            if (s0 < 16 * (b1 + 1)) tmem_ld16(taddr + d_col(b1) + s0, v1);
+            tmem_wait_ld();
+            const bool lo = blk == b0;
+            const bool valid = s0 < 16 * (blk + 1);
+            if (q < 2) {
+                const float bt = small[SM_B + t];
+                float* Af = reinterpret_cast<float*>(sm + R_AF);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    float o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = s0 + 4 * s4 + e;
+                        const float val = lo ? v0[4 * s4 + e] : v1[4 * s4 + e];
+                        o4[e] = (valid && s < t) ? bt * val : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(Af + t * F_LD + s0 + 4 * s4) =
+                        make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
             } else {
-                emit_block_row<2>(taddr, blk == 2, key_rows, t, bt, Af, sm + R_P);
-                emit_block_row<3>(taddr, blk == 3, key_rows, t, bt, Af, sm + R_P);
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float o8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s0 + 8 * h8 + e;
+                        const float val = lo ? v0[8 * h8 + e] : v1[8 * h8 + e];
+                        o8[e] = (valid && s <= t) ? val : 0.f;
+                    }
+                    *reinterpret_cast<uint4*>(sm + R_P + sw128(t, (s0 >> 3) + h8)) = pack8(o8);
+                }
             }
         }
         tc_fence_before();
@@ -749,25 +740,28 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         __syncthreads();
         tc_fence_after();
 
-        // ---- N = (K^C)^T W -> cols [0,128); X = (K^C)^T U~ -> [128,256);
-        //      P W -> [256,384); O' = P U~ -> [384,512).  The last two are M=128
-        //      products whose A rows 0..63 are P (rows 64..127 read the next tile
-        //      and land in unused accumulator rows).
+        // ---- [N | X] = (K^C)^T [W | U~] -> cols [0,256), then
+        //      [P W | O'] = P [W | U~] -> [256,512), with W^T and U~^T stacked
+        //      as one 256-row operand.  The second pair is M=128 with A rows
+        //      0..63 = P (rows 64..127 read the next tile and land in unused
+        //      accumulator rows); it completes on bar2, so that the readback of
+        //      X overlaps it.
         if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 128);
+            const uint32_t idesc = idesc_bf16(128, 256);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint32_t off = ks * 32;
-                const uint64_t kc = desc_sw128(smem_u32(sm + R_KC + off));
-                const uint64_t pp = desc_sw128(smem_u32(sm + R_P + off));
-                const uint64_t wt = desc_sw128(smem_u32(sm + R_WT + off));
-                const uint64_t ut = desc_sw128(smem_u32(sm + R_UT + off));
-                mma_bf16(tbase + 0, kc, wt, idesc, ks > 0);
-                mma_bf16(tbase + 128, kc, ut, idesc, ks > 0);
-                mma_bf16(tbase + 256, pp, wt, idesc, ks > 0);
-                mma_bf16(tbase + 384, pp, ut, idesc, ks > 0);
+                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_KC + off)),
+                         desc_sw128(smem_u32(sm + R_WT + off)), idesc, ks > 0);
             }
             mma_commit(bar);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t off = ks * 32;
+                mma_bf16(tbase + 256, desc_sw128(smem_u32(sm + R_P + off)),
+                         desc_sw128(smem_u32(sm + R_WT + off)), idesc, ks > 0);
+            }
+            mma_commit(bar2);
         }
         ok = mbar_wait(bar, phase) && ok;
         phase ^= 1u;
@@ -779,6 +773,12 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             const uint32_t row = lane_base + lane;
             const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
             const int role = warp >> 2;
+            // The image of N overwrites W^T / U~^T, which the second pair of
+            // products still reads: only X (role 2) is written before bar2.
+            if (role != 2) {
+                ok = mbar_wait(bar2, phase2) && ok;
+                tc_fence_after();
+            }
             if (role == 0) {            // N[c][c' < 64] -> B rows c, K-block 0
                 tmem_row_to_tile<4>(taddr + 0, sm + R_PKG + PKG_B0, 0, row);
             } else if (role == 1) {     // N[c][c' >= 64] -> B rows c, K-block 1
@@ -810,6 +810,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             }
             if (tid < 128)
                 reinterpret_cast<float*>(sm + R_PKG + PKG_LAM)[tid] = small[SM_LAM + tid];
+            phase2 ^= 1u;
         }
         fence_async_smem();
         tc_fence_before();
