@@ -104,7 +104,7 @@ constexpr uint32_t R_ZQ = R_G;         // raw z [64][128] bf16, then raw q, of t
 constexpr uint32_t R_AF = 0;           // A fp32 [64][68]
 constexpr uint32_t R_TF = 17408;       // T fp32 [64][68]
 constexpr uint32_t R_TB = 34816;       // T bf16 [64][64] swizzled
-constexpr uint32_t R_XS = 43008;       // solve scratch, 1024 fp32
+constexpr uint32_t R_XS = 43008;       // solve scratch, 5 x 1024 fp32
 constexpr uint32_t F_LD = 68;           // fp32 row stride: 16-byte aligned rows, 4-bank skew
 // reuse after W / U~ (the solve's buffers and the A/P operands are dead)
 constexpr uint32_t R_WT = 0;           // W^T  [128 c][64 s] swizzled
@@ -170,7 +170,7 @@ constexpr int kL2Ahead = 6;                        // packages prefetched into L
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
-static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 1024 * 4 <= R_BKT, "solve scratch");
+static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 5 * 1024 * 4 <= R_BKT, "solve scratch");
 static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions");
 static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
@@ -314,6 +314,84 @@ __device__ __forceinline__ void solve_level(const float* __restrict__ Af, float*
     named_bar_sync(1, kSolveThreads);
 }
 
+// The last level (n = 32, one pair) with 4 x 4 register tiles and the
+// 32-term sums split four ways: thread (kg, i0, j0) of 256 sums terms
+// 8 kg .. 8 kg + 7 for rows i0 .. i0 + 3 and columns j0 .. j0 + 3, so that
+// each pair of 16-byte loads feeds sixteen FMAs; the four partial tiles are
+// then added.  Scratch: five 32 x 32 fp32 slices (X, then four partials).
+__device__ __forceinline__ void tile4x4_part(float (&acc)[4][4], const float* __restrict__ a, int lda,
+                                             const float* __restrict__ b, int ldb) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll
+    for (int m4 = 0; m4 < 8; m4 += 4) {
+        float ar[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float4 v = *reinterpret_cast<const float4*>(a + r * lda + m4);
+            ar[r][0] = v.x; ar[r][1] = v.y; ar[r][2] = v.z; ar[r][3] = v.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 bv = *reinterpret_cast<const float4*>(b + (m4 + e) * ldb);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                acc[r][0] = fmaf(ar[r][e], bv.x, acc[r][0]);
+                acc[r][1] = fmaf(ar[r][e], bv.y, acc[r][1]);
+                acc[r][2] = fmaf(ar[r][e], bv.z, acc[r][2]);
+                acc[r][3] = fmaf(ar[r][e], bv.w, acc[r][3]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void solve_level32(const float* __restrict__ Af, float* Tf, float* Xs,
+                                              int tid) {
+    constexpr int n = 32;
+    const int kg = tid >> 6, i0 = 4 * ((tid >> 3) & 7), j0 = 4 * (tid & 7), m0 = 8 * kg;
+    float* part = Xs + 1024 * (1 + kg);
+    float acc[4][4];
+    // partial sums of X = A21 T11
+    tile4x4_part(acc, Af + (n + i0) * F_LD + m0, F_LD, Tf + m0 * F_LD + j0, F_LD);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4*>(part + (i0 + r) * n + j0) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    named_bar_sync(1, kSolveThreads);
+    {
+        const int e = 4 * tid;
+        float4 x = *reinterpret_cast<const float4*>(Xs + 1024 + e);
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+            const float4 y = *reinterpret_cast<const float4*>(Xs + 1024 * (1 + k) + e);
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+        }
+        *reinterpret_cast<float4*>(Xs + e) = x;
+    }
+    named_bar_sync(1, kSolveThreads);
+    // partial sums of T22 X
+    tile4x4_part(acc, Tf + (n + i0) * F_LD + n + m0, F_LD, Xs + m0 * n + j0, n);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4*>(part + (i0 + r) * n + j0) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    named_bar_sync(1, kSolveThreads);
+    {
+        const int e = 4 * tid, r = e / n, c = e % n;
+        float4 x = *reinterpret_cast<const float4*>(Xs + 1024 + e);
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+            const float4 y = *reinterpret_cast<const float4*>(Xs + 1024 * (1 + k) + e);
+            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+        }
+        *reinterpret_cast<float4*>(Tf + (n + r) * F_LD + c) = make_float4(-x.x, -x.y, -x.z, -x.w);
+        *reinterpret_cast<float4*>(Tf + r * F_LD + n + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    named_bar_sync(1, kSolveThreads);
+}
+
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, float* Tf,
                                                  float* Xs, int tid) {
     if (tid < 64) {
@@ -335,7 +413,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, f
     solve_level<4>(Af, Tf, Xs, tid);
     solve_level<8>(Af, Tf, Xs, tid);
     solve_level<16>(Af, Tf, Xs, tid);
-    solve_level<32>(Af, Tf, Xs, tid);
+    solve_level32(Af, Tf, Xs, tid);
 }
 
 // Which chunk package slot `slot` holds: its first token t0 and length.
@@ -469,45 +547,39 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         in_phase ^= 1u;
         __syncthreads();
         int tt[2];
-        uint4 zraw[2], qraw[2];
+        uint4 qraw[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             tt[it] = it * 32 + (tid >> 4);
-            const bool in = tt[it] < len;
-            zraw[it] = in ? *reinterpret_cast<const uint4*>(sm + R_ZQ + tt[it] * 256 + c8 * 16)
-                          : make_uint4(0, 0, 0, 0);
-            qraw[it] = in ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
-                          : make_uint4(0, 0, 0, 0);
+            qraw[it] = tt[it] < len
+                           ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
+                           : make_uint4(0, 0, 0, 0);
         }
-        if (tid < kD) small[SM_A + tid] = __expf(small[SM_A + tid]);       // A -> e^A, in place
+        // Gate and scan are fused, thread = (channel c, 16-token block b): z of
+        // the block's tokens in channel c is read before G (which overlays the
+        // raw z and q tiles) is written.
+        const int gc = tid & 127, gb = tid >> 7;
+        float zc[16];
+        {
+            const __nv_bfloat16* zr = reinterpret_cast<const __nv_bfloat16*>(sm + R_ZQ);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zc[i] = __bfloat162float(zr[(16 * gb + i) * kD + gc]);
+        }
+        const float eAc = __expf(small[SM_A + gc]);
         if (tid < kC) small[SM_B + tid] = __uint_as_float(bt_raw << 16);   // bf16 -> fp32
         __syncthreads();                         // raw z, q are read before G is written
-        float eA[8];
-        load8f(small + SM_A + c8 * 8, eA);
 
-        // ---- gate g = -5 sigmoid(e^A z) into G (0 on padded rows)
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            float zf[8], g[8];
-            unpack8(zraw[it], zf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) g[e] = tt[it] < len ? gate_fast(eA[e], zf[e]) : 0.f;
-            float4* dst = reinterpret_cast<float4*>(G + tt[it] * G_LD + c8 * 8);
-            dst[0] = make_float4(g[0], g[1], g[2], g[3]);
-            dst[1] = make_float4(g[4], g[5], g[6], g[7]);
-        }
-        __syncthreads();
-
-        // ---- block-local cumulative log-decay L_t = G_t - r_b (16-token scans), and
+        // ---- gate g = -5 sigmoid(e^A z) (0 on padded rows) and the block-local
+        //      cumulative log-decay L_t = G_t - r_b (16-token scans), then the
         //      per-channel block factors from the block totals.
         {
-            const int c = tid & 127, b = tid >> 7;
+            const int c = gc, b = gb;
             float run = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float* p = G + (16 * b + i) * G_LD + c;
-                run += *p;
-                *p = run;
+                const int t = 16 * b + i;
+                run += t < len ? gate_fast(eAc, zc[i]) : 0.f;
+                G[t * G_LD + c] = run;
             }
             small[SM_TOT + b * 128 + c] = run;
             __syncthreads();
