@@ -678,29 +678,23 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             mma_commit(bar);
         }
 
-        // ---- column-side operands, transposed (thread = channel c, tokens of block b)
+        // ---- column-side operand (K^C)^T, transposed (thread = channel c, tokens
+        //      of block b); (b K^g)^T and (b V)^T follow during the solve.
         {
             const int c = tid & 127, b = tid >> 7;
             const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
-            const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_V);
-            const float er = small[SM_ER + b * 128 + c], ec = small[SM_EC + b * 128 + c];
+            const float ec = small[SM_EC + b * 128 + c];
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int s8 = 2 * b + it;
-                float bk[8], kc[8], bv[8];
+                float kc[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int s = s8 * 8 + e;
-                    const float bs = small[SM_B + s];
                     const float kf = s < len ? __bfloat162float(kraw[s * kD + c]) : 0.f;
-                    const float E = G[s * G_LD + c];
-                    bk[e] = bs * kf * E * er;                  // b_s k_s e^{G_s}
-                    kc[e] = kf * ec * __fdividef(1.0f, E);     // k_s e^{G_C - G_s}
-                    bv[e] = s < len ? bs * __bfloat162float(vraw[s * kD + c]) : 0.f;
+                    kc[e] = kf * ec * __fdividef(1.0f, G[s * G_LD + c]);   // k_s e^{G_C - G_s}
                 }
-                *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
                 *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
-                *reinterpret_cast<uint4*>(sm + R_BVT + sw128(c, s8)) = pack8(bv);
             }
         }
         ok = mbar_wait(bar, phase) && ok;
@@ -765,10 +759,34 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             float* Xs = reinterpret_cast<float*>(sm + R_XS);
             if (tid < kSolveThreads) {
                 solve_unit_lower(Af, Tf, Xs, tid);
-            } else if (tid == kLoadThread && nitem < n_items) {
-                // Raw k, v, z, q and G are dead now: an idle warp starts loading
-                // the next item's inputs while the solve runs.
-                issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
+            } else {
+                // Meanwhile the other warps build (b K^g)^T and (b V)^T, thread =
+                // (channel c, tokens 32 half .. 32 half + 31).
+                const int u = tid - kSolveThreads, c = u & 127, half = u >> 7;
+                const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
+                const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_V);
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int s8 = 4 * half + it;
+                    const float er = small[SM_ER + (s8 >> 1) * 128 + c];
+                    float bk[8], bv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s8 * 8 + e;
+                        const float bs = small[SM_B + s];
+                        const bool in = s < len;
+                        const float kf = in ? __bfloat162float(kraw[s * kD + c]) : 0.f;
+                        bk[e] = bs * kf * G[s * G_LD + c] * er;             // b_s k_s e^{G_s}
+                        bv[e] = in ? bs * __bfloat162float(vraw[s * kD + c]) : 0.f;
+                    }
+                    *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
+                    *reinterpret_cast<uint4*>(sm + R_BVT + sw128(c, s8)) = pack8(bv);
+                }
+                // Raw k, v, z, q and G are dead once all of these warps are
+                // here: one of them starts loading the next item's inputs.
+                named_bar_sync(3, kPrepThreads - kSolveThreads);
+                if (tid == kLoadThread && nitem < n_items)
+                    issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
             }
             __syncthreads();
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
