@@ -993,40 +993,57 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(dfree + 2);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
-    // Update warps: row c, columns jh .. jh + 15 of the tile (jh = 0 or 16).
-    const int c = 32 * (warp & 3) + lane;
+    // Update warp w holds rows 32 q4 .. 32 q4 + 31 (q4 = w mod 4) and tile
+    // columns jh .. jh + 15 (jh = 16 (w / 4)) in the layout of a 16x256b TMEM
+    // load: element e (0..15) of a thread is
+    //   row    erow(e) = 32 q4 + 16 (e >> 3) + 8 ((e >> 1) & 1) + lane / 4,
+    //   column ecol(e) = jh + 8 ((e >> 2) & 1) + 2 (lane mod 4) + (e & 1),
+    // so elements 2i and 2i + 1 are adjacent columns of one row.
+    const int q4 = warp & 3;
     const int jh = 16 * ((warp >> 2) & 1);
     const bool upd = warp < kUpdWarps;
-    const size_t srow = (((size_t)n * H + h) * kD + c) * kD + j0 + jh;
+    auto erow = [&](int e) { return 32 * q4 + 16 * (e >> 3) + 8 * ((e >> 1) & 1) + (lane >> 2); };
+    auto ecol = [&](int e) { return jh + 8 * ((e >> 2) & 1) + 2 * (lane & 3) + (e & 1); };
+    const size_t smat = ((size_t)n * H + h) * kD * kD + j0;        // this tile of S0 / S1
     float st[16];
-    auto store_row = [&](float* dst) {
+    auto store_state = [&](float* mat) {                             // mat: [128][128] of (n, h) + j0
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            reinterpret_cast<float4*>(dst)[q] =
-                make_float4(st[4 * q], st[4 * q + 1], st[4 * q + 2], st[4 * q + 3]);
+        for (int e = 0; e < 16; e += 2)
+            *reinterpret_cast<float2*>(mat + (size_t)erow(e) * kD + ecol(e)) = make_float2(st[e], st[e + 1]);
     };
     if (upd) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = S0 ? __ldg(reinterpret_cast<const float4*>(S0 + srow) + q)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            st[4 * q] = v.x; st[4 * q + 1] = v.y; st[4 * q + 2] = v.z; st[4 * q + 3] = v.w;
+        for (int e = 0; e < 16; e += 2) {
+            const float2 v = S0 ? __ldg(reinterpret_cast<const float2*>(S0 + smat + (size_t)erow(e) * kD + ecol(e)))
+                                : make_float2(0.f, 0.f);
+            st[e] = v.x;
+            st[e + 1] = v.y;
         }
     }
     if (nc == 0 || (smem_u32(smem_raw) & 1023u) != 0) {
         if (nc != 0 && tid == 0) set_status(status, kErrSmemAlign);
-        if (S1 && upd) store_row(S1 + srow);
+        if (S1 && upd) store_state(S1 + smat);
         return;
     }
 
-    // Copy p of the tile's S^T as the bf16 B operand: column c of rows
-    // jh .. jh + 15 (K-block c / 64).
+    // Copy p of the tile's S^T as the bf16 B operand (rows j, 128-byte-swizzled
+    // K-major over c): per 16-row half hh one transposing stmatrix of the four
+    // 8 x 8 matrices (m, k) = (i / 2, i mod 2): rows c = 32 q4 + 16 hh + 8 k ..,
+    // columns j = jh + 8 m ..  Thread t gives stored row j = jh + 8 m + t mod 8
+    // of matrix i = t / 8.
     auto write_st = [&](int p) {
-        uint8_t* kbase = sm + S_ST + p * 8192 + (c >> 6) * 4096 + ((c & 7) * 2);
+        const int i = lane >> 3, m = i >> 1, k = i & 1, jrow = jh + 8 * m + (lane & 7);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-            *reinterpret_cast<__nv_bfloat16*>(kbase + sw128(jh + jj, (c & 63) >> 3)) =
-                __float2bfloat16_rn(st[jj]);
+        for (int hh = 0; hh < 2; ++hh) {
+            const int c0 = 32 * q4 + 16 * hh + 8 * k;
+            uint32_t rg[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                const int e = 8 * hh + 4 * (ii >> 1) + 2 * (ii & 1);
+                rg[ii] = pack_bf16x2(st[e], st[e + 1]);
+            }
+            stmatrix_x4_trans(smem_u32(sm + S_ST + p * 8192 + (c0 >> 6) * 4096 + sw128(jrow, (c0 & 63) >> 3)), rg);
+        }
     };
 
     if (warp == 0) tmem_alloc<kTmemCols>(tslot);
@@ -1176,28 +1193,37 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
         if (!ok) *abort = 1;
     } else {
         // ------------------------------- state S <- lam (.) S - (N S) + X
-        const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + jh;
-        // X[c][jh .. jh + 15] and lam[c] of chunk m, loaded two chunks ahead of their use
-        auto load_x = [&](int m, uint4& a, uint4& b2, float& l) {
+        const uint32_t tl = tbase + ((uint32_t)(32 * q4) << 16) + jh;
+        // X at the thread's element pairs and lam at its four rows, of chunk m,
+        // loaded two chunks ahead of their use
+        struct XRegs { uint32_t x[8]; float lam[4]; };
+        auto load_x = [&](int m, XRegs& r) {
             const uint8_t* pk = pkg_of(m);
-            a = __ldg(reinterpret_cast<const uint4*>(pk + PKG_X + tile * 8192 + jtile_off(c, jh >> 3)));
-            b2 = __ldg(reinterpret_cast<const uint4*>(pk + PKG_X + tile * 8192 + jtile_off(c, (jh >> 3) + 1)));
-            l = __ldg(reinterpret_cast<const float*>(pk + PKG_LAM) + c);
+            const uint8_t* xt = pk + PKG_X + tile * 8192;
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const int jj = ecol(e);
+                r.x[e >> 1] = __ldg(reinterpret_cast<const uint32_t*>(xt + jtile_off(erow(e), jj >> 3) + (jj & 7) * 2));
+            }
+#pragma unroll
+            for (int hk = 0; hk < 4; ++hk)
+                r.lam[hk] = __ldg(reinterpret_cast<const float*>(pk + PKG_LAM) + erow(2 * hk + ((hk >> 1) * 4)));
         };
-        auto step = [&](int cc, uint4& x0, uint4& x1, float& lam) -> bool {
+        auto step = [&](int cc, XRegs& xr) -> bool {
             const int b = cc & 1;
             ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
             if (!ok) return false;
             tc_fence_after();
             float d[16];
-            tmem_ld16(tl + b * kDBuf, d);
+            tmem_ld_16x256b_x2(tl + b * kDBuf, *reinterpret_cast<float(*)[8]>(d));
+            tmem_ld_16x256b_x2(tl + (16u << 16) + b * kDBuf, *reinterpret_cast<float(*)[8]>(d + 8));
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float x8[8];
-                unpack8(q == 0 ? x0 : x1, x8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) st[8 * q + e] = fmaf(lam, st[8 * q + e], x8[e] - d[8 * q + e]);
+            for (int e = 0; e < 16; e += 2) {
+                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr.x[e >> 1]));
+                const float lam = xr.lam[2 * (e >> 3) + ((e >> 1) & 1)];
+                st[e] = fmaf(lam, st[e], x.x - d[e]);
+                st[e + 1] = fmaf(lam, st[e + 1], x.y - d[e + 1]);
             }
             if (cc + 1 < nc) {
                 // S^T copy (cc + 1) & 1 is still read by chunk cc - 1's O product
@@ -1211,26 +1237,24 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 if (cc + 1 < nc) mbar_arrive(stready + ((cc + 1) & 1));
                 mbar_arrive(dfree + b);
             }
-            if (cc + 2 < nc) load_x(cc + 2, x0, x1, lam);
+            if (cc + 2 < nc) load_x(cc + 2, xr);
             // Checkpoint: the state after every `ck.every` tokens of this sequence.
             if (ck.out) {
                 const int64_t done = (int64_t)(cc + 1) * kC;
                 if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
-                    store_row(ck.out + ((((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) *
-                                            kD + c) * kD + j0 + jh);
+                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * kD * kD + j0);
             }
             return true;
         };
-        uint4 xa0, xa1, xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
-        float la, lb = 0.f;
-        load_x(0, xa0, xa1, la);
-        if (nc > 1) load_x(1, xb0, xb1, lb);
+        XRegs xa, xb;
+        load_x(0, xa);
+        if (nc > 1) load_x(1, xb);
         for (int cc = 0; cc < nc; cc += 2) {
-            if (!step(cc, xa0, xa1, la)) break;
-            if (cc + 1 < nc && !step(cc + 1, xb0, xb1, lb)) break;
+            if (!step(cc, xa)) break;
+            if (cc + 1 < nc && !step(cc + 1, xb)) break;
         }
         if (!ok) *abort = 1;
-        if (S1) store_row(S1 + srow);
+        if (S1) store_state(S1 + smat);
     }
     if (!ok) set_status(status, kErrStateWait);
 

@@ -229,6 +229,30 @@ __host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
     return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
 
+// 16 lanes x 256 bits (8 columns), two column groups: thread t receives
+// lane L + t/4 in v[0..1] and lane L + 8 + t/4 in v[2..3], columns
+// C + 2 (t mod 4) + {0, 1}; v[4..7] are the same for columns C + 8 ...
+// (the layout of an m16n8 accumulator fragment).
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Four 8 x 8 bf16 matrices stored transposed: register i of thread t holds
+// fragment row t/4, columns 2 (t mod 4) and + 1 (low half first) of matrix
+// i, and thread t gives the shared address of stored row t mod 8 of matrix
+// t / 8 (16 bytes = the matrix's 8 fragment rows).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
