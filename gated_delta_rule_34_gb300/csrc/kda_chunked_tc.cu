@@ -220,6 +220,22 @@ __device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// The same 8 floats, for rows where the 8 lanes of a quarter-warp read
+// consecutive 32-byte pieces: lanes with `swap` take their upper half first,
+// so that each of the two 16-byte loads touches 8 distinct bank groups.
+__device__ __forceinline__ void load8f_sw(const float* p, float (&f)[8], bool swap) {
+    const float4 a = reinterpret_cast<const float4*>(p)[swap ? 1 : 0];
+    const float4 b = reinterpret_cast<const float4*>(p)[swap ? 0 : 1];
+    const float4 lo = swap ? b : a, hi = swap ? a : b;
+    f[0] = lo.x; f[1] = lo.y; f[2] = lo.z; f[3] = lo.w;
+    f[4] = hi.x; f[5] = hi.y; f[6] = hi.z; f[7] = hi.w;
+}
+__device__ __forceinline__ void store8f_sw(float* p, const float (&f)[8], bool swap) {
+    const float4 lo = make_float4(f[0], f[1], f[2], f[3]), hi = make_float4(f[4], f[5], f[6], f[7]);
+    reinterpret_cast<float4*>(p)[swap ? 1 : 0] = swap ? hi : lo;
+    reinterpret_cast<float4*>(p)[swap ? 0 : 1] = swap ? lo : hi;
+}
+
 // Copies TMEM columns [col0, col0 + 16 N16) of this thread's lane, as bf16,
 // into row `row` of a swizzled K-major tile (atoms 1024-aligned): column
 // col0 + x becomes element x of the row; elements 64 kb .. 64 kb + 63 sit in
@@ -550,7 +566,9 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         uint4 qraw[2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
-            tt[it] = it * 32 + (tid >> 4);
+            // tokens r and 63 - r: blocks b and 3 - b, so that every thread
+            // writes the same number of K^(i) variants (4 - b of them) below
+            tt[it] = it == 0 ? (tid >> 4) : 63 - (tid >> 4);
             qraw[it] = tt[it] < len
                            ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
                            : make_uint4(0, 0, 0, 0);
@@ -615,12 +633,13 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         // ---- row-side operands (thread = token t, 8 channels); G keeps E = e^{L} after.
         {
             const int kb = c8 >> 3, chk = c8 & 7;
+            const bool sw = (c8 >> 2) & 1;
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int t = tt[it], b = t >> 4;
                 float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], o8[8];
-                load8f(G + t * G_LD + c8 * 8, Lt);
-                load8f(small + SM_ER + b * 128 + c8 * 8, er);
+                load8f_sw(G + t * G_LD + c8 * 8, Lt, sw);
+                load8f_sw(small + SM_ER + b * 128 + c8 * 8, er, sw);
                 unpack8(t < len ? *reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16)
                                 : make_uint4(0, 0, 0, 0), kf);
                 unpack8(qraw[it], qf);
@@ -629,9 +648,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                     E[e] = __expf(Lt[e]);                      // e^{G_t - r_b} in [e^-80, 1]
                     Rr[e] = __fdividef(1.0f, E[e]);            // e^{r_b - G_t} in [1, e^80]
                 }
-                float4* gp = reinterpret_cast<float4*>(G + t * G_LD + c8 * 8);
-                gp[0] = make_float4(E[0], E[1], E[2], E[3]);
-                gp[1] = make_float4(E[4], E[5], E[6], E[7]);
+                store8f_sw(G + t * G_LD + c8 * 8, E, sw);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
                 *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(t, chk)) = pack8(o8);
@@ -649,7 +666,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x[e] = 1.f;
                     } else {
-                        load8f(small + SM_X + xidx(i, b) * 128 + c8 * 8, x);
+                        load8f_sw(small + SM_X + xidx(i, b) * 128 + c8 * 8, x, sw);
                     }
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * x[e];  // k e^{r_i - G_t}
@@ -793,7 +810,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             {
                 const int t = tid >> 3, ch = tid & 7;
                 float o8[8];
-                load8f(Tf + t * F_LD + ch * 8, o8);
+                load8f_sw(Tf + t * F_LD + ch * 8, o8, (ch >> 2) & 1);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     if (ch * 8 + e > t) o8[e] = 0.f;
