@@ -119,7 +119,8 @@ constexpr uint32_t SM_LAM = 2304;      // [128] e^{G_C}
 constexpr uint32_t SM_B = 2432;        // [64] beta
 constexpr uint32_t SM_A = 2496;        // [128] A row of the next item (prefetched)
 constexpr uint32_t R_SMALL_BYTES = (2496 + 128) * 4;
-constexpr uint32_t kInputBytes = 4 * 16384 + 512;    // q, k, v, z tiles and the A row
+constexpr uint32_t kInputBytesZQ = 2 * 16384 + 512;  // z, q tiles and the A row
+constexpr uint32_t kInputBytesKV = 2 * 16384;        // k, v tiles
 constexpr uint32_t R_BAR = R_SMALL + R_SMALL_BYTES;
 constexpr uint32_t P_SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
 
@@ -479,18 +480,20 @@ struct InputMaps {
 };
 
 // One thread issues the loads of an item's inputs: q, k, v, z tiles by TMA
-// and the A row by a bulk copy, all completing on `inbar`.  Rows past the
+// and the A row by a bulk copy: z, q and A (needed first) complete on
+// `inbar`, k and v on `kvbar`.  Rows past the
 // item's `len` belong to the next sequence (or are zero); the consumers mask
 // them.
 __device__ __forceinline__ void issue_item_tma(uint8_t* sm, const InputMaps& maps,
                                                const float* __restrict__ A, int64_t t0, int h,
-                                               uint64_t* inbar) {
-    mbar_expect_tx(inbar, kInputBytes);
-    tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
-    tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, inbar);
-    tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, inbar);
+                                               uint64_t* inbar, uint64_t* kvbar) {
+    mbar_expect_tx(inbar, kInputBytesZQ);
     tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
+    tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
     bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
+    mbar_expect_tx(kvbar, kInputBytesKV);
+    tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, kvbar);
+    tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, kvbar);
 }
 
 // beta's raw bits for threads < 64, converted only when the item starts so
@@ -520,6 +523,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
     uint64_t* inbar = bar + 1;
     uint64_t* bar2 = bar + 2;               // second half of the last products
+    uint64_t* kvbar = bar + 3;              // k, v tiles of the item
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 32);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
 
@@ -528,6 +532,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         mbar_init(bar, 1);
         mbar_init(inbar, 1);
         mbar_init(bar2, 1);
+        mbar_init(kvbar, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -537,6 +542,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     uint32_t phase = 0;                      // parity of the next completion of `bar`
     uint32_t in_phase = 0;                   // parity of the next completion of `inbar`
     uint32_t phase2 = 0;                     // parity of the next completion of `bar2`
+    uint32_t kv_phase = 0;                   // parity of the next completion of `kvbar`
     bool ok = true;
     const int c8 = tid & 15;                 // channels 8 c8 .. 8 c8 + 7 in the row-side passes
 
@@ -547,7 +553,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     uint32_t bt_raw = 0u;
     while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
     if (item < n_items) {
-        if (tid == kLoadThread) issue_item_tma(sm, maps, A, t0, (int)(item % H), inbar);
+        if (tid == kLoadThread) issue_item_tma(sm, maps, A, t0, (int)(item % H), inbar, kvbar);
         bt_raw = load_beta_raw(beta, t0, len, (int)(item % H), H, tid);
     }
 
@@ -627,6 +633,8 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             // The previous item's package store must have read the staging area
             // before the row-side pass overwrites it.
             if (tid == 0) bulk_wait_read_all();
+            ok = mbar_wait(kvbar, kv_phase) && ok;          // k, v of this item
+            kv_phase ^= 1u;
             __syncthreads();
         }
 
@@ -803,7 +811,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 // here: one of them starts loading the next item's inputs.
                 named_bar_sync(3, kPrepThreads - kSolveThreads);
                 if (tid == kLoadThread && nitem < n_items)
-                    issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar);
+                    issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar, kvbar);
             }
             __syncthreads();
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
