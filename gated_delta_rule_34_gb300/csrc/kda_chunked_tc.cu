@@ -450,6 +450,44 @@ __device__ __forceinline__ bool slot_chunk(const SeqMap& map, int64_t slot, int6
     return true;
 }
 
+// Copies TMEM columns [col, col + 32) of this thread's lane, as bf16, into
+// 16-byte chunks chunk0 .. chunk0 + 3 of row `row` of a 128-byte-swizzled
+// K-major tile.
+__device__ __forceinline__ void tmem32_to_swizzled(uint32_t taddr, uint8_t* tile, uint32_t row,
+                                                   uint32_t chunk0) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float v[16];
+        tmem_ld16(taddr + 16u * q, v);
+        tmem_wait_ld();
+        uint4 lo, hi;
+        lo.x = pack_bf16x2(v[0], v[1]);   lo.y = pack_bf16x2(v[2], v[3]);
+        lo.z = pack_bf16x2(v[4], v[5]);   lo.w = pack_bf16x2(v[6], v[7]);
+        hi.x = pack_bf16x2(v[8], v[9]);   hi.y = pack_bf16x2(v[10], v[11]);
+        hi.z = pack_bf16x2(v[12], v[13]); hi.w = pack_bf16x2(v[14], v[15]);
+        *reinterpret_cast<uint4*>(tile + sw128(row, chunk0 + 2 * q)) = lo;
+        *reinterpret_cast<uint4*>(tile + sw128(row, chunk0 + 2 * q + 1)) = hi;
+    }
+}
+
+// Copies TMEM columns [col, col + 32) of this thread's lane, as bf16, into
+// row `row` of one [rows][32] tile.
+__device__ __forceinline__ void tmem32_to_jtile(uint32_t taddr, uint8_t* tile, uint32_t row) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float v[16];
+        tmem_ld16(taddr + 16u * q, v);
+        tmem_wait_ld();
+        uint4 lo, hi;
+        lo.x = pack_bf16x2(v[0], v[1]);   lo.y = pack_bf16x2(v[2], v[3]);
+        lo.z = pack_bf16x2(v[4], v[5]);   lo.w = pack_bf16x2(v[6], v[7]);
+        hi.x = pack_bf16x2(v[8], v[9]);   hi.y = pack_bf16x2(v[10], v[11]);
+        hi.z = pack_bf16x2(v[12], v[13]); hi.w = pack_bf16x2(v[14], v[15]);
+        *reinterpret_cast<uint4*>(tile + jtile_off(row, 2 * q)) = lo;
+        *reinterpret_cast<uint4*>(tile + jtile_off(row, 2 * q + 1)) = hi;
+    }
+}
+
 // Copies TMEM columns [col0, col0 + 128) of this thread's lane, as bf16, into
 // row `row` of four [rows][32] tiles `tile_bytes` apart (columns 32 r .. 32 r
 // + 31 go to tile r).
@@ -855,14 +893,17 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         __syncthreads();
         tc_fence_after();
 
-        // ---- [N | X] = (K^C)^T [W | U~] -> cols [0,256), then
-        //      [P W | O'] = P [W | U~] -> [256,512), with W^T and U~^T stacked
-        //      as one 256-row operand.  The second pair is M=128 with A rows
-        //      0..63 = P (rows 64..127 read the next tile and land in unused
-        //      accumulator rows); it completes on bar2, so that the readback of
-        //      X overlaps it.
+        // ---- [N | X] = (K^C)^T [W | U~] -> cols [0,256), with W^T and U~^T
+        //      stacked as one 256-row operand; then P W -> [256,384) and
+        //      O' = P U~ -> [384,512) on bar2, so that the readback of X
+        //      overlaps them.  Both are M=128 products with P as 64 of the A
+        //      rows: P W reads A from 64 rows before P, so that its rows land
+        //      in TMEM lanes 64..127, and O' from P itself (lanes 0..63); the
+        //      other 64 A rows read neighbouring tiles and land in unused
+        //      accumulator rows.  That splits the readback evenly over the
+        //      four lane quadrants.
         if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 256);
+            const uint32_t idesc = idesc_bf16(128, 256), idesc_h = idesc_bf16(128, 128);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint32_t off = ks * 32;
@@ -873,8 +914,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint32_t off = ks * 32;
-                mma_bf16(tbase + 256, desc_sw128(smem_u32(sm + R_P + off)),
-                         desc_sw128(smem_u32(sm + R_WT + off)), idesc, ks > 0);
+                mma_bf16(tbase + 256, desc_sw128(smem_u32(sm + R_P - 8192 + off)),
+                         desc_sw128(smem_u32(sm + R_WT + off)), idesc_h, ks > 0);
+                mma_bf16(tbase + 384, desc_sw128(smem_u32(sm + R_P + off)),
+                         desc_sw128(smem_u32(sm + R_UT + off)), idesc_h, ks > 0);
             }
             mma_commit(bar2);
         }
@@ -882,38 +925,33 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         phase ^= 1u;
         tc_fence_after();
 
-        // ---- the package image, staged in shared memory
+        // ---- the package image, staged in shared memory.  Warp (quadrant q =
+        //      warp mod 4, slot s = warp / 4) does three 32-column jobs on the
+        //      rows of its lane quadrant: X tile s; then, after bar2 (the image
+        //      of N overwrites W^T / U~^T, which the second products read),
+        //      columns 32 s .. 32 s + 31 of N, and O' tile s (q < 2, token
+        //      rows) or those columns of Q' = Q^g - P W (q >= 2, token rows).
         {
-            const int lane_base = 32 * (warp & 3);
-            const uint32_t row = lane_base + lane;
-            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16);
-            const int role = warp >> 2;
-            // The image of N overwrites W^T / U~^T, which the second pair of
-            // products still reads: only X (role 2) is written before bar2.
-            if (role != 2) {
-                ok = mbar_wait(bar2, phase2) && ok;
-                tc_fence_after();
-            }
-            if (role == 0) {            // N[c][c' < 64] -> B rows c, K-block 0
-                tmem_row_to_tile<4>(taddr + 0, sm + R_PKG + PKG_B0, 0, row);
-            } else if (role == 1) {     // N[c][c' >= 64] -> B rows c, K-block 1
-                tmem_row_to_tile<4>(taddr + 64, sm + R_PKG + PKG_B0 + PKG_BK, 0, row);
-            } else if (role == 2) {     // X[c][j] -> four column tiles
-                tmem_row_to_jtiles(taddr + 128, sm + R_PKG + PKG_X, 8192, row);
-            } else if ((warp & 3) < 2) {  // O'[t][j] (lanes 0..63) -> four column tiles
-                tmem_row_to_jtiles(taddr + 384, sm + R_PKG + PKG_OP, 4096, row);
-            }
-            // Q'[t][c] = Q^g[t][c] - (P W)[t][c] -> B rows 128 + t; lanes 0..63 hold rows t.
-            if ((warp & 3) < 2 && role < 2) {
-                const uint32_t t = row, kb = (uint32_t)role;
+            const int q = warp & 3, sl = warp >> 2;
+            const uint32_t row = 32 * q + lane;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * q) << 16);
+            tmem32_to_jtile(taddr + 128 + 32 * sl, sm + R_PKG + PKG_X + sl * 8192, row);
+            ok = mbar_wait(bar2, phase2) && ok;
+            tc_fence_after();
+            const uint32_t kb = (uint32_t)sl >> 1, ch0 = 4 * ((uint32_t)sl & 1);
+            tmem32_to_swizzled(taddr + 32 * sl, sm + R_PKG + PKG_B0 + kb * PKG_BK, row, ch0);
+            if (q < 2) {
+                tmem32_to_jtile(taddr + 384 + 32 * sl, sm + R_PKG + PKG_OP + sl * 4096, row);
+            } else {
+                const uint32_t t = row - 64;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q2 = 0; q2 < 2; ++q2) {
                     float pw[16];
-                    tmem_ld16(taddr + 256 + 64 * kb + 16 * q4, pw);
+                    tmem_ld16(taddr + 256 + 32 * sl + 16 * q2, pw);
                     tmem_wait_ld();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const uint32_t ch = 2 * q4 + hh;
+                        const uint32_t ch = ch0 + 2 * q2 + hh;
                         float qg[8], o8[8];
                         unpack8(*reinterpret_cast<const uint4*>(sm + R_QG + kb * 8192 + sw128(t, ch)), qg);
 #pragma unroll
