@@ -488,6 +488,26 @@ __device__ __forceinline__ void tmem32_to_jtile(uint32_t taddr, uint8_t* tile, u
     }
 }
 
+// As tmem32_to_jtile, with the columns of each 16-column group stored in the
+// order 0 1 8 9 2 3 10 11 | 4 5 12 13 6 7 14 15, so that a reader holding
+// columns 2w, 2w + 1, 8 + 2w, 9 + 2w (the 16x256b fragment layout) finds them
+// in 8 contiguous bytes.  Used for the X tiles.
+__device__ __forceinline__ void tmem32_to_jtile_pairs(uint32_t taddr, uint8_t* tile, uint32_t row) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        float v[16];
+        tmem_ld16(taddr + 16u * q, v);
+        tmem_wait_ld();
+        uint4 lo, hi;
+        lo.x = pack_bf16x2(v[0], v[1]);   lo.y = pack_bf16x2(v[8], v[9]);
+        lo.z = pack_bf16x2(v[2], v[3]);   lo.w = pack_bf16x2(v[10], v[11]);
+        hi.x = pack_bf16x2(v[4], v[5]);   hi.y = pack_bf16x2(v[12], v[13]);
+        hi.z = pack_bf16x2(v[6], v[7]);   hi.w = pack_bf16x2(v[14], v[15]);
+        *reinterpret_cast<uint4*>(tile + jtile_off(row, 2 * q)) = lo;
+        *reinterpret_cast<uint4*>(tile + jtile_off(row, 2 * q + 1)) = hi;
+    }
+}
+
 // Copies TMEM columns [col0, col0 + 128) of this thread's lane, as bf16, into
 // row `row` of four [rows][32] tiles `tile_bytes` apart (columns 32 r .. 32 r
 // + 31 go to tile r).
@@ -935,7 +955,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             const int q = warp & 3, sl = warp >> 2;
             const uint32_t row = 32 * q + lane;
             const uint32_t taddr = tbase + ((uint32_t)(32 * q) << 16);
-            tmem32_to_jtile(taddr + 128 + 32 * sl, sm + R_PKG + PKG_X + sl * 8192, row);
+            tmem32_to_jtile_pairs(taddr + 128 + 32 * sl, sm + R_PKG + PKG_X + sl * 8192, row);
             ok = mbar_wait(bar2, phase2) && ok;
             tc_fence_after();
             const uint32_t kb = (uint32_t)sl >> 1, ch0 = 4 * ((uint32_t)sl & 1);
@@ -1263,10 +1283,17 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
         auto load_x = [&](int m, XRegs& r) {
             const uint8_t* pk = pkg_of(m);
             const uint8_t* xt = pk + PKG_X + tile * 8192;
+            // row erow(8 hh + 2 k): columns 2w, 2w + 1 (m = 0) and 8 + 2w, 9 + 2w
+            // (m = 1) of the warp's 16-column group, 8 contiguous bytes in the
+            // package's pair order (w = lane mod 4)
+            const uint32_t xoff = 8u * (lane & 1);
+            const int xch = 2 * (jh >> 4) + ((lane & 3) >> 1);
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const int jj = ecol(e);
-                r.x[e >> 1] = __ldg(reinterpret_cast<const uint32_t*>(xt + jtile_off(erow(e), jj >> 3) + (jj & 7) * 2));
+            for (int hk = 0; hk < 4; ++hk) {
+                const int e = 8 * (hk >> 1) + 2 * (hk & 1);
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(xt + jtile_off(erow(e), xch) + xoff));
+                r.x[e >> 1] = v.x;
+                r.x[(e + 4) >> 1] = v.y;
             }
 #pragma unroll
             for (int hk = 0; hk < 4; ++hk)
