@@ -422,29 +422,33 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
     return out
 
 
-def e2e_prefill(kda, xp, wp, steps: int):
-    """Prefill through the C ABI from pinned host buffers: H2D inputs, kernels, D2H o and S."""
+def e2e_prefill(kda, xp, wp, steps: int, segment_tokens: int = 8192):
+    """Prefill through the C ABI from page-locked host buffers (kda_chunk_prefill_from_host):
+    every step copies q, k, v, z, beta, A and S0 to the device and o and S back, the copies
+    of one token segment overlapping the kernels of another."""
     import torch
-    host = {n: xp[n].cpu().pin_memory() for n in ("q", "k", "v", "z", "beta", "A", "S0")}
-    dev = {n: torch.empty_like(xp[n]) for n in host}
+    host = {n: xp[n].cpu().contiguous().pin_memory() for n in ("q", "k", "v", "z", "beta", "A", "S0")}
+    dev = {n: torch.empty_like(xp[n]) for n in ("A", "S0")}
     B, T, H, dk = xp["q"].shape
     dv = xp["v"].shape[-1]
-    o = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
+    staging = {n: torch.empty_like(xp[n]) for n in ("q", "k", "v", "z", "beta")}
+    staging["o"] = torch.empty((B, T, H, dv), dtype=torch.bfloat16, device="cuda")
     S1 = torch.empty((B, H, dk, dv), dtype=torch.float32, device="cuda")
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    o_h = torch.empty((B, T, H, dv), dtype=torch.bfloat16).pin_memory()
     S_h = torch.empty(S1.shape, dtype=S1.dtype).pin_memory()
-    ws = torch.empty(kda.workspace_size(B, B, T, H, dk, dv, wp.chunk, torch.bfloat16),
-                     dtype=torch.uint8, device="cuda")
+    ws = torch.empty(kda.workspace_size(1, 1, min(segment_tokens, T), H, dk, dv, wp.chunk,
+                                        torch.bfloat16), dtype=torch.uint8, device="cuda")
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o.numel() * o.element_size() + S1.numel() * S1.element_size()
+    d2h = o_h.numel() * o_h.element_size() + S1.numel() * S1.element_size()
 
     def step():
-        for n in host:
+        for n in dev:
             dev[n].copy_(host[n], non_blocking=True)
-        kda.chunk_prefill(dev["q"], dev["k"], dev["v"], dev["z"], dev["beta"], dev["A"],
-                          initial_state=dev["S0"], chunk=wp.chunk, out=o, final_state=S1,
-                          workspace=ws)
-        o_h.copy_(o, non_blocking=True)
+        kda.chunk_prefill_from_host(host["q"], host["k"], host["v"], host["z"], host["beta"],
+                                    dev["A"], initial_state=dev["S0"],
+                                    segment_tokens=segment_tokens, out=o_h, final_state=S1,
+                                    staging=staging, workspace=ws, copy_streams=streams)
         S_h.copy_(S1, non_blocking=True)
 
     step()
@@ -457,7 +461,8 @@ def e2e_prefill(kda, xp, wp, steps: int):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     return {"value": B * T / (ms * 1e-3), "unit": "tokens/s", "ms": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": f"kda_chunk_prefill_from_host, {segment_tokens}-token segments"}
 
 
 def run_ncu_case(case: str) -> int:

@@ -52,6 +52,10 @@ def _declare(lib):
     lib.kda_chunk_prefill_workspace_size.restype = sz
     lib.kda_chunk_prefill_path.argtypes = [i32, i32, i32, i32]
     lib.kda_chunk_prefill_path.restype = i32
+    lib.kda_chunk_prefill_from_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, i32, i64, i32, i32, i32, i32, i64, vp,
+                                                sz, vp, vp, vp]
+    lib.kda_chunk_prefill_from_host.restype = i32
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.kda_decode_step.restype = i32
     lib.kda_chunk_prefill_static_workspace.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -177,6 +181,48 @@ def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chun
             _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
             chunk, _dtype_code(q.dtype), _ptr(checkpoints), int(checkpoint_every),
             checkpoints.shape[2], _ptr(workspace), ws_bytes, _stream(q.device)))
+    return out, final_state
+
+
+def chunk_prefill_from_host(q, k, v, z, beta, A, initial_state=None, segment_tokens: int = 8192,
+                            out=None, final_state=None, staging=None, workspace=None,
+                            copy_streams=None):
+    """Prefill through kda_chunk_prefill_from_host: q, k, v, z, beta and the returned o are
+    page-locked host tensors ([B, T, H, d] bf16, beta [B, T, H]); A and initial_state are on
+    the device.  The host copies of each ``segment_tokens``-token segment overlap the
+    kernels of another.  Returns (o on the host, final_state on the device).  Device staging
+    buffers, the workspace and the two copy streams are made with torch when not given
+    (``staging`` is a dict with q, k, v, z, beta, o device tensors of the host shapes).
+    The call is asynchronous on the current stream; ``out`` is valid after it syncs.
+    """
+    dev = A.device
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t in (q, k, v, z, beta):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous page-locked CPU tensors")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype).pin_memory()
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    if staging is None:
+        staging = {n: torch.empty(t.shape, dtype=t.dtype, device=dev)
+                   for n, t in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta), ("o", out))}
+    seg = max(64, min(int(segment_tokens), T))
+    need = workspace_size(1, 1, seg, H, dk, dv, 64, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if copy_streams is None:
+        copy_streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    _need_cuda(A, initial_state, final_state, workspace, *staging.values())
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().kda_chunk_prefill_from_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+        _ptr(staging["q"]), _ptr(staging["k"]), _ptr(staging["v"]), _ptr(staging["z"]),
+        _ptr(staging["beta"]), _ptr(staging["o"]), _ptr(initial_state), _ptr(final_state),
+        B, T, H, dk, dv, _dtype_code(q.dtype), int(segment_tokens), _ptr(workspace), ws_bytes,
+        _stream(dev), ctypes.c_void_p(copy_streams[0].cuda_stream),
+        ctypes.c_void_p(copy_streams[1].cuda_stream)))
     return out, final_state
 
 

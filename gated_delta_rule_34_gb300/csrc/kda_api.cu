@@ -199,6 +199,103 @@ kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const 
                         kda::CheckpointSpec{}, stream);
 }
 
+kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const void* v_h,
+                                       const void* z_h, const void* beta_h, const float* A,
+                                       void* o_h, void* q_d, void* k_d, void* v_d, void* z_d,
+                                       void* beta_d, void* o_d, const float* initial_state,
+                                       float* final_state, int B, int64_t T, int H, int d_k,
+                                       int d_v, kda_dtype dtype, int64_t segment_tokens,
+                                       void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream, cudaStream_t h2d_stream,
+                                       cudaStream_t d2h_stream) {
+    if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B <= 0 || T < 0 || H <= 0 || H > 65535)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%lld H=%d", B, (long long)T, H);
+    if (!use_chunked_tc(d_k, d_v, 64, dtype))
+        return fail(KDA_ERR_UNSUPPORTED, "kda_chunk_prefill_from_host supports bf16 with "
+                                         "d_k = d_v = 128 only (d_k=%d d_v=%d dtype=%d)",
+                    d_k, d_v, (int)dtype);
+    if (segment_tokens <= 0 || segment_tokens % 64 != 0)
+        return fail(KDA_ERR_INVALID_ARG, "segment_tokens must be a positive multiple of 64, got %lld",
+                    (long long)segment_tokens);
+    if (stream == h2d_stream || stream == d2h_stream || h2d_stream == d2h_stream)
+        return fail(KDA_ERR_INVALID_ARG, "the compute, host-to-device and device-to-host streams "
+                                         "must differ");
+    KDA_REQUIRE_PTR(A);
+    KDA_REQUIRE_PTR(final_state);
+    KDA_OPTIONAL_PTR(initial_state);
+    if (T == 0)
+        return prefill_impl(nullptr, nullptr, nullptr, nullptr, nullptr, A, nullptr, initial_state,
+                            final_state, nullptr, B, B, 0, H, d_k, d_v, 64, dtype, workspace,
+                            workspace_bytes, kda::CheckpointSpec{}, stream);
+    if (!q_h || !k_h || !v_h || !z_h || !beta_h || !o_h)
+        return fail(KDA_ERR_INVALID_ARG, "a host input or output pointer is NULL");
+    KDA_REQUIRE_PTR(q_d);
+    KDA_REQUIRE_PTR(k_d);
+    KDA_REQUIRE_PTR(v_d);
+    KDA_REQUIRE_PTR(z_d);
+    KDA_REQUIRE_PTR(beta_d);
+    KDA_REQUIRE_PTR(o_d);
+    const int64_t seg = segment_tokens < T ? segment_tokens : T;
+    const size_t need = kda::chunked_tc_workspace_bytes(1, seg, H);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
+                    workspace_bytes);
+
+    const size_t es = 2;                                    // bf16
+    const size_t qb = (size_t)H * d_k * es, vb = (size_t)H * d_v * es, bb = (size_t)H * es;
+    const size_t sb = (size_t)H * d_k * d_v;                // floats per sequence state
+    cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+    cudaError_t e = cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out, cudaEventDisableTiming);
+    // The copy streams start after the work already queued on `stream`.
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h2d_stream, ev_in, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h_stream, ev_in, 0);
+    kda_status st = KDA_OK;
+    auto cp = [&](void* dst, const void* src, size_t off, size_t n, cudaMemcpyKind kind,
+                  cudaStream_t s) {
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off,
+                                n, kind, s);
+    };
+    for (int b = 0; b < B && e == cudaSuccess && st == KDA_OK; ++b) {
+        for (int64_t t0 = 0; t0 < T && e == cudaSuccess && st == KDA_OK; t0 += seg) {
+            const int64_t len = (T - t0) < seg ? (T - t0) : seg;
+            const size_t tok = (size_t)b * T + t0;
+            cp(q_d, q_h, tok * qb, len * qb, cudaMemcpyHostToDevice, h2d_stream);
+            cp(k_d, k_h, tok * qb, len * qb, cudaMemcpyHostToDevice, h2d_stream);
+            cp(v_d, v_h, tok * vb, len * vb, cudaMemcpyHostToDevice, h2d_stream);
+            cp(z_d, z_h, tok * qb, len * qb, cudaMemcpyHostToDevice, h2d_stream);
+            cp(beta_d, beta_h, tok * bb, len * bb, cudaMemcpyHostToDevice, h2d_stream);
+            if (e == cudaSuccess) e = cudaEventRecord(ev_in, h2d_stream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev_in, 0);
+            if (e != cudaSuccess) break;
+            float* S = final_state + (size_t)b * sb;
+            const float* S_in = t0 == 0 ? (initial_state ? initial_state + (size_t)b * sb : nullptr) : S;
+            st = prefill_impl(static_cast<const char*>(q_d) + tok * qb,
+                              static_cast<const char*>(k_d) + tok * qb,
+                              static_cast<const char*>(v_d) + tok * vb,
+                              static_cast<const char*>(z_d) + tok * qb,
+                              static_cast<const char*>(beta_d) + tok * bb, A,
+                              static_cast<char*>(o_d) + tok * vb, S_in, S, nullptr, 1, 1, len, H,
+                              d_k, d_v, 64, dtype, workspace, workspace_bytes,
+                              kda::CheckpointSpec{}, stream);
+            if (st != KDA_OK) break;
+            if (e == cudaSuccess) e = cudaEventRecord(ev_out, stream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h_stream, ev_out, 0);
+            cp(o_h, o_d, tok * vb, len * vb, cudaMemcpyDeviceToHost, d2h_stream);
+        }
+    }
+    // `stream` finishes after the last copy back.
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out, d2h_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev_out, 0);
+    if (ev_in) cudaEventDestroy(ev_in);
+    if (ev_out) cudaEventDestroy(ev_out);
+    if (st != KDA_OK) return st;
+    return cuda_status(e, "kda_chunk_prefill_from_host");
+}
+
 kda_status kda_chunk_prefill_checkpoints(const void* q, const void* k, const void* v,
                                          const void* z, const void* beta, const float* A, void* o,
                                          const float* initial_state, float* final_state,

@@ -145,6 +145,47 @@ kda_status kda_chunk_prefill_checkpoints(const void *q, const void *k, const voi
                                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_chunk_prefill_from_host -- kda_chunk_prefill for a fixed-length batch
+ * whose inputs and output live in host memory, with the transfers overlapped
+ * with the kernels.  The layer computed is the one of kda_chunk_prefill; the
+ * pages describe no host interface, so this entry has no counterpart there.
+ *
+ * Each sequence is processed in segments of segment_tokens tokens: the
+ * segment's q, k, v, z, beta are copied to the device on h2d_stream, prefilled
+ * on `stream` (continuing from the state the previous segment left in
+ * final_state), and its o is copied back on d2h_stream, so that the copies of
+ * one segment run while another is computed.  The result equals one
+ * kda_chunk_prefill call on the whole batch.
+ *   q_h, k_h, v_h, z_h, beta_h  host inputs [B, T, H, d] (beta [B, T, H]) in
+ *                 `dtype`; page-locked (cudaHostAlloc) for the copies to
+ *                 overlap.
+ *   o_h           host output [B, T, H, d_v], page-locked.
+ *   q_d .. beta_d, o_d  device buffers of the same shapes (staging), written.
+ *   A             device [H, d_k] fp32.
+ *   initial_state nullable device [B, H, d_k, d_v] fp32 (read before the
+ *                 first segment of each sequence writes final_state, so it
+ *                 may equal final_state).
+ *   final_state   device [B, H, d_k, d_v] fp32, required: it carries the
+ *                 state from segment to segment and ends as the final state.
+ *   segment_tokens  a positive multiple of 64.
+ *   workspace     as for kda_chunk_prefill with B = 1, T = segment_tokens.
+ * Only the tensor-core path: bf16, d_k = d_v = 128, chunk 64; anything else
+ * returns KDA_ERR_UNSUPPORTED.  The three streams must differ; h2d_stream and
+ * d2h_stream first wait for the work already queued on `stream`, and `stream`
+ * finishes only after the last copy back, so synchronising `stream` covers
+ * the whole call.  Each call creates and destroys two CUDA events.
+ */
+kda_status kda_chunk_prefill_from_host(const void *q_h, const void *k_h, const void *v_h,
+                                       const void *z_h, const void *beta_h, const float *A,
+                                       void *o_h, void *q_d, void *k_d, void *v_d, void *z_d,
+                                       void *beta_d, void *o_d, const float *initial_state,
+                                       float *final_state, int B, int64_t T, int H, int d_k,
+                                       int d_v, kda_dtype dtype, int64_t segment_tokens,
+                                       void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream, cudaStream_t h2d_stream,
+                                       cudaStream_t d2h_stream);
+
+/*
  * Bytes of workspace kda_chunk_prefill needs for these sizes (0 if none).
  * For packed batches pass B = 1, T = total tokens and the sequence count; the
  * bound does not depend on the individual lengths.

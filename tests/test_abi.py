@@ -150,3 +150,21 @@ def test_spec_rejects_bad_arguments(L):
                              None) == INVALID
     assert L.kda_spec_commit(None, None, None, None, None, None, None, 0, 4, 2, 128, 128, 1,
                              None) == 0                                   # empty: no launch
+
+
+def test_from_host_rejects_bad_arguments(L):
+    f = _fake()
+    s1, s2, s3 = ctypes.c_void_p(1), ctypes.c_void_p(2), ctypes.c_void_p(3)
+
+    def call(**kw):
+        a = dict(d=128, dtype=1, seg=1024, st=(s1, s2, s3), S1=f)
+        a.update(kw)
+        return L.kda_chunk_prefill_from_host(f, f, f, f, f, f, f, f, f, f, f, f, f, None, a["S1"],
+                                             1, 4096, 2, a["d"], a["d"], a["dtype"], a["seg"], f,
+                                             1 << 30, *a["st"])
+    assert call(dtype=0) == UNSUPPORTED                       # fp32: not the tensor-core path
+    assert call(d=64) == UNSUPPORTED
+    assert call(seg=100) == INVALID                           # not a multiple of 64
+    assert call(seg=0) == INVALID
+    assert call(st=(s1, s1, s3)) == INVALID                   # streams must differ
+    assert call(S1=None) == INVALID                           # the state carrier is required
