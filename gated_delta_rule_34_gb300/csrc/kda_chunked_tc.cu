@@ -537,18 +537,20 @@ struct InputMaps {
     CUtensorMap q, k, v, z;
 };
 
-// One thread issues the loads of an item's inputs: q, k, v, z tiles by TMA
-// and the A row by a bulk copy: z, q and A (needed first) complete on
-// `inbar`, k and v on `kvbar`.  Rows past the
-// item's `len` belong to the next sequence (or are zero); the consumers mask
-// them.
-__device__ __forceinline__ void issue_item_tma(uint8_t* sm, const InputMaps& maps,
-                                               const float* __restrict__ A, int64_t t0, int h,
-                                               uint64_t* inbar, uint64_t* kvbar) {
+// One thread issues the loads of an item's inputs, q, k, v, z tiles by TMA
+// and the A row by a bulk copy, in two groups: z, q and A (read first)
+// complete on `inbar`, k and v on `kvbar`.  Rows past the item's `len` belong
+// to the next sequence (or are zero); the consumers mask them.
+__device__ __forceinline__ void issue_item_zq(uint8_t* sm, const InputMaps& maps,
+                                              const float* __restrict__ A, int64_t t0, int h,
+                                              uint64_t* inbar) {
     mbar_expect_tx(inbar, kInputBytesZQ);
     tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
     tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
     bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
+}
+__device__ __forceinline__ void issue_item_kv(uint8_t* sm, const InputMaps& maps, int64_t t0, int h,
+                                              uint64_t* kvbar) {
     mbar_expect_tx(kvbar, kInputBytesKV);
     tma_load_3d(sm + R_K, &maps.k, 0, h, (int)t0, kvbar);
     tma_load_3d(sm + R_V, &maps.v, 0, h, (int)t0, kvbar);
@@ -611,7 +613,10 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     uint32_t bt_raw = 0u;
     while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
     if (item < n_items) {
-        if (tid == kLoadThread) issue_item_tma(sm, maps, A, t0, (int)(item % H), inbar, kvbar);
+        if (tid == kLoadThread) {
+            issue_item_zq(sm, maps, A, t0, (int)(item % H), inbar);
+            issue_item_kv(sm, maps, t0, (int)(item % H), kvbar);
+        }
         bt_raw = load_beta_raw(beta, t0, len, (int)(item % H), H, tid);
     }
 
@@ -761,23 +766,28 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             mma_commit(bar);
         }
 
-        // ---- column-side operand (K^C)^T, transposed (thread = channel c, tokens
-        //      of block b); (b K^g)^T and (b V)^T follow during the solve.
+        // ---- column-side operands (K^C)^T and (b K^g)^T, transposed (thread =
+        //      channel c, tokens of block b): the last readers of G, so that the
+        //      next item's z and q can be copied in from the solve on; (b V)^T
+        //      follows during the solve.
         {
             const int c = tid & 127, b = tid >> 7;
             const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
-            const float ec = small[SM_EC + b * 128 + c];
+            const float er = small[SM_ER + b * 128 + c], ec = small[SM_EC + b * 128 + c];
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int s8 = 2 * b + it;
-                float kc[8];
+                float kc[8], bk[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int s = s8 * 8 + e;
                     const float kf = s < len ? __bfloat162float(kraw[s * kD + c]) : 0.f;
-                    kc[e] = kf * ec * __fdividef(1.0f, G[s * G_LD + c]);   // k_s e^{G_C - G_s}
+                    const float E = G[s * G_LD + c];
+                    kc[e] = kf * ec * __fdividef(1.0f, E);             // k_s e^{G_C - G_s}
+                    bk[e] = small[SM_B + s] * kf * E * er;             // b_s k_s e^{G_s}
                 }
                 *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
+                *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
             }
         }
         ok = mbar_wait(bar, phase) && ok;
@@ -843,33 +853,29 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             if (tid < kSolveThreads) {
                 solve_unit_lower(Af, Tf, Xs, tid);
             } else {
-                // Meanwhile the other warps build (b K^g)^T and (b V)^T, thread =
-                // (channel c, tokens 32 half .. 32 half + 31).
+                // G and the raw z, q are dead: the next item's z, q and A row
+                // start loading now.
+                if (tid == kLoadThread && nitem < n_items)
+                    issue_item_zq(sm, maps, A, nt0, (int)(nitem % H), inbar);
+                // Meanwhile the other warps build (b V)^T, thread = (channel c,
+                // tokens 32 half .. 32 half + 31).
                 const int u = tid - kSolveThreads, c = u & 127, half = u >> 7;
-                const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
                 const __nv_bfloat16* vraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_V);
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
                     const int s8 = 4 * half + it;
-                    const float er = small[SM_ER + (s8 >> 1) * 128 + c];
-                    float bk[8], bv[8];
+                    float bv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = s8 * 8 + e;
-                        const float bs = small[SM_B + s];
-                        const bool in = s < len;
-                        const float kf = in ? __bfloat162float(kraw[s * kD + c]) : 0.f;
-                        bk[e] = bs * kf * G[s * G_LD + c] * er;             // b_s k_s e^{G_s}
-                        bv[e] = in ? bs * __bfloat162float(vraw[s * kD + c]) : 0.f;
+                        bv[e] = s < len ? small[SM_B + s] * __bfloat162float(vraw[s * kD + c]) : 0.f;
                     }
-                    *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
                     *reinterpret_cast<uint4*>(sm + R_BVT + sw128(c, s8)) = pack8(bv);
                 }
-                // Raw k, v, z, q and G are dead once all of these warps are
-                // here: one of them starts loading the next item's inputs.
+                // Raw k and v are dead once all of these warps are here.
                 named_bar_sync(3, kPrepThreads - kSolveThreads);
                 if (tid == kLoadThread && nitem < n_items)
-                    issue_item_tma(sm, maps, A, nt0, (int)(nitem % H), inbar, kvbar);
+                    issue_item_kv(sm, maps, nt0, (int)(nitem % H), kvbar);
             }
             __syncthreads();
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
