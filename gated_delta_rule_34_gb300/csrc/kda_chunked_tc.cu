@@ -607,25 +607,36 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     const int c8 = tid & 15;                 // channels 8 c8 .. 8 c8 + 7 in the row-side passes
 
     // The first item's inputs; later items' inputs are issued one item ahead.
-    int64_t item = blockIdx.x;
+    // item = slot * H + head, walked as (slot, head) so that no 64-bit
+    // division is left in the loop.
+    const int step_slot = (int)(gridDim.x / (unsigned)H), step_head = (int)(gridDim.x % (unsigned)H);
+    auto advance = [&](int64_t& it, int64_t& sl, int& hd) {
+        it += gridDim.x;
+        sl += step_slot;
+        hd += step_head;
+        if (hd >= H) { hd -= H; ++sl; }
+    };
+    int64_t item = blockIdx.x, slot = blockIdx.x / (unsigned)H;
+    int head = (int)(blockIdx.x % (unsigned)H);
     int64_t t0 = 0;
     int len = 0;
     uint32_t bt_raw = 0u;
-    while (item < n_items && !slot_chunk(map, item / H, t0, len)) item += gridDim.x;
+    while (item < n_items && !slot_chunk(map, slot, t0, len)) advance(item, slot, head);
     if (item < n_items) {
         if (tid == kLoadThread) {
-            issue_item_zq(sm, maps, A, t0, (int)(item % H), inbar);
-            issue_item_kv(sm, maps, t0, (int)(item % H), kvbar);
+            issue_item_zq(sm, maps, A, t0, head, inbar);
+            issue_item_kv(sm, maps, t0, head, kvbar);
         }
-        bt_raw = load_beta_raw(beta, t0, len, (int)(item % H), H, tid);
+        bt_raw = load_beta_raw(beta, t0, len, head, H, tid);
     }
 
     while (item < n_items) {
         uint8_t* pkg = ws + WS_HEADER + (size_t)item * PKG_BYTES;
         // The next item this CTA processes (skipping slots that hold no chunk).
-        int64_t nitem = item + gridDim.x, nt0 = 0;
-        int nlen = 0;
-        while (nitem < n_items && !slot_chunk(map, nitem / H, nt0, nlen)) nitem += gridDim.x;
+        int64_t nitem = item, nslot = slot, nt0 = 0;
+        int nhead = head, nlen = 0;
+        advance(nitem, nslot, nhead);
+        while (nitem < n_items && !slot_chunk(map, nslot, nt0, nlen)) advance(nitem, nslot, nhead);
 
         // ---- inputs of this item (issued during the previous one) -> registers
         ok = mbar_wait(inbar, in_phase) && ok;
@@ -843,7 +854,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         }
         tc_fence_before();
         __syncthreads();
-        if (nitem < n_items) bt_raw = load_beta_raw(beta, nt0, nlen, (int)(nitem % H), H, tid);
+        if (nitem < n_items) bt_raw = load_beta_raw(beta, nt0, nlen, nhead, H, tid);
 
         // ---- T = (I + A)^{-1}
         {
@@ -856,7 +867,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 // G and the raw z, q are dead: the next item's z, q and A row
                 // start loading now.
                 if (tid == kLoadThread && nitem < n_items)
-                    issue_item_zq(sm, maps, A, nt0, (int)(nitem % H), inbar);
+                    issue_item_zq(sm, maps, A, nt0, nhead, inbar);
                 // Meanwhile the other warps build (b V)^T, thread = (channel c,
                 // tokens 32 half .. 32 half + 31).
                 const int u = tid - kSolveThreads, c = u & 127, half = u >> 7;
@@ -875,7 +886,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 // Raw k and v are dead once all of these warps are here.
                 named_bar_sync(3, kPrepThreads - kSolveThreads);
                 if (tid == kLoadThread && nitem < n_items)
-                    issue_item_kv(sm, maps, nt0, (int)(nitem % H), kvbar);
+                    issue_item_kv(sm, maps, nt0, nhead, kvbar);
             }
             __syncthreads();
             // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
@@ -1000,6 +1011,8 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             bulk_commit();
         }
         item = nitem;
+        slot = nslot;
+        head = nhead;
         t0 = nt0;
         len = nlen;
     }
