@@ -653,17 +653,17 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                            ? *reinterpret_cast<const uint4*>(sm + R_ZQ + 16384 + tt[it] * 256 + c8 * 16)
                            : make_uint4(0, 0, 0, 0);
         }
-        // Gate and scan are fused, thread = (channel c, 16-token block b): z of
-        // the block's tokens in channel c is read before G (which overlays the
-        // raw z and q tiles) is written.
-        const int gc = tid & 127, gb = tid >> 7;
-        float zc[16];
+        // Gate and scan are fused, thread = (channel pair gc, gc + 1; tokens
+        // 16 gb + 8 hb .. + 7): z of those tokens and channels is read before G
+        // (which overlays the raw z and q tiles) is written.
+        const int hb = tid & 1, gc = 2 * ((tid >> 1) & 63), gb = tid >> 7;
+        uint32_t zc[8];
         {
-            const __nv_bfloat16* zr = reinterpret_cast<const __nv_bfloat16*>(sm + R_ZQ);
+            const uint32_t* zr = reinterpret_cast<const uint32_t*>(sm + R_ZQ);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) zc[i] = __bfloat162float(zr[(16 * gb + i) * kD + gc]);
+            for (int i = 0; i < 8; ++i) zc[i] = zr[(16 * gb + 8 * hb + i) * (kD / 2) + (gc >> 1)];
         }
-        const float eAc = __expf(small[SM_A + gc]);
+        const float eA0 = __expf(small[SM_A + gc]), eA1 = __expf(small[SM_A + gc + 1]);
         if (tid < kC) small[SM_B + tid] = __uint_as_float(bt_raw << 16);   // bf16 -> fp32
         __syncthreads();                         // raw z, q are read before G is written
 
@@ -671,16 +671,31 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         //      cumulative log-decay L_t = G_t - r_b (16-token scans), then the
         //      per-channel block factors from the block totals.
         {
-            const int c = gc, b = gb;
-            float run = 0.f;
+            // Each half-block scans its 8 tokens; the second half then adds the
+            // first half's total (from the neighbouring lane).
+            float s0[8], s1[8], run0 = 0.f, run1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 16 * b + i;
-                run += t < len ? gate_fast(eAc, zc[i]) : 0.f;
-                G[t * G_LD + c] = run;
+            for (int i = 0; i < 8; ++i) {
+                const bool in = 16 * gb + 8 * hb + i < len;
+                const float2 zz = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zc[i]));
+                run0 += in ? gate_fast(eA0, zz.x) : 0.f;
+                run1 += in ? gate_fast(eA1, zz.y) : 0.f;
+                s0[i] = run0;
+                s1[i] = run1;
             }
-            small[SM_TOT + b * 128 + c] = run;
+            const float p0 = __shfl_xor_sync(0xffffffffu, run0, 1);
+            const float p1 = __shfl_xor_sync(0xffffffffu, run1, 1);
+            const float a0 = hb ? p0 : 0.f, a1 = hb ? p1 : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float2*>(G + (16 * gb + 8 * hb + i) * G_LD + gc) =
+                    make_float2(s0[i] + a0, s1[i] + a1);
+            if (hb) {
+                small[SM_TOT + gb * 128 + gc] = run0 + a0;
+                small[SM_TOT + gb * 128 + gc + 1] = run1 + a1;
+            }
             __syncthreads();
+            const int c = tid & 127, b = tid >> 7;
             const float t0v = small[SM_TOT + c], t1v = small[SM_TOT + 128 + c];
             const float t2v = small[SM_TOT + 256 + c], t3v = small[SM_TOT + 384 + c];
             const float r1 = t0v, r2 = t0v + t1v, r3 = r2 + t2v, rc = r3 + t3v;
