@@ -920,25 +920,32 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         __syncthreads();
         tc_fence_after();
 
-        // ---- W^T = (b K^g)^T T^T -> cols [0,64), U~^T = (b V)^T T^T -> cols [64,128)
+        // ---- W^T = (b K^g)^T T^T -> cols [0,64) on bar, U~^T = (b V)^T T^T ->
+        //      cols [64,128) on bar2, so that W^T's readback overlaps U~^T.
         if (tid == 0) {
             const uint32_t idesc = idesc_bf16(128, 64);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bd = desc_sw128(smem_u32(sm + R_TB + ks * 32));
-                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_BKT + ks * 32)), bd, idesc, ks > 0);
-                mma_bf16(tbase + 64, desc_sw128(smem_u32(sm + R_BVT + ks * 32)), bd, idesc, ks > 0);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_BKT + ks * 32)),
+                         desc_sw128(smem_u32(sm + R_TB + ks * 32)), idesc, ks > 0);
             mma_commit(bar);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tbase + 64, desc_sw128(smem_u32(sm + R_BVT + ks * 32)),
+                         desc_sw128(smem_u32(sm + R_TB + ks * 32)), idesc, ks > 0);
+            mma_commit(bar2);
         }
-        ok = mbar_wait(bar, phase) && ok;
-        phase ^= 1u;
-        tc_fence_after();
-        // W^T and U~^T as bf16 K-major operands, thread = row (channel / column).
-        if (warp < 8) {
-            const int lane_base = 32 * (warp & 3);
-            const uint32_t taddr = tbase + ((uint32_t)lane_base << 16) + (warp < 4 ? 0u : 64u);
-            tmem_row_to_tile<4>(taddr, sm + (warp < 4 ? R_WT : R_UT), 0, lane_base + lane);
+        // W^T and U~^T as bf16 K-major operands, thread = row (channel / column):
+        // warps 0-7 take W^T, warps 8-15 U~^T, 32 columns each.
+        {
+            const bool wpart = warp < 8;
+            const uint32_t half = (uint32_t)(warp >> 2) & 1u;
+            ok = mbar_wait(wpart ? bar : bar2, wpart ? phase : phase2) && ok;
+            tc_fence_after();
+            const uint32_t taddr = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (wpart ? 0u : 64u) + 32 * half;
+            tmem32_to_swizzled(taddr, sm + (wpart ? R_WT : R_UT), 32 * (warp & 3) + lane, 4 * half);
+            phase ^= 1u;
+            phase2 ^= 1u;
         }
         fence_async_smem();
         tc_fence_before();
