@@ -128,10 +128,146 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// decode_stream_kernel: the same step for d_k = d_v = 128, persistent, with
+// the next (b, h) state streamed in while the current one is finished.  Each
+// thread copies its own 16 x 16 bytes of the next state into its own slots of
+// shared memory with cp.async (so no barrier guards the buffer), issued as soon
+// as the current state's values have been consumed from registers; the
+// reductions, the output and the 64 KiB state write of the current pair then
+// overlap the next pair's read.  Two CTAs per SM keep about 128 KiB of state
+// reads in flight per SM.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16_cg(void* dst_smem, const void* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_own() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+constexpr uint32_t kStreamSmem = kDecodeRows * kDecodeThreads * 16;   // 64 KiB
+
+template <typename T>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+decode_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                     const T* __restrict__ z, const T* __restrict__ beta,
+                     const float* __restrict__ A, float* __restrict__ state, T* __restrict__ o,
+                     int H, int n_pairs) {
+    constexpr int d = 128;
+    extern __shared__ float4 s_buf[];                 // [kDecodeRows][kDecodeThreads]
+    __shared__ float s_a[d], s_k[d], s_q[d];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int rg = lane >> 2, cg = lane & 3;
+    const int j0 = warp * 16 + cg * 4;
+    auto prefetch = [&](int bh) {
+        const float* Sbh = state + (size_t)bh * d * d;
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i)
+            cp_async16_cg(&s_buf[i * kDecodeThreads + tid], Sbh + (size_t)(rg + 8 * i) * d + j0);
+    };
+    int bh = blockIdx.x;
+    if (bh < n_pairs) prefetch(bh);
+    for (; bh < n_pairs; bh += gridDim.x) {
+        const int h = bh % H;
+        float* Sbh = state + (size_t)bh * d * d;
+        __syncthreads();                              // the previous pair is done with s_a, s_k, s_q
+        if (tid < d) {
+            const size_t idx = (size_t)bh * d + tid;
+            s_k[tid] = to_f32(k[idx]);
+            s_q[tid] = to_f32(q[idx]);
+            s_a[tid] = expf(gate_accurate(expf(A[(size_t)h * d + tid]), to_f32(z[idx])));
+        }
+        const float b = to_f32(beta[bh]);
+        float vj[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vj[c] = to_f32(v[(size_t)bh * d + j0 + c]);
+        __syncthreads();
+        float kq = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) kq += s_k[lane + 32 * m] * s_q[lane + 32 * m];
+        kq = warp_sum(kq);
+
+        cp_async_wait_all_own();                      // this thread's slots of the state
+        float4 s[kDecodeRows];
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) s[i] = s_buf[i * kDecodeThreads + tid];
+        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) {
+            const int r = rg + 8 * i;
+            const float a = s_a[r], kr = s_k[r], qr = s_q[r];
+            s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
+            pk[0] = fmaf(s[i].x, kr, pk[0]); pk[1] = fmaf(s[i].y, kr, pk[1]);
+            pk[2] = fmaf(s[i].z, kr, pk[2]); pk[3] = fmaf(s[i].w, kr, pk[3]);
+            pq[0] = fmaf(s[i].x, qr, pq[0]); pq[1] = fmaf(s[i].y, qr, pq[1]);
+            pq[2] = fmaf(s[i].z, qr, pq[2]); pq[3] = fmaf(s[i].w, qr, pq[3]);
+        }
+        // every s[i] has been consumed: the slots can take the next pair
+        if (bh + (int)gridDim.x < n_pairs) prefetch(bh + gridDim.x);
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
+                pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
+            }
+        }
+        float u[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u[c] = b * (vj[c] - pk[c]);
+        if (rg == 0) {
+            T* ob = o + (size_t)bh * d + j0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ob[c] = from_f32<T>(fmaf(u[c], kq, pq[c]));
+        }
+#pragma unroll
+        for (int i = 0; i < kDecodeRows; ++i) {
+            const int r = rg + 8 * i;
+            const float kr = s_k[r];
+            float4 w;
+            w.x = fmaf(kr, u[0], s[i].x);
+            w.y = fmaf(kr, u[1], s[i].y);
+            w.z = fmaf(kr, u[2], s[i].z);
+            w.w = fmaf(kr, u[3], s[i].w);
+            __stcs(reinterpret_cast<float4*>(Sbh + (size_t)r * d + j0), w);
+        }
+    }
+    cp_async_wait_all_own();
+}
+
 cudaError_t run_decode(const void* q, const void* k, const void* v, const void* z,
                        const void* beta, const float* A, float* state, void* o, int B, int H,
                        int dk, int dv, bool bf16, cudaStream_t stream) {
     const unsigned grid = (unsigned)((int64_t)B * H);
+    if (dk == 128 && dv == 128) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int n_pairs = B * H;
+        const unsigned sgrid = (unsigned)(n_pairs < 2 * sms ? n_pairs : 2 * sms);
+        if (bf16) {
+            using T = __nv_bfloat16;
+            e = cudaFuncSetAttribute(decode_stream_kernel<T>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem);
+            if (e != cudaSuccess) return e;
+            decode_stream_kernel<T><<<sgrid, kDecodeThreads, kStreamSmem, stream>>>(
+                static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+                static_cast<const T*>(z), static_cast<const T*>(beta), A, state,
+                static_cast<T*>(o), H, n_pairs);
+        } else {
+            e = cudaFuncSetAttribute(decode_stream_kernel<float>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem);
+            if (e != cudaSuccess) return e;
+            decode_stream_kernel<float><<<sgrid, kDecodeThreads, kStreamSmem, stream>>>(
+                static_cast<const float*>(q), static_cast<const float*>(k),
+                static_cast<const float*>(v), static_cast<const float*>(z),
+                static_cast<const float*>(beta), A, state, static_cast<float*>(o), H, n_pairs);
+        }
+        return cudaGetLastError();
+    }
     if (bf16) {
         using T = __nv_bfloat16;
         decode_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
