@@ -85,17 +85,17 @@ constexpr int kLoadThread = 480;       // lane 0 of the last warp issues the inp
 // shared memory (offsets from a 1024-byte aligned base).  The package image of
 // one item is staged in [0, PKG_BYTES) and stored asynchronously while the next
 // item starts: that range only holds buffers the next item first writes after
-// its scan (A-stack, K^(i), (b K^g)^T, (b V)^T), so the store has time to drain.
+// its scan (A-stack, K^(i), b K^g, (b V)^T), so the store has time to drain.
 constexpr uint32_t R_AST = 0;          // A-stack [128][128] swizzled (k rows, then q rows)
 constexpr uint32_t R_KV = 32768;       // K^(i) variants, 40 KB
-constexpr uint32_t R_BKT = 73728;      // (b K^g)^T [128 c][64 s] swizzled
+constexpr uint32_t R_BKT = 73728;      // b K^g [64 s][128 c]: two 64-channel halves, swizzled
 constexpr uint32_t R_BVT = 90112;      // (b V)^T  [128 j][64 s] swizzled
 constexpr uint32_t R_G = 106496;       // L = block-local cumulative gate, fp32 [64][132];
                                        // also raw z and q of the next item (prefetched)
 constexpr uint32_t G_LD = 132;
 constexpr uint32_t R_K = 141312;       // raw k [64][128] bf16
 constexpr uint32_t R_V = 157696;       // raw v [64][128] bf16
-constexpr uint32_t R_KC = 174080;      // (K^C)^T  [128 c][64 s] swizzled
+constexpr uint32_t R_KC = 174080;      // K^C [64 s][128 c]: two 64-channel halves, swizzled
 constexpr uint32_t R_P = 190464;       // P        [64 t][64 s] swizzled (follows K^C)
 constexpr uint32_t R_QG = 198656;      // Q^g      [64 t][128 c] swizzled, two K-blocks
 constexpr uint32_t R_SMALL = 215040;   // per-channel constants, beta
@@ -727,16 +727,20 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             __syncthreads();
         }
 
-        // ---- row-side operands (thread = token t, 8 channels); G keeps E = e^{L} after.
+        // ---- operands from the token rows (thread = token t, 8 channels).  The
+        //      key-side operands of the later products, (K^C)^T and (b K^g)^T,
+        //      are written here too, as token rows: their MMAs read them
+        //      MN-major, so no transposed copy is built.
         {
             const int kb = c8 >> 3, chk = c8 & 7;
             const bool sw = (c8 >> 2) & 1;
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int t = tt[it], b = t >> 4;
-                float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], o8[8];
+                float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], ec[8], o8[8];
                 load8f_sw(G + t * G_LD + c8 * 8, Lt, sw);
                 load8f_sw(small + SM_ER + b * 128 + c8 * 8, er, sw);
+                load8f_sw(small + SM_EC + b * 128 + c8 * 8, ec, sw);
                 unpack8(t < len ? *reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16)
                                 : make_uint4(0, 0, 0, 0), kf);
                 unpack8(qraw[it], qf);
@@ -745,7 +749,6 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                     E[e] = __expf(Lt[e]);                      // e^{G_t - r_b} in [e^-80, 1]
                     Rr[e] = __fdividef(1.0f, E[e]);            // e^{r_b - G_t} in [1, e^80]
                 }
-                store8f_sw(G + t * G_LD + c8 * 8, E, sw);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
                 *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(t, chk)) = pack8(o8);
@@ -755,6 +758,13 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e] * er[e];          // q e^{G_t}
                 *reinterpret_cast<uint4*>(sm + R_QG + kb * 8192 + sw128(t, chk)) = pack8(o8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * ec[e];          // k e^{G_C - G_t}
+                *reinterpret_cast<uint4*>(sm + R_KC + kb * 8192 + sw128(t, chk)) = pack8(o8);
+                const float bt = small[SM_B + t];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = bt * kf[e] * E[e] * er[e];      // b k e^{G_t}
+                *reinterpret_cast<uint4*>(sm + R_BKT + kb * 8192 + sw128(t, chk)) = pack8(o8);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i < b) continue;
@@ -778,8 +788,9 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         tc_fence_after();
 
         // ---- A and P: the row-block products D_i = Astack * K^(i)^T, as one
-        //      N=160 product into TMEM columns [0, 160), running while the
-        //      column-side operands are built.
+        //      N=160 product into TMEM columns [0, 160).  G and the raw z, q
+        //      are dead: the next item's z, q and A row start loading now.
+        if (tid == kLoadThread && nitem < n_items) issue_item_zq(sm, maps, A, nt0, nhead, inbar);
         if (tid == 0) {
             const uint32_t idesc = idesc_bf16(128, KV_ROWS);
 #pragma unroll
@@ -792,30 +803,6 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             mma_commit(bar);
         }
 
-        // ---- column-side operands (K^C)^T and (b K^g)^T, transposed (thread =
-        //      channel c, tokens of block b): the last readers of G, so that the
-        //      next item's z and q can be copied in from the solve on; (b V)^T
-        //      follows during the solve.
-        {
-            const int c = tid & 127, b = tid >> 7;
-            const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + R_K);
-            const float er = small[SM_ER + b * 128 + c], ec = small[SM_EC + b * 128 + c];
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int s8 = 2 * b + it;
-                float kc[8], bk[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = s8 * 8 + e;
-                    const float kf = s < len ? __bfloat162float(kraw[s * kD + c]) : 0.f;
-                    const float E = G[s * G_LD + c];
-                    kc[e] = kf * ec * __fdividef(1.0f, E);             // k_s e^{G_C - G_s}
-                    bk[e] = small[SM_B + s] * kf * E * er;             // b_s k_s e^{G_s}
-                }
-                *reinterpret_cast<uint4*>(sm + R_KC + sw128(c, s8)) = pack8(kc);
-                *reinterpret_cast<uint4*>(sm + R_BKT + sw128(c, s8)) = pack8(bk);
-            }
-        }
         ok = mbar_wait(bar, phase) && ok;
         phase ^= 1u;
         tc_fence_after();
@@ -879,10 +866,6 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             if (tid < kSolveThreads) {
                 solve_unit_lower(Af, Tf, Xs, tid);
             } else {
-                // G and the raw z, q are dead: the next item's z, q and A row
-                // start loading now.
-                if (tid == kLoadThread && nitem < n_items)
-                    issue_item_zq(sm, maps, A, nt0, nhead, inbar);
                 // Meanwhile the other warps build (b V)^T, thread = (channel c,
                 // tokens 32 half .. 32 half + 31).
                 const int u = tid - kSolveThreads, c = u & 127, half = u >> 7;
@@ -923,11 +906,11 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         // ---- W^T = (b K^g)^T T^T -> cols [0,64) on bar, U~^T = (b V)^T T^T ->
         //      cols [64,128) on bar2, so that W^T's readback overlaps U~^T.
         if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 64);
+            const uint32_t idesc = idesc_bf16(128, 64), idesc_mn = idesc_bf16_amn(128, 64);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_BKT + ks * 32)),
-                         desc_sw128(smem_u32(sm + R_TB + ks * 32)), idesc, ks > 0);
+            for (int ks = 0; ks < 4; ++ks)      // (b K^g)^T MN-major: 16 tokens = 2 KB
+                mma_bf16(tbase + 0, desc_sw128_mn(smem_u32(sm + R_BKT + ks * 2048), 8192, 1024),
+                         desc_sw128(smem_u32(sm + R_TB + ks * 32)), idesc_mn, ks > 0);
             mma_commit(bar);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -962,13 +945,11 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         //      accumulator rows.  That splits the readback evenly over the
         //      four lane quadrants.
         if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 256), idesc_h = idesc_bf16(128, 128);
+            const uint32_t idesc = idesc_bf16_amn(128, 256), idesc_h = idesc_bf16(128, 128);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t off = ks * 32;
-                mma_bf16(tbase + 0, desc_sw128(smem_u32(sm + R_KC + off)),
-                         desc_sw128(smem_u32(sm + R_WT + off)), idesc, ks > 0);
-            }
+            for (int ks = 0; ks < 4; ++ks)      // (K^C)^T MN-major: 16 tokens = 2 KB
+                mma_bf16(tbase + 0, desc_sw128_mn(smem_u32(sm + R_KC + ks * 2048), 8192, 1024),
+                         desc_sw128(smem_u32(sm + R_WT + ks * 32)), idesc, ks > 0);
             mma_commit(bar);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {

@@ -195,12 +195,29 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Descriptor of an MN-major operand with 128-byte swizzling: the M (or N)
+// index runs along the 128-byte rows (64 bf16 per row), the K index down the
+// rows.  An atom is 8 K-rows x 64 MN-elements (1024 B); `lbo` is the byte
+// stride between atoms along MN, `sbo` between groups of 8 K-rows.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator,
 // shape M x N.  Bits: D format [4,6) = 1 (f32), A format [7,10) = 1 (bf16),
 // B format [10,13) = 1 (bf16), A/B major [15], [16] = 0 (K-major),
 // N >> 3 [17,23), M >> 4 [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+// The same with A MN-major (bit 15 set).
+__host__ __device__ constexpr uint32_t idesc_bf16_amn(uint32_t M, uint32_t N) {
+    return idesc_bf16(M, N) | (1u << 15);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
