@@ -261,11 +261,11 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile_k
     }
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A (fp32, row stride F_LD),
-// by blocked doubling so that every step spreads over many threads: the 4 x 4
-// diagonal blocks by forward substitution, then for n = 4, 8, 16, 32 each
-// 2n x 2n diagonal block [T11 0; T21 T22] from its halves by
-// T21 = -T22 (A21 T11), with the n x n scratch X = A21 T11.  Every T entry
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A (fp32, row stride F_LD):
+// the four 16 x 16 diagonal blocks by forward substitution (one thread per
+// block column), then for n = 16, 32 each 2n x 2n diagonal block
+// [T11 0; T21 T22] from its halves by T21 = -T22 (A21 T11), with the n x n
+// scratch X = A21 T11.  Every T entry
 // that a later step reads is written first, zeros above the diagonal included.
 // Run by the first kSolveThreads threads, which synchronise among themselves
 // on named barrier 1, so that the other warps are free meanwhile.
@@ -412,23 +412,29 @@ __device__ __forceinline__ void solve_level32(const float* __restrict__ Af, floa
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, float* Tf,
                                                  float* Xs, int tid) {
     if (tid < 64) {
-        // column j of the 4 x 4 diagonal block k by forward substitution
-        const int k = tid >> 2, j = tid & 3;
-        const float* ab = Af + 4 * k * F_LD + 4 * k;
-        float x[4];
+        // column j of the 16 x 16 diagonal block k: x_r = -sum_{m<r} A_rm x_m
+        // below the unit entry, 0 above it.  The lanes of a block read the same
+        // A row (a broadcast).
+        const int k = tid >> 4, j = tid & 15;
+        const float* ab = Af + 16 * k * F_LD + 16 * k;
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 16; ++r) {
+            float a[16];
+#pragma unroll
+            for (int m4 = 0; m4 < r; m4 += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(ab + r * F_LD + m4);
+                a[m4] = v.x; a[m4 + 1] = v.y; a[m4 + 2] = v.z; a[m4 + 3] = v.w;
+            }
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) acc = fmaf(ab[r * F_LD + m], x[m], acc);
+            for (int m = 0; m < r; ++m) acc = fmaf(a[m], x[m], acc);
             x[r] = (r < j) ? 0.f : (r == j ? 1.f : -acc);
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) Tf[(4 * k + r) * F_LD + 4 * k + j] = x[r];
+        for (int r = 0; r < 16; ++r) Tf[(16 * k + r) * F_LD + 16 * k + j] = x[r];
     }
     named_bar_sync(1, kSolveThreads);
-    solve_level<4>(Af, Tf, Xs, tid);
-    solve_level<8>(Af, Tf, Xs, tid);
     solve_level<16>(Af, Tf, Xs, tid);
     solve_level32(Af, Tf, Xs, tid);
 }
