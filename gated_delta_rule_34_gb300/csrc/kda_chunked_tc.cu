@@ -104,7 +104,7 @@ constexpr uint32_t R_ZQ = R_G;         // raw z [64][128] bf16, then raw q, of t
 constexpr uint32_t R_AF = 0;           // A fp32 [64][68]
 constexpr uint32_t R_TF = 17408;       // T fp32 [64][68]
 constexpr uint32_t R_TB = 34816;       // T bf16 [64][64] swizzled
-constexpr uint32_t R_XS = 43008;       // solve scratch, 5 x 1024 fp32
+constexpr uint32_t R_XS = 43008;       // solve scratch, 1024 fp32
 constexpr uint32_t F_LD = 68;           // fp32 row stride: 16-byte aligned rows, 4-bank skew
 // reuse after W / U~ (the solve's buffers and the A/P operands are dead)
 constexpr uint32_t R_WT = 0;           // W^T  [128 c][64 s] swizzled
@@ -171,7 +171,7 @@ constexpr int kL2Ahead = 6;                        // packages prefetched into L
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
 static_assert(P_SMEM <= 232448, "chunk_prep shared memory");
-static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 5 * 1024 * 4 <= R_BKT, "solve scratch");
+static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 1024 * 4 <= R_BKT, "solve scratch");
 static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions");
 static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
@@ -332,10 +332,12 @@ __device__ __forceinline__ void solve_level(const float* __restrict__ Af, float*
 }
 
 // The last level (n = 32, one pair) with 4 x 4 register tiles and the
-// 32-term sums split four ways: thread (kg, i0, j0) of 256 sums terms
-// 8 kg .. 8 kg + 7 for rows i0 .. i0 + 3 and columns j0 .. j0 + 3, so that
-// each pair of 16-byte loads feeds sixteen FMAs; the four partial tiles are
-// then added.  Scratch: five 32 x 32 fp32 slices (X, then four partials).
+// 32-term sums split four ways inside a warp: warp w takes rows 4w .. 4w + 3,
+// lane (kg, jt) columns 4 jt .. 4 jt + 3 and terms 8 kg .. 8 kg + 7, so that
+// each pair of 16-byte loads feeds sixteen FMAs.  The four partial tiles are
+// added with shuffles across kg, and lane kg stores row kg of the tile.  The
+// eight lanes of a quarter warp share kg: they read one A (or T22) row
+// segment (a broadcast) and 128 contiguous bytes of T11 (or X).
 __device__ __forceinline__ void tile4x4_part(float (&acc)[4][4], const float* __restrict__ a, int lda,
                                              const float* __restrict__ b, int ldb) {
 #pragma unroll
@@ -364,48 +366,37 @@ __device__ __forceinline__ void tile4x4_part(float (&acc)[4][4], const float* __
     }
 }
 
+// Sums the tile over the four kg lanes (lane bits 3 and 4) and returns row kg.
+__device__ __forceinline__ float4 tile4x4_reduce_row(float (&acc)[4][4], int kg) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            acc[r][c] += __shfl_xor_sync(0xffffffffu, acc[r][c], 8);
+            acc[r][c] += __shfl_xor_sync(0xffffffffu, acc[r][c], 16);
+        }
+    float4 out = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+#pragma unroll
+    for (int r = 1; r < 4; ++r)
+        if (kg == r) out = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    return out;
+}
+
 __device__ __forceinline__ void solve_level32(const float* __restrict__ Af, float* Tf, float* Xs,
                                               int tid) {
     constexpr int n = 32;
-    const int kg = tid >> 6, i0 = 4 * ((tid >> 3) & 7), j0 = 4 * (tid & 7), m0 = 8 * kg;
-    float* part = Xs + 1024 * (1 + kg);
+    const int lane = tid & 31, kg = lane >> 3;
+    const int i0 = 4 * (tid >> 5), j0 = 4 * (lane & 7), m0 = 8 * kg;
     float acc[4][4];
-    // partial sums of X = A21 T11
+    // X = A21 T11
     tile4x4_part(acc, Af + (n + i0) * F_LD + m0, F_LD, Tf + m0 * F_LD + j0, F_LD);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-        *reinterpret_cast<float4*>(part + (i0 + r) * n + j0) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    *reinterpret_cast<float4*>(Xs + (i0 + kg) * n + j0) = tile4x4_reduce_row(acc, kg);
     named_bar_sync(1, kSolveThreads);
-    {
-        const int e = 4 * tid;
-        float4 x = *reinterpret_cast<const float4*>(Xs + 1024 + e);
-#pragma unroll
-        for (int k = 1; k < 4; ++k) {
-            const float4 y = *reinterpret_cast<const float4*>(Xs + 1024 * (1 + k) + e);
-            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-        }
-        *reinterpret_cast<float4*>(Xs + e) = x;
-    }
-    named_bar_sync(1, kSolveThreads);
-    // partial sums of T22 X
+    // T21 = -T22 X; T12 = 0
     tile4x4_part(acc, Tf + (n + i0) * F_LD + n + m0, F_LD, Xs + m0 * n + j0, n);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-        *reinterpret_cast<float4*>(part + (i0 + r) * n + j0) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-    named_bar_sync(1, kSolveThreads);
-    {
-        const int e = 4 * tid, r = e / n, c = e % n;
-        float4 x = *reinterpret_cast<const float4*>(Xs + 1024 + e);
-#pragma unroll
-        for (int k = 1; k < 4; ++k) {
-            const float4 y = *reinterpret_cast<const float4*>(Xs + 1024 * (1 + k) + e);
-            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-        }
-        *reinterpret_cast<float4*>(Tf + (n + r) * F_LD + c) = make_float4(-x.x, -x.y, -x.z, -x.w);
-        *reinterpret_cast<float4*>(Tf + r * F_LD + n + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    const float4 x = tile4x4_reduce_row(acc, kg);
+    *reinterpret_cast<float4*>(Tf + (n + i0 + kg) * F_LD + j0) = make_float4(-x.x, -x.y, -x.z, -x.w);
+    *reinterpret_cast<float4*>(Tf + (i0 + kg) * F_LD + n + j0) = make_float4(0.f, 0.f, 0.f, 0.f);
     named_bar_sync(1, kSolveThreads);
 }
 
