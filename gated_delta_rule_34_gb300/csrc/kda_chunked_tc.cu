@@ -724,44 +724,36 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             __syncthreads();
         }
 
-        // ---- operands from the token rows (thread = token t, 8 channels).  The
-        //      key-side operands of the later products, (K^C)^T and (b K^g)^T,
-        //      are written here too, as token rows: their MMAs read them
-        //      MN-major, so no transposed copy is built.
+        // ---- operands from the token rows (thread = token t, 8 channels): first
+        //      the two of the A/P product, then (below, while it runs) Q^g and
+        //      the key-side operands of the later products, K^C and b K^g, also
+        //      as token rows: their MMAs read them MN-major, so no transposed
+        //      copy is built.
+        const int kb = c8 >> 3, chk = c8 & 7;
+        const bool sw = (c8 >> 2) & 1;
+        float E[2][8], Rr[2][8];                 // e^{G_t - r_b} in [e^-80, 1], its inverse
+        uint4 kraw[2];
         {
-            const int kb = c8 >> 3, chk = c8 & 7;
-            const bool sw = (c8 >> 2) & 1;
 #pragma unroll
             for (int it = 0; it < 2; ++it) {
                 const int t = tt[it], b = t >> 4;
-                float Lt[8], kf[8], qf[8], E[8], Rr[8], er[8], ec[8], o8[8];
+                float Lt[8], kf[8], qf[8], o8[8];
                 load8f_sw(G + t * G_LD + c8 * 8, Lt, sw);
-                load8f_sw(small + SM_ER + b * 128 + c8 * 8, er, sw);
-                load8f_sw(small + SM_EC + b * 128 + c8 * 8, ec, sw);
-                unpack8(t < len ? *reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16)
-                                : make_uint4(0, 0, 0, 0), kf);
+                kraw[it] = t < len ? *reinterpret_cast<const uint4*>(sm + R_K + t * 256 + c8 * 16)
+                                   : make_uint4(0, 0, 0, 0);
+                unpack8(kraw[it], kf);
                 unpack8(qraw[it], qf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    E[e] = __expf(Lt[e]);                      // e^{G_t - r_b} in [e^-80, 1]
-                    Rr[e] = __fdividef(1.0f, E[e]);            // e^{r_b - G_t} in [1, e^80]
+                    E[it][e] = __expf(Lt[e]);
+                    Rr[it][e] = __fdividef(1.0f, E[it][e]);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[it][e];
                 *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(t, chk)) = pack8(o8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[it][e];
                 *reinterpret_cast<uint4*>(sm + R_AST + kb * 16384 + sw128(64 + t, chk)) = pack8(o8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e] * er[e];          // q e^{G_t}
-                *reinterpret_cast<uint4*>(sm + R_QG + kb * 8192 + sw128(t, chk)) = pack8(o8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * ec[e];          // k e^{G_C - G_t}
-                *reinterpret_cast<uint4*>(sm + R_KC + kb * 8192 + sw128(t, chk)) = pack8(o8);
-                const float bt = small[SM_B + t];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = bt * kf[e] * E[e] * er[e];      // b k e^{G_t}
-                *reinterpret_cast<uint4*>(sm + R_BKT + kb * 8192 + sw128(t, chk)) = pack8(o8);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if (i < b) continue;
@@ -773,7 +765,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                         load8f_sw(small + SM_X + xidx(i, b) * 128 + c8 * 8, x, sw);
                     }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[e] * x[e];  // k e^{r_i - G_t}
+                    for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[it][e] * x[e];  // k e^{r_i - G_t}
                     *reinterpret_cast<uint4*>(sm + R_KV + kb * KV_KB + sw128(d_col(i) + t, chk)) =
                         pack8(o8);
                 }
@@ -798,6 +790,25 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 mma_bf16(tbase, ad, bd, idesc, ks > 0);
             }
             mma_commit(bar);
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int t = tt[it], b = t >> 4;
+            float kf[8], qf[8], er[8], ec[8], o8[8];
+            load8f_sw(small + SM_ER + b * 128 + c8 * 8, er, sw);
+            load8f_sw(small + SM_EC + b * 128 + c8 * 8, ec, sw);
+            unpack8(kraw[it], kf);
+            unpack8(qraw[it], qf);
+            const float bt = small[SM_B + t];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[it][e] * er[e];          // q e^{G_t}
+            *reinterpret_cast<uint4*>(sm + R_QG + kb * 8192 + sw128(t, chk)) = pack8(o8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * Rr[it][e] * ec[e];         // k e^{G_C - G_t}
+            *reinterpret_cast<uint4*>(sm + R_KC + kb * 8192 + sw128(t, chk)) = pack8(o8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = bt * kf[e] * E[it][e] * er[e];     // b k e^{G_t}
+            *reinterpret_cast<uint4*>(sm + R_BKT + kb * 8192 + sw128(t, chk)) = pack8(o8);
         }
 
         ok = mbar_wait(bar, phase) && ok;
