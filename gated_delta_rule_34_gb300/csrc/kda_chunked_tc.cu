@@ -265,10 +265,12 @@ __device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, uint8_t* tile_k
 // the four 16 x 16 diagonal blocks by forward substitution (one thread per
 // block column), then for n = 16, 32 each 2n x 2n diagonal block
 // [T11 0; T21 T22] from its halves by T21 = -T22 (A21 T11), with the n x n
-// scratch X = A21 T11.  Every T entry
-// that a later step reads is written first, zeros above the diagonal included.
-// Run by the first kSolveThreads threads, which synchronise among themselves
-// on named barrier 1, so that the other warps are free meanwhile.
+// scratch X = A21 T11.  Every fp32 T entry that a later level reads is
+// written first, zeros above the diagonal included.  The last level writes its
+// T21 straight into the bf16 image of T; the other warps image the two
+// diagonal 32 x 32 blocks (and the zero block above T21) once named barrier 4
+// says they are final.  Run by the first kSolveThreads threads, which
+// synchronise among themselves on named barrier 1.
 constexpr int kSolveThreads = 256;
 
 // acc[0..3] += sum_{m < n} row[m] * M[m][0..3], with M's rows `ld` floats
@@ -383,7 +385,7 @@ __device__ __forceinline__ float4 tile4x4_reduce_row(float (&acc)[4][4], int kg)
 }
 
 __device__ __forceinline__ void solve_level32(const float* __restrict__ Af, float* Tf, float* Xs,
-                                              int tid) {
+                                              uint8_t* Tb, int tid) {
     constexpr int n = 32;
     const int lane = tid & 31, kg = lane >> 3;
     const int i0 = 4 * (tid >> 5), j0 = 4 * (lane & 7), m0 = 8 * kg;
@@ -392,16 +394,17 @@ __device__ __forceinline__ void solve_level32(const float* __restrict__ Af, floa
     tile4x4_part(acc, Af + (n + i0) * F_LD + m0, F_LD, Tf + m0 * F_LD + j0, F_LD);
     *reinterpret_cast<float4*>(Xs + (i0 + kg) * n + j0) = tile4x4_reduce_row(acc, kg);
     named_bar_sync(1, kSolveThreads);
-    // T21 = -T22 X; T12 = 0
+    // T21 = -T22 X, straight into the bf16 image Tb (the other blocks of the
+    // image are written by the other warps)
     tile4x4_part(acc, Tf + (n + i0) * F_LD + n + m0, F_LD, Xs + m0 * n + j0, n);
     const float4 x = tile4x4_reduce_row(acc, kg);
-    *reinterpret_cast<float4*>(Tf + (n + i0 + kg) * F_LD + j0) = make_float4(-x.x, -x.y, -x.z, -x.w);
-    *reinterpret_cast<float4*>(Tf + (i0 + kg) * F_LD + n + j0) = make_float4(0.f, 0.f, 0.f, 0.f);
-    named_bar_sync(1, kSolveThreads);
+    const int r = n + i0 + kg;
+    *reinterpret_cast<uint2*>(Tb + sw128(r, j0 >> 3) + (j0 & 7) * 2) =
+        make_uint2(pack_bf16x2(-x.x, -x.y), pack_bf16x2(-x.z, -x.w));
 }
 
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, float* Tf,
-                                                 float* Xs, int tid) {
+                                                 float* Xs, uint8_t* Tb, int tid) {
     if (tid < 64) {
         // column j of the 16 x 16 diagonal block k: x_r = -sum_{m<r} A_rm x_m
         // below the unit entry, 0 above it.  The lanes of a block read the same
@@ -427,7 +430,9 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ Af, f
     }
     named_bar_sync(1, kSolveThreads);
     solve_level<16>(Af, Tf, Xs, tid);
-    solve_level32(Af, Tf, Xs, tid);
+    // The diagonal 32 x 32 blocks are final: the other warps image them.
+    named_bar_arrive(4, kPrepThreads);
+    solve_level32(Af, Tf, Xs, Tb, tid);
 }
 
 // Which chunk package slot `slot` holds: its first token t0 and length.
@@ -872,7 +877,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
             float* Tf = reinterpret_cast<float*>(sm + R_TF);
             float* Xs = reinterpret_cast<float*>(sm + R_XS);
             if (tid < kSolveThreads) {
-                solve_unit_lower(Af, Tf, Xs, tid);
+                solve_unit_lower(Af, Tf, Xs, sm + R_TB, tid);
             } else {
                 // Meanwhile the other warps build (b V)^T, thread = (channel c,
                 // tokens 32 half .. 32 half + 31).
@@ -893,17 +898,22 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
                 named_bar_sync(3, kPrepThreads - kSolveThreads);
                 if (tid == kLoadThread && nitem < n_items)
                     issue_item_kv(sm, maps, nt0, nhead, kvbar);
-            }
-            __syncthreads();
-            // T as a bf16 K-major operand [t][s]: thread = (t, 8-column chunk)
-            {
-                const int t = tid >> 3, ch = tid & 7;
-                float o8[8];
-                load8f_sw(Tf + t * F_LD + ch * 8, o8, (ch >> 2) & 1);
+                // T as a bf16 K-major operand [t][s], 16-byte chunk (t, ch):
+                // once the diagonal 32 x 32 blocks are final, these warps write
+                // them and the zero block above them; the solve writes T21.
+                named_bar_sync(4, kPrepThreads);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (ch * 8 + e > t) o8[e] = 0.f;
-                *reinterpret_cast<uint4*>(sm + R_TB + sw128(t, ch)) = pack8(o8);
+                for (int pass = 0; pass < 2; ++pass) {
+                    if (pass == 1 && u >= 128) break;
+                    const int t = pass == 0 ? (u >> 3) : 32 + (u >> 2);
+                    const int ch = pass == 0 ? (u & 7) : 4 + (u & 3);
+                    float o8[8];
+                    load8f_sw(Tf + t * F_LD + ch * 8, o8, (ch >> 2) & 1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (ch * 8 + e > t) o8[e] = 0.f;
+                    *reinterpret_cast<uint4*>(sm + R_TB + sw128(t, ch)) = pack8(o8);
+                }
             }
         }
         fence_async_smem();
