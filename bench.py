@@ -148,23 +148,37 @@ def barrier(dist):
         dist.barrier()
 
 
+TRAFFIC_SOURCES = {
+    "decode": ("kda_decode.cu", "kda_common.cuh", "kda_internal.h"),
+    "chunked": ("kda_chunked_tc.cu", "tc_util.cuh", "kda_common.cuh", "kda_internal.h"),
+}
+
+
+def source_hash(kernel: str):
+    """First 16 hex digits of the sha256 over the sources `kernel` is built
+    from (its .cu file and the headers it includes), or None if one is missing."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES["decode" if kernel == "decode" else "chunked"]:
+        try:
+            with open(os.path.join(ROOT, "gated_delta_rule_34_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/traffic.json), or None if the kernel's source changed since."""
-    import hashlib
+    (profiles/traffic.json), or None if the kernel's sources changed since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             tr = json.load(f)
     except (OSError, ValueError):
         return None
-    src = ("gated_delta_rule_34_gb300/csrc/kda_decode.cu" if kernel == "decode"
-           else "gated_delta_rule_34_gb300/csrc/kda_chunked_tc.cu")
-    try:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
-    if tr.get("source_sha256_16", {}).get(src) != h:
+    key = "decode" if kernel == "decode" else "chunked"
+    h = source_hash(kernel)
+    if h is None or tr.get("source_sha256_16", {}).get(key) != h:
         return None
     return tr.get(kernel)
 
