@@ -58,8 +58,12 @@ bool valid_dtype(kda_dtype d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16
             return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);          \
     } while (0)
 
+// The tensor-core path: bf16, chunk 64, d_k a multiple of 16 and d_v a
+// multiple of 32 (one 32-column state tile per CTA of the state pass), both
+// at most 128; narrower heads are zero-padded to 128 on chip.
 bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
-    return dtype == KDA_DTYPE_BF16 && dk == 128 && dv == 128 && chunk == 64;
+    return dtype == KDA_DTYPE_BF16 && chunk == 64 && dk >= 16 && dk <= 128 && dk % 16 == 0 &&
+           dv >= 32 && dv <= 128 && dv % 32 == 0;
 }
 
 }  // namespace
@@ -177,7 +181,7 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         }
         return cuda_status(kda::run_chunked_tc(q, k, v, z, beta, A, o, initial_state,
                                                final_state, cu_seqlens, n_seqs, T, T_total, H,
-                                               workspace, ck, stream, device_sm_count()),
+                                               d_k, d_v, workspace, ck, stream, device_sm_count()),
                            "kda_chunk_prefill (chunked tensor-core path)");
     }
     kda::profile_event(0, stream);
@@ -212,8 +216,9 @@ kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const v
     if (B <= 0 || T < 0 || H <= 0 || H > 65535)
         return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%lld H=%d", B, (long long)T, H);
     if (!use_chunked_tc(d_k, d_v, 64, dtype))
-        return fail(KDA_ERR_UNSUPPORTED, "kda_chunk_prefill_from_host supports bf16 with "
-                                         "d_k = d_v = 128 only (d_k=%d d_v=%d dtype=%d)",
+        return fail(KDA_ERR_UNSUPPORTED, "kda_chunk_prefill_from_host supports the tensor-core "
+                                         "path only: bf16, d_k a multiple of 16 and d_v a multiple "
+                                         "of 32, both <= 128 (d_k=%d d_v=%d dtype=%d)",
                     d_k, d_v, (int)dtype);
     if (segment_tokens <= 0 || segment_tokens % 64 != 0)
         return fail(KDA_ERR_INVALID_ARG, "segment_tokens must be a positive multiple of 64, got %lld",

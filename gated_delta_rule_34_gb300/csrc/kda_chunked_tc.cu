@@ -1,5 +1,7 @@
 // kda_chunked_tc.cu -- chunked KDA prefill on the sm_103a tensor cores
-// (bf16 inputs, d_k = d_v = 128, chunk C = 64).
+// (bf16 inputs, chunk C = 64, d_k = d_v = 128; narrower heads -- d_k a
+// multiple of 16, d_v a multiple of 32 -- run on the same 128-wide tiles, the
+// extra channels arriving as zeros from the input tensor maps).
 //
 // The pages describe the kernel in outline only: the tokens of a chunk are
 // processed in parallel and the state is then passed on across all heads
@@ -119,7 +121,7 @@ constexpr uint32_t SM_LAM = 2304;      // [128] e^{G_C}
 constexpr uint32_t SM_B = 2432;        // [64] beta
 constexpr uint32_t SM_A = 2496;        // [128] A row of the next item (prefetched)
 constexpr uint32_t R_SMALL_BYTES = (2496 + 128) * 4;
-constexpr uint32_t kInputBytesZQ = 2 * 16384 + 512;  // z, q tiles and the A row
+constexpr uint32_t kInputBytesZQ = 2 * 16384;        // z, q tiles (the A row adds 4 d_k)
 constexpr uint32_t kInputBytesKV = 2 * 16384;        // k, v tiles
 constexpr uint32_t R_BAR = R_SMALL + R_SMALL_BYTES;
 constexpr uint32_t P_SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
@@ -158,7 +160,7 @@ __host__ __device__ constexpr int xidx(int i, int b) {
 // chain's floor is about eight of those plus the update.
 constexpr int kStateThreads = 32 * 15;
 constexpr int kUpdWarps = 8, kOutWarps = 4;
-constexpr int kTiles = 4;                          // column tiles per (sequence, head)
+constexpr int kTiles = 4;                          // column tiles per (sequence, head) at d_v = 128
 constexpr int kJ = 32;                             // state columns per tile
 constexpr int kStages = 4;
 constexpr uint32_t ST_BYTES = 49152;               // per stage: [N ; Q'], both K-blocks
@@ -545,11 +547,11 @@ struct InputMaps {
 // to the next sequence (or are zero); the consumers mask them.
 __device__ __forceinline__ void issue_item_zq(uint8_t* sm, const InputMaps& maps,
                                               const float* __restrict__ A, int64_t t0, int h,
-                                              uint64_t* inbar) {
-    mbar_expect_tx(inbar, kInputBytesZQ);
+                                              int dk, uint64_t* inbar) {
+    mbar_expect_tx(inbar, kInputBytesZQ + 4u * (uint32_t)dk);
     tma_load_3d(sm + R_ZQ, &maps.z, 0, h, (int)t0, inbar);
     tma_load_3d(sm + R_ZQ + 16384, &maps.q, 0, h, (int)t0, inbar);
-    bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * kD, 512, inbar);
+    bulk_g2s(sm + R_SMALL + SM_A * 4, A + (size_t)h * dk, 4u * (uint32_t)dk, inbar);
 }
 __device__ __forceinline__ void issue_item_kv(uint8_t* sm, const InputMaps& maps, int64_t t0, int h,
                                               uint64_t* kvbar) {
@@ -573,7 +575,7 @@ __device__ __forceinline__ uint32_t load_beta_raw(const __nv_bfloat16* __restric
 // ============================================================================
 __global__ void __launch_bounds__(kPrepThreads, 1)
 chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* __restrict__ beta,
-                  const float* __restrict__ A, uint8_t* __restrict__ ws, SeqMap map, int H,
+                  const float* __restrict__ A, uint8_t* __restrict__ ws, SeqMap map, int H, int dk,
                   int64_t n_items) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -590,6 +592,11 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     uint32_t* status = reinterpret_cast<uint32_t*>(ws);
 
     if (warp == 0) tmem_alloc<512>(tslot);
+    // Channels d_k .. 127 of a narrower head: the input tiles arrive
+    // zero-filled there (the tensor maps are d_k wide), and the A row entries,
+    // which the copies never write, are set to 0 once so that those channels
+    // stay finite; with k = q = 0 they contribute nothing.
+    if (tid >= dk && tid < kD) small[SM_A + tid] = 0.f;
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(inbar, 1);
@@ -626,7 +633,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
     while (item < n_items && !slot_chunk(map, slot, t0, len)) advance(item, slot, head);
     if (item < n_items) {
         if (tid == kLoadThread) {
-            issue_item_zq(sm, maps, A, t0, head, inbar);
+            issue_item_zq(sm, maps, A, t0, head, dk, inbar);
             issue_item_kv(sm, maps, t0, head, kvbar);
         }
         bt_raw = load_beta_raw(beta, t0, len, head, H, tid);
@@ -784,7 +791,7 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
         // ---- A and P: the row-block products D_i = Astack * K^(i)^T, as one
         //      N=160 product into TMEM columns [0, 160).  G and the raw z, q
         //      are dead: the next item's z, q and A row start loading now.
-        if (tid == kLoadThread && nitem < n_items) issue_item_zq(sm, maps, A, nt0, nhead, inbar);
+        if (tid == kLoadThread && nitem < n_items) issue_item_zq(sm, maps, A, nt0, nhead, dk, inbar);
         if (tid == 0) {
             const uint32_t idesc = idesc_bf16(128, KV_ROWS);
 #pragma unroll
@@ -1093,7 +1100,7 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volati
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
-                  CheckpointSpec ck) {
+                  int dk, int dv, CheckpointSpec ck) {
     const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = tile * kJ;
@@ -1127,18 +1134,22 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     const bool upd = warp < kUpdWarps;
     auto erow = [&](int e) { return 32 * q4 + 16 * (e >> 3) + 8 * ((e >> 1) & 1) + (lane >> 2); };
     auto ecol = [&](int e) { return jh + 8 * ((e >> 2) & 1) + 2 * (lane & 3) + (e & 1); };
-    const size_t smat = ((size_t)n * H + h) * kD * kD + j0;        // this tile of S0 / S1
+    // this tile of S0 / S1 ([d_k][d_v] per (n, h)); rows d_k .. 127 of a
+    // narrower head stay 0 on chip and are neither read nor written
+    const size_t smat = ((size_t)n * H + h) * dk * dv + j0;
     float st[16];
-    auto store_state = [&](float* mat) {                             // mat: [128][128] of (n, h) + j0
+    auto store_state = [&](float* mat) {                             // mat: S of (n, h) + j0
 #pragma unroll
         for (int e = 0; e < 16; e += 2)
-            *reinterpret_cast<float2*>(mat + (size_t)erow(e) * kD + ecol(e)) = make_float2(st[e], st[e + 1]);
+            if (erow(e) < dk)
+                *reinterpret_cast<float2*>(mat + (size_t)erow(e) * dv + ecol(e)) = make_float2(st[e], st[e + 1]);
     };
     if (upd) {
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-            const float2 v = S0 ? __ldg(reinterpret_cast<const float2*>(S0 + smat + (size_t)erow(e) * kD + ecol(e)))
-                                : make_float2(0.f, 0.f);
+            const float2 v = S0 && erow(e) < dk
+                                 ? __ldg(reinterpret_cast<const float2*>(S0 + smat + (size_t)erow(e) * dv + ecol(e)))
+                                 : make_float2(0.f, 0.f);
             st[e] = v.x;
             st[e + 1] = v.y;
         }
@@ -1291,7 +1302,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             if (lane == 0) mbar_arrive(dfree + b);
             const int64_t t0 = bos + (int64_t)cc * kC;
             if (act && t < eos - t0) {
-                uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * kD + j0);
+                uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * dv + j0);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float op[8], o8[8];
@@ -1372,7 +1383,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             if (ck.out) {
                 const int64_t done = (int64_t)(cc + 1) * kC;
                 if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
-                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * kD * kD + j0);
+                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv + j0);
             }
             return true;
         };
@@ -1414,12 +1425,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Tensor map of one [T_total][H][128] bf16 input with 64 x 1 x 128 boxes.
-static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+// Tensor map of one [T_total][H][d] bf16 input (d <= 128, 2 d a multiple of
+// 16 bytes) with 64 x 1 x 128 boxes: channels d .. 127 of a box lie outside
+// the tensor and arrive as zeros.
+static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int d) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
-    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
-    cuuint64_t strides[2] = {256, (cuuint64_t)H * 256};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T_total};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {128, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -1436,8 +1449,8 @@ size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0, float* S1,
                            const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                           void* workspace, const CheckpointSpec& ck, cudaStream_t stream,
-                           int num_sms) {
+                           int dk, int dv, void* workspace, const CheckpointSpec& ck,
+                           cudaStream_t stream, int num_sms) {
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -1462,20 +1475,20 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
     if (T_total > 0) {
         tc::InputMaps maps;
-        if (!make_input_map(&maps.q, q, T_total, H) || !make_input_map(&maps.k, k, T_total, H) ||
-            !make_input_map(&maps.v, v, T_total, H) || !make_input_map(&maps.z, z, T_total, H))
+        if (!make_input_map(&maps.q, q, T_total, H, dk) || !make_input_map(&maps.k, k, T_total, H, dk) ||
+            !make_input_map(&maps.v, v, T_total, H, dv) || !make_input_map(&maps.z, z, T_total, H, dk))
             return cudaErrorInvalidValue;
         const int64_t n_items = slots * H;
         const int64_t grid = n_items < num_sms ? n_items : num_sms;
         tc::chunk_prep_kernel<<<(unsigned)grid, tc::kPrepThreads, tc::P_SMEM, stream>>>(
-            maps, static_cast<const bf*>(beta), A, ws, map, H, n_items);
+            maps, static_cast<const bf*>(beta), A, ws, map, H, dk, n_items);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     profile_event(1, stream);
-    dim3 grid_s((unsigned)tc::kTiles, (unsigned)n_seqs, (unsigned)H);
+    dim3 grid_s((unsigned)(dv / tc::kJ), (unsigned)n_seqs, (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
-        ws, static_cast<bf*>(o), S0, S1, map, H, ck);
+        ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck);
     e = cudaGetLastError();
     profile_event(2, stream);
     return e;

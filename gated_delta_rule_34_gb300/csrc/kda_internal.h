@@ -43,12 +43,13 @@ cudaError_t run_recurrent(const void* q, const void* k, const void* v, const voi
                           int dk, int dv, bool bf16, const CheckpointSpec& ck,
                           cudaStream_t stream);
 
-// Chunked tensor-core path (bf16, d_k = d_v = 128, chunk 64).
+// Chunked tensor-core path (bf16, chunk 64; d_k a multiple of 16 and d_v a
+// multiple of 32, both <= 128, zero-padded to 128 on chip).
 size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H);
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0,
                            float* S1, const int32_t* cu, int n_seqs, int64_t T,
-                           int64_t T_total, int H, void* workspace, const CheckpointSpec& ck,
-                           cudaStream_t stream, int num_sms);
+                           int64_t T_total, int H, int dk, int dv, void* workspace,
+                           const CheckpointSpec& ck, cudaStream_t stream, int num_sms);
 
 }  // namespace kda

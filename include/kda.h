@@ -62,7 +62,9 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 /* Which kernels kda_chunk_prefill runs for a given shape. */
 typedef enum {
     KDA_PATH_RECURRENT = 0,    /* SIMT fp32, token by token, any d_k, d_v <= 128     */
-    KDA_PATH_CHUNKED_TC = 1    /* chunked WY/UT form on tcgen05 (bf16, d=128, C=64)  */
+    KDA_PATH_CHUNKED_TC = 1    /* chunked WY/UT form on tcgen05: bf16, chunk 64,
+                                  d_k a multiple of 16 and d_v a multiple of 32,
+                                  both <= 128 (zero-padded to 128 on chip)      */
 } kda_prefill_path;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -103,6 +105,10 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *   final_state    nullable; [N, H, d_k, d_v] fp32 (written).
  *   o              [B, T, H, d_v] in `dtype` (written).
  *   chunk          16 or 64 (the exact result does not depend on it).
+ *                  bf16 with chunk 64, d_k a multiple of 16 and d_v a multiple
+ *                  of 32 (both <= 128) runs on the tensor cores
+ *                  (kda_chunk_prefill_path says which path a shape takes);
+ *                  everything else on the fp32 SIMT recurrence.
  *   workspace      device scratch of at least kda_chunk_prefill_workspace_size()
  *                  bytes (may be NULL when that size is 0); 256-byte aligned;
  *                  contents on entry are ignored.
@@ -169,8 +175,9 @@ kda_status kda_chunk_prefill_checkpoints(const void *q, const void *k, const voi
  *                 state from segment to segment and ends as the final state.
  *   segment_tokens  a positive multiple of 64.
  *   workspace     as for kda_chunk_prefill with B = 1, T = segment_tokens.
- * Only the tensor-core path: bf16, d_k = d_v = 128, chunk 64; anything else
- * returns KDA_ERR_UNSUPPORTED.  The three streams must differ; h2d_stream and
+ * Only shapes of the tensor-core path (bf16, chunk 64, d_k a multiple of 16
+ * and d_v a multiple of 32, both <= 128); anything else returns
+ * KDA_ERR_UNSUPPORTED.  The three streams must differ; h2d_stream and
  * d2h_stream first wait for the work already queued on `stream`, and `stream`
  * finishes only after the last copy back, so synchronising `stream` covers
  * the whole call.  Each call creates and destroys two CUDA events.

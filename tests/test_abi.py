@@ -109,7 +109,16 @@ def test_workspace_size_query(L):
 def test_path_query(L):
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(16, 16, 16, 0)] == "recurrent"
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 64, 0)] == "recurrent"   # fp32
-    assert api.PATH_NAMES[L.kda_chunk_prefill_path(64, 64, 64, 1)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 16, 1)] == "recurrent"   # chunk 16
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 64, 1)] == "chunked_tc"
+    # narrower bf16 heads: d_k a multiple of 16, d_v a multiple of 32
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(64, 64, 64, 1)] == "chunked_tc"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(16, 32, 64, 1)] == "chunked_tc"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(48, 64, 64, 1)] == "chunked_tc"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(40, 64, 64, 1)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(64, 48, 64, 1)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(8, 32, 64, 1)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(144, 128, 64, 1)] == "recurrent"
 
 
 def test_gate_rejects_bad_arguments(L):
@@ -163,7 +172,7 @@ def test_from_host_rejects_bad_arguments(L):
                                              1, 4096, 2, a["d"], a["d"], a["dtype"], a["seg"], f,
                                              1 << 30, *a["st"])
     assert call(dtype=0) == UNSUPPORTED                       # fp32: not the tensor-core path
-    assert call(d=64) == UNSUPPORTED
+    assert call(d=40) == UNSUPPORTED                          # d_k not a multiple of 16
     assert call(seg=100) == INVALID                           # not a multiple of 64
     assert call(seg=0) == INVALID
     assert call(st=(s1, s1, s3)) == INVALID                   # streams must differ
