@@ -400,7 +400,8 @@ def _time_ms(fn, iters=5, warm=2):
 def measure_next_rows(kda, xp, wp, xd, wd, peaks):
     """Timings of the rows beyond the base path (outside the timed step):
     speculative verify / commit on the decode workload's states with T draft
-    tokens, and long-context prefill with a checkpoint every 512 tokens."""
+    tokens, long-context prefill with a checkpoint every 512 tokens, and a
+    d = 64 head on the tensor cores beside the SIMT recurrence."""
     import torch
     from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs
     out = {}
@@ -433,6 +434,23 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
                    iters=3, warm=1)
     out["prefill_checkpoint_every_512"] = {"ms": tck, "tokens_per_s": Bp * Tp / (tck * 1e-3),
                                            "checkpoint_bytes": ck.numel() * 4}
+    del ck, ws
+    # A narrower head (d_k = d_v = 64, bf16) on the tensor cores, beside the same
+    # shape on the fp32 SIMT recurrence (chunk 16 keeps it there).
+    from dataclasses import replace
+    T64 = 16384
+    w64 = replace(WORKLOADS[2], dk=64, dv=64, seed=110)
+    x64 = make_inputs(w64, device="cuda", B=1, T=T64)
+    ws64 = torch.empty(kda.workspace_size(1, 1, T64, w64.H, 64, 64, 64, torch.bfloat16),
+                       dtype=torch.uint8, device="cuda")
+    args64 = (x64["q"], x64["k"], x64["v"], x64["z"], x64["beta"], x64["A"])
+    t_tc = _time_ms(lambda: kda.chunk_prefill(*args64, initial_state=x64["S0"], chunk=64,
+                                              workspace=ws64), iters=5, warm=2)
+    t_rec = _time_ms(lambda: kda.chunk_prefill(*args64, initial_state=x64["S0"], chunk=16),
+                     iters=2, warm=1)
+    out[f"prefill_d64_h{w64.H}_t{T64}"] = {
+        "tensor_core_ms": t_tc, "tensor_core_tokens_per_s": T64 / (t_tc * 1e-3),
+        "recurrent_ms": t_rec, "recurrent_tokens_per_s": T64 / (t_rec * 1e-3)}
     return out
 
 
