@@ -155,16 +155,22 @@ TRAFFIC_SOURCES = {
 
 
 def source_hash(kernel: str):
-    """First 16 hex digits of the sha256 over the sources `kernel` is built
-    from (its .cu file and the headers it includes), or None if one is missing."""
+    """First 16 hex digits of the sha256 over the code `kernel` is built from
+    (its .cu file and the headers it includes, with comments and blank space
+    removed, so that an edit to a comment keeps the recorded counters), or None
+    if a file is missing."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in TRAFFIC_SOURCES["decode" if kernel == "decode" else "chunked"]:
         try:
-            with open(os.path.join(ROOT, "gated_delta_rule_34_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(ROOT, "gated_delta_rule_34_gb300", "csrc", name)) as f:
+                text = f.read()
         except OSError:
             return None
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -30,12 +30,12 @@
 //                X, O' and P W (tcgen05).  Writes one 97 KB "package" per
 //                (chunk, head): the operand images the state pass feeds to the
 //                tensor cores unchanged.
-//   state_pass   one CTA per (sequence, head), sequential over its chunks.
-//                S lives in fp32 registers; per chunk ONE tcgen05 MMA of shape
-//                M=128, N=192, K=128 computes (N S)^T and (Q' S)^T together
-//                from the bf16 copy of S^T, then S <- lam (.) S - N S + X.  The
-//                output half of the product is read out, finished with O' and
-//                bulk-stored while the next chunk's MMA runs.
+//   state_pass   one CTA per (sequence, head, 32-column tile of S), sequential
+//                over its chunks.  The tile lives in fp32 registers; per chunk
+//                one tcgen05 product N S (M=128, N=32, K=128) from the bf16
+//                copy of the tile's S^T feeds S <- lam (.) S - N S + X, and a
+//                second one, Q' S (M=64), runs beside the chain; its result is
+//                finished with O' and stored as o.
 //
 // Decay factoring.  Over 64 tokens G reaches -320, outside fp32/bf16; across
 // a 16-token block it spans at most e^80, which fits.  Row t of 16-row block i
