@@ -160,7 +160,6 @@ __host__ __device__ constexpr int xidx(int i, int b) {
 // chain's floor is about eight of those plus the update.
 constexpr int kStateThreads = 32 * 15;
 constexpr int kUpdWarps = 8, kOutWarps = 4;
-constexpr int kTiles = 4;                          // column tiles per (sequence, head) at d_v = 128
 constexpr int kJ = 32;                             // state columns per tile
 constexpr int kStages = 4;
 constexpr uint32_t ST_BYTES = 49152;               // per stage: [N ; Q'], both K-blocks
