@@ -6,10 +6,10 @@ The binding loads ``_build/libkda.so`` on first use (build it with
 ``python -m gated_delta_rule_34_gb300.build``); importing the package loads
 nothing, so the seeded input generator (``.inputs``) can be used without a GPU.
 """
-from .api import (KDAError, chunk_prefill, chunk_prefill_from_host, decode_step,  # noqa: F401
-                  gate, lib, library_path, prefill_path, set_profile_events, spec_commit,
-                  spec_verify, workspace_size)
+from .api import (KDAError, chunk_prefill, chunk_prefill_from_host,  # noqa: F401
+                  chunk_prefill_static_workspace, decode_step, gate, lib, library_path,
+                  prefill_path, set_profile_events, spec_commit, spec_verify, workspace_size)
 
-__all__ = ["KDAError", "chunk_prefill", "chunk_prefill_from_host", "decode_step", "gate", "lib",
-           "library_path", "prefill_path", "set_profile_events", "spec_commit", "spec_verify",
-           "workspace_size"]
+__all__ = ["KDAError", "chunk_prefill", "chunk_prefill_from_host", "chunk_prefill_static_workspace",
+           "decode_step", "gate", "lib", "library_path", "prefill_path", "set_profile_events",
+           "spec_commit", "spec_verify", "workspace_size"]
