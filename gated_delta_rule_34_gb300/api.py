@@ -69,6 +69,8 @@ def _declare(lib):
     lib.kda_spec_commit.restype = i32
     lib.kda_set_profile_events.argtypes = [vp, i32]
     lib.kda_set_profile_events.restype = i32
+    lib.kda_selftest_bounded_wait.argtypes = [vp, i32, vp]
+    lib.kda_selftest_bounded_wait.restype = i32
     return lib
 
 
@@ -248,6 +250,17 @@ def set_profile_events(events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     set_profile_events._keep = arr
     _check(lib().kda_set_profile_events(arr, len(events)))
+
+
+def selftest_bounded_wait(status: torch.Tensor, arrive: bool) -> None:
+    """kda_selftest_bounded_wait: one thread waits through the kernels' bounded mbarrier
+    wait, on a barrier nothing arrives on (arrive False: gives up after about 2 s) or one it
+    completes itself; writes 1 (gave up) or 0 into ``status`` (an int32 CUDA tensor)."""
+    _need_cuda(status)
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise ValueError("status must be an int32 CUDA tensor")
+    _check(lib().kda_selftest_bounded_wait(_ptr(status), int(bool(arrive)),
+                                           _stream(status.device)))
 
 
 def chunk_prefill_static_workspace(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,

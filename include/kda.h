@@ -293,6 +293,22 @@ kda_status kda_spec_commit(const void *k, const void *v, const void *z, const vo
  */
 kda_status kda_set_profile_events(cudaEvent_t *events, int n_events);
 
+/*
+ * kda_selftest_bounded_wait -- failure detection, exercised without a fault
+ * (not part of the layer's arithmetic; the pages have no counterpart).  The
+ * tensor-core kernels bound every mbarrier wait: after about 2 s the wait
+ * gives up, the kernel sets a bit in the workspace status word and returns,
+ * and the context stays usable.  This launches one thread that waits through
+ * that same bounded wait on an mbarrier nothing arrives on (arrive == 0; the
+ * call's kernel then runs for about 2 s) or on one that its own arrival
+ * completes (arrive != 0), and writes the outcome to *status: 1 if the wait
+ * gave up, 0 if it was satisfied.
+ *   status  device uint32_t, 4-byte aligned, owned by the caller (written).
+ * Asynchronous on `stream`.  Returns KDA_ERR_INVALID_ARG for a null or
+ * misaligned status, KDA_ERR_CUDA if the launch fails.
+ */
+kda_status kda_selftest_bounded_wait(uint32_t *status, int arrive, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -177,3 +177,8 @@ def test_from_host_rejects_bad_arguments(L):
     assert call(seg=0) == INVALID
     assert call(st=(s1, s1, s3)) == INVALID                   # streams must differ
     assert call(S1=None) == INVALID                           # the state carrier is required
+
+
+def test_selftest_rejects_bad_status_pointer(L):
+    assert L.kda_selftest_bounded_wait(None, 0, None) == INVALID
+    assert L.kda_selftest_bounded_wait(_fake(0x10002), 0, None) == INVALID   # not 4-byte aligned
