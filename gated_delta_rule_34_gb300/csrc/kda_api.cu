@@ -4,6 +4,7 @@
 // reads device memory.  Each entry point returns a kda_status and records a
 // one-line reason for the last failure in thread-local storage.
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 
 #include "../../include/kda.h"
@@ -171,6 +172,10 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
     const bool bf16 = dtype == KDA_DTYPE_BF16;
 
     if (use_chunked_tc(d_k, d_v, chunk, dtype)) {
+        // TMA tile coordinates are 32-bit: token indices must fit.
+        if (T_total > (int64_t)INT32_MAX - 64)
+            return fail(KDA_ERR_UNSUPPORTED, "the tensor-core path takes fewer than 2^31 tokens (%lld)",
+                        (long long)T_total);
         const size_t need = kda::chunked_tc_workspace_bytes(n_seqs, T_total, H);
         if (need > 0) {
             if (workspace == nullptr || workspace_bytes < need)

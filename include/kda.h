@@ -108,7 +108,9 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *                  bf16 with chunk 64, d_k a multiple of 16 and d_v a multiple
  *                  of 32 (both <= 128) runs on the tensor cores
  *                  (kda_chunk_prefill_path says which path a shape takes);
- *                  everything else on the fp32 SIMT recurrence.
+ *                  everything else on the fp32 SIMT recurrence.  The
+ *                  tensor-core path takes fewer than 2^31 tokens in all
+ *                  (KDA_ERR_UNSUPPORTED otherwise).
  *   workspace      device scratch of at least kda_chunk_prefill_workspace_size()
  *                  bytes (may be NULL when that size is 0); 256-byte aligned;
  *                  contents on entry are ignored.

@@ -101,6 +101,13 @@ def test_prefill_tc_path_requires_workspace(L):
     assert rc == INVALID                                        # not 256-byte aligned
 
 
+def test_prefill_tc_path_rejects_token_counts_past_32_bit_coordinates(L):
+    rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, B=1, T=1 << 31, ws=_fake(0x100000),
+                  ws_bytes=1 << 62)
+    assert rc == UNSUPPORTED
+    assert b"2^31" in L.kda_last_error()
+
+
 def test_workspace_size_query(L):
     assert L.kda_chunk_prefill_workspace_size(1, 1, 64, 1, 16, 16, 16, 0) == 0   # SIMT path
     assert L.kda_chunk_prefill_workspace_size(0, 1, 64, 1, 128, 128, 64, 1) == 0
