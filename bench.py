@@ -43,6 +43,18 @@ PREFILL_FLOP_PER_TH = 64 * (3 * 128 + 2 * 128) + 6 * 128 * 128 + 64 * 64 / 3
 PREFILL_FLOP_DENSE_PER_TH = 2 * 64 * (3 * 128 + 2 * 128) + 6 * 128 * 128 + 64 * 64 / 3
 PREFILL_BYTES_PER_TH = 1282
 STATE_BYTES = 128 * 128 * 4
+# Bytes a prefill kernel must move by itself, per token-head: chunk_prep reads q, k,
+# v, z and beta (1,026 B); the state pass writes o (256 B).  Its package hand-off is
+# not algorithmic and is not counted.
+KERNEL_OWN_BYTES_PER_TH = {"chunk_prep": 1026, "state_pass": 256}
+TRAFFIC_SOURCE_NOTE = {
+    "chunk_prep": "ncu --set full on the T=16384 case of the same kernel (bench.py --ncu-case "
+                  "prefill); dram read+write bytes scaled x4 to the T=65536 launch "
+                  "(profiles/traffic.json)",
+    "state_pass": "ncu --set full on the T=16384 case of the same kernel (bench.py --ncu-case "
+                  "prefill); dram read+write bytes scaled x4 to the T=65536 launch "
+                  "(profiles/traffic.json)",
+}
 DECODE_BYTES_PER_BH = 2 * STATE_BYTES + 4 * 256 + 2 + 256
 
 
@@ -340,11 +352,25 @@ def run_ours(args):
     dom = max(range(n_prefill_kernels), key=lambda j: kern_avg[j])
     achieved = pbytes / (kern_avg[dom] * 1e-3) / 1e9
     traffic = recorded_traffic(names[dom])
+    own = KERNEL_OWN_BYTES_PER_TH.get(names[dom])
+    path_gbs = pbytes / (pre_avg * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "kernel": names[dom], "kernel_ms": kern_avg[dom],
                 "peak_source": peaks["source"],
-                "per_kernel_ms": {n: t for n, t in zip(names, kern_avg)}}
+                "achieved_definition": "path algorithmic bytes (1,282 B per token-head + states) "
+                                       "/ dominant kernel's average time",
+                "per_kernel_ms": {n: t for n, t in zip(names, kern_avg)},
+                # the dominant kernel on its own bytes (what it must read or write by itself)
+                "kernel_own_bytes": None if own is None else th * own,
+                "kernel_own_frac": None if own is None else
+                th * own / (kern_avg[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                # the whole layer call against both roofs
+                "path_ms": pre_avg, "path_gbs": path_gbs, "path_hbm_frac": path_gbs / peaks["hbm_gbs"],
+                "path_tensor_frac_causal": tflops / peaks["bf16_tflops"],
+                "path_tensor_frac_dense_count": flops_dense / (pre_avg * 1e-3) / 1e12
+                / peaks["bf16_tflops"],
+                "traffic_source": None if traffic is None else TRAFFIC_SOURCE_NOTE.get(names[dom])}
 
     # End to end through the C ABI with pinned host buffers (copies inside the timing).
     e2e = None

@@ -9,8 +9,9 @@ nothing, so the seeded input generator (``.inputs``) can be used without a GPU.
 from .api import (KDAError, chunk_prefill, chunk_prefill_from_host,  # noqa: F401
                   chunk_prefill_static_workspace, decode_step, gate, lib, library_path,
                   prefill_path, selftest_bounded_wait, set_profile_events, spec_commit,
-                  spec_verify, workspace_size)
+                  spec_verify, static_workspace_status, workspace_size)
 
 __all__ = ["KDAError", "chunk_prefill", "chunk_prefill_from_host", "chunk_prefill_static_workspace",
            "decode_step", "gate", "lib", "library_path", "prefill_path", "selftest_bounded_wait",
-           "set_profile_events", "spec_commit", "spec_verify", "workspace_size"]
+           "set_profile_events", "spec_commit", "spec_verify", "static_workspace_status",
+           "workspace_size"]

@@ -71,6 +71,8 @@ def _declare(lib):
     lib.kda_set_profile_events.restype = i32
     lib.kda_selftest_bounded_wait.argtypes = [vp, i32, vp]
     lib.kda_selftest_bounded_wait.restype = i32
+    lib.kda_static_workspace_status.argtypes = [vp, vp]
+    lib.kda_static_workspace_status.restype = i32
     return lib
 
 
@@ -90,6 +92,12 @@ def lib():
 def _check(status: int):
     if status != 0:
         raise KDAError(status, lib().kda_last_error().decode())
+
+
+def _on(device):
+    """Makes ``device`` current for the duration of a library call: the library launches
+    on the current device and resolves its per-device state there."""
+    return torch.cuda.device(device)
 
 
 def _dtype_code(t: torch.dtype) -> int:
@@ -124,8 +132,9 @@ def gate(z: torch.Tensor, A: torch.Tensor, out: torch.Tensor | None = None) -> t
     if out is None:
         out = torch.empty(z.shape, dtype=torch.float32, device=z.device)
     _need_cuda(z, A, out)
-    _check(lib().kda_gate(_ptr(z), _ptr(A), _ptr(out), n_tokens, H, dk, _dtype_code(z.dtype),
-                          _stream(z.device)))
+    with _on(z.device):
+        _check(lib().kda_gate(_ptr(z), _ptr(A), _ptr(out), n_tokens, H, dk, _dtype_code(z.dtype),
+                              _stream(z.device)))
     return out
 
 
@@ -171,18 +180,20 @@ def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chun
                checkpoints)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if checkpoints is None:
-        _check(lib().kda_chunk_prefill(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
-            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
-            chunk, _dtype_code(q.dtype), _ptr(workspace), ws_bytes, _stream(q.device)))
+        with _on(q.device):
+            _check(lib().kda_chunk_prefill(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+                _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
+                chunk, _dtype_code(q.dtype), _ptr(workspace), ws_bytes, _stream(q.device)))
     else:
         if checkpoints.dtype != torch.float32 or checkpoints.dim() != 5:
             raise ValueError("checkpoints must be fp32 [N, H, max_checkpoints, d_k, d_v]")
-        _check(lib().kda_chunk_prefill_checkpoints(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
-            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
-            chunk, _dtype_code(q.dtype), _ptr(checkpoints), int(checkpoint_every),
-            checkpoints.shape[2], _ptr(workspace), ws_bytes, _stream(q.device)))
+        with _on(q.device):
+            _check(lib().kda_chunk_prefill_checkpoints(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+                _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
+                chunk, _dtype_code(q.dtype), _ptr(checkpoints), int(checkpoint_every),
+                checkpoints.shape[2], _ptr(workspace), ws_bytes, _stream(q.device)))
     return out, final_state
 
 
@@ -218,13 +229,14 @@ def chunk_prefill_from_host(q, k, v, z, beta, A, initial_state=None, segment_tok
         copy_streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
     _need_cuda(A, initial_state, final_state, workspace, *staging.values())
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().kda_chunk_prefill_from_host(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
-        _ptr(staging["q"]), _ptr(staging["k"]), _ptr(staging["v"]), _ptr(staging["z"]),
-        _ptr(staging["beta"]), _ptr(staging["o"]), _ptr(initial_state), _ptr(final_state),
-        B, T, H, dk, dv, _dtype_code(q.dtype), int(segment_tokens), _ptr(workspace), ws_bytes,
-        _stream(dev), ctypes.c_void_p(copy_streams[0].cuda_stream),
-        ctypes.c_void_p(copy_streams[1].cuda_stream)))
+    with _on(dev):
+        _check(lib().kda_chunk_prefill_from_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+            _ptr(staging["q"]), _ptr(staging["k"]), _ptr(staging["v"]), _ptr(staging["z"]),
+            _ptr(staging["beta"]), _ptr(staging["o"]), _ptr(initial_state), _ptr(final_state),
+            B, T, H, dk, dv, _dtype_code(q.dtype), int(segment_tokens), _ptr(workspace), ws_bytes,
+            _stream(dev), ctypes.c_void_p(copy_streams[0].cuda_stream),
+            ctypes.c_void_p(copy_streams[1].cuda_stream)))
     return out, final_state
 
 
@@ -235,9 +247,10 @@ def decode_step(q, k, v, z, beta, A, state, out=None):
     if out is None:
         out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
     _need_cuda(q, k, v, z, beta, A, state, out)
-    _check(lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
-                                 _ptr(state), _ptr(out), B, H, dk, dv, _dtype_code(q.dtype),
-                                 _stream(q.device)))
+    with _on(q.device):
+        _check(lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                     _ptr(state), _ptr(out), B, H, dk, dv, _dtype_code(q.dtype),
+                                     _stream(q.device)))
     return out
 
 
@@ -259,8 +272,9 @@ def selftest_bounded_wait(status: torch.Tensor, arrive: bool) -> None:
     _need_cuda(status)
     if status.dtype != torch.int32 or status.numel() < 1:
         raise ValueError("status must be an int32 CUDA tensor")
-    _check(lib().kda_selftest_bounded_wait(_ptr(status), int(bool(arrive)),
-                                           _stream(status.device)))
+    with _on(status.device):
+        _check(lib().kda_selftest_bounded_wait(_ptr(status), int(bool(arrive)),
+                                               _stream(status.device)))
 
 
 def chunk_prefill_static_workspace(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
@@ -281,10 +295,11 @@ def chunk_prefill_static_workspace(q, k, v, z, beta, A, initial_state=None, cu_s
     if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
     _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, cu_seqlens)
-    _check(lib().kda_chunk_prefill_static_workspace(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
-        _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
-        _dtype_code(q.dtype), _stream(q.device)))
+    with _on(q.device):
+        _check(lib().kda_chunk_prefill_static_workspace(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv, chunk,
+            _dtype_code(q.dtype), _stream(q.device)))
     return out, final_state
 
 
@@ -298,9 +313,10 @@ def spec_verify(q, k, v, z, beta, A, state, out=None):
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     _need_cuda(q, k, v, z, beta, A, state, out)
-    _check(lib().kda_spec_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
-                                 _ptr(state), _ptr(out), B, T, H, dk, dv, _dtype_code(q.dtype),
-                                 _stream(q.device)))
+    with _on(q.device):
+        _check(lib().kda_spec_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
+                                     _ptr(state), _ptr(out), B, T, H, dk, dv, _dtype_code(q.dtype),
+                                     _stream(q.device)))
     return out
 
 
@@ -311,7 +327,21 @@ def spec_commit(k, v, z, beta, A, state, n_accept):
     if n_accept.dtype != torch.int32:
         raise TypeError("n_accept must be int32")
     _need_cuda(k, v, z, beta, A, state, n_accept)
-    _check(lib().kda_spec_commit(_ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state),
-                                 _ptr(n_accept), B, T, H, dk, dv, _dtype_code(k.dtype),
-                                 _stream(k.device)))
+    with _on(k.device):
+        _check(lib().kda_spec_commit(_ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state),
+                                     _ptr(n_accept), B, T, H, dk, dv, _dtype_code(k.dtype),
+                                     _stream(k.device)))
     return state
+
+
+def static_workspace_status(out: torch.Tensor) -> torch.Tensor:
+    """kda_static_workspace_status: copies the device status word of the last
+    static-workspace prefill on ``out``'s device into ``out`` (an int32 CUDA tensor),
+    on the current stream.  0 after the stream finishes means every bounded wait of
+    that call was satisfied."""
+    _need_cuda(out)
+    if out.dtype != torch.int32 or out.numel() < 1:
+        raise ValueError("out must be an int32 CUDA tensor")
+    with _on(out.device):
+        _check(lib().kda_static_workspace_status(_ptr(out), _stream(out.device)))
+    return out

@@ -10,8 +10,6 @@
 // the scratch taken from a file-scope __device__ array of fixed size,
 // KDA_STATIC_WORKSPACE_BYTES.  The array exists on every GPU that loads the
 // library and is held until the process exits.
-#include <mutex>
-
 #include "../../include/kda.h"
 #include "kda_internal.h"
 
@@ -19,26 +17,16 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_workspace[KDA_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_ws_addr[kMaxDevices] = {};
-std::mutex g_ws_mutex;
-
-// Device address of g_static_workspace on the current device.  In host code the
-// symbol names a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress, called once per device with that device current.
+// Device address of g_static_workspace for the current device and context.  In
+// host code the symbol names a host-side stand-in, so the address must come
+// from cudaGetSymbolAddress with the right device current.  It is looked up on
+// every call rather than cached: after cudaDeviceReset, or in a second context
+// on the same device, the module is loaded again and the array may move.
 cudaError_t static_workspace_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_ws_mutex);
-    if (g_ws_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_workspace);
-        if (e != cudaSuccess) return e;
-        g_ws_addr[dev] = p;
-    }
-    *out = g_ws_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -64,4 +52,17 @@ extern "C" kda_status kda_chunk_prefill_static_workspace(
     return kda_chunk_prefill(q, k, v, z, beta, A, o, initial_state, final_state, cu_seqlens,
                              n_seqs, B, T, H, d_k, d_v, chunk, dtype, ws,
                              (size_t)KDA_STATIC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" kda_status kda_static_workspace_status(uint32_t* status, cudaStream_t stream) {
+    if (status == nullptr) return kda::report(KDA_ERR_INVALID_ARG, "status is NULL");
+    if ((reinterpret_cast<uintptr_t>(status) & 3u) != 0)
+        return kda::report(KDA_ERR_INVALID_ARG, "status is not 4-byte aligned");
+    void* ws = nullptr;
+    cudaError_t e = static_workspace_address(&ws);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(status, ws, sizeof(uint32_t), cudaMemcpyDefault, stream);
+    if (e != cudaSuccess)
+        return kda::report(KDA_ERR_CUDA, "kda_static_workspace_status: %s", cudaGetErrorString(e));
+    return kda::report(KDA_OK, "%s", "");
 }

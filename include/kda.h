@@ -113,7 +113,12 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *                  (KDA_ERR_UNSUPPORTED otherwise).
  *   workspace      device scratch of at least kda_chunk_prefill_workspace_size()
  *                  bytes (may be NULL when that size is 0); 256-byte aligned;
- *                  contents on entry are ignored.
+ *                  contents on entry are ignored.  Its first 32-bit word is the
+ *                  call's device status: the call clears it, and a kernel that
+ *                  gives up a bounded wait (about 2 s; nothing in a correct
+ *                  run waits that long) sets a nonzero bit there and returns
+ *                  instead of hanging.  Read it after the stream has finished:
+ *                  nonzero means o and the states of that call are not valid.
  * T == 0 (or every sequence empty) writes only the final states (copies of the
  * initial ones, or zeros).
  */
@@ -239,9 +244,13 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
  *   - Sizes whose workspace (kda_chunk_prefill_workspace_size) exceeds
  *     KDA_STATIC_WORKSPACE_BYTES are rejected with KDA_ERR_UNSUPPORTED before
  *     any launch; kda_last_error() says how much they would need.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The array lives on the current device: make the device that owns the
+ *     pointers and `stream` current before the call.  Each call looks up the
+ *     array's device address there (cudaGetSymbolAddress), so a reset device
+ *     or a second context gets its own array.  The first call on a device also
+ *     loads the library's kernels there; make it before any stream capture.
+ *   - The device status word of the call (see `workspace` above) sits in the
+ *     array; kda_static_workspace_status copies it out.
  *   - All calls share the one array and it keeps the last call's contents (the
  *     kernels clear what must start at zero).  Calls whose kernels overlap on
  *     the GPU -- concurrent streams, or several host threads -- race on it;
@@ -257,6 +266,21 @@ kda_status kda_chunk_prefill_static_workspace(const void *q, const void *k, cons
                                               int n_seqs, int B, int64_t T, int H, int d_k,
                                               int d_v, int chunk, kda_dtype dtype,
                                               cudaStream_t stream);
+
+/*
+ * kda_static_workspace_status -- copies the device status word of the last
+ * kda_chunk_prefill_static_workspace call on the current device (word 0 of
+ * the library's array; 0 = every bounded wait was satisfied) into *status,
+ * asynchronously on `stream`.  Issue it on the stream of that call (or after
+ * it), then read *status once the stream has finished.  Nonzero means the
+ * call's outputs are not valid.  The next static-workspace call clears the
+ * word again.  The pages have no counterpart; this only reports.
+ *   status  uint32_t, device or page-locked host memory, 4-byte aligned
+ *           (written).
+ * Returns KDA_ERR_INVALID_ARG for a null or misaligned pointer and
+ * KDA_ERR_CUDA if the lookup or the copy cannot be queued.
+ */
+kda_status kda_static_workspace_status(uint32_t *status, cudaStream_t stream);
 
 /*
  * kda_spec_verify / kda_spec_commit -- speculative decoding without a state

@@ -14,15 +14,22 @@ def rel_err(got, ref) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
-    scale = np.abs(ref).max()
+    scale = np.abs(ref).max() if ref.size else 0.0
     if scale == 0:
-        return float(np.abs(got).max())
+        return float(np.abs(got).max()) if got.size else 0.0
     return float(np.abs(got - ref).max() / scale)
+
+
+def report(what: str, err: float, tol: float, extra: str = "") -> None:
+    """Prints one margin line (visible with pytest -s): the measured relative error,
+    the bound it is held to, and their ratio."""
+    print(f"PARITY {what}: rel_err={err:.3e} tol={tol:.1e} used={err / tol:.1%}{extra}")
 
 
 def assert_parity(got, ref, dtype, what="", tol=None):
     tol = TOL[dtype] if tol is None else tol
     e = rel_err(got, ref)
+    report(what, e, tol)
     assert e <= tol, f"{what}: max|gpu-oracle|/max|oracle| = {e:.3e} > {tol:.1e}"
     return e
 

@@ -189,3 +189,10 @@ def test_from_host_rejects_bad_arguments(L):
 def test_selftest_rejects_bad_status_pointer(L):
     assert L.kda_selftest_bounded_wait(None, 0, None) == INVALID
     assert L.kda_selftest_bounded_wait(_fake(0x10002), 0, None) == INVALID   # not 4-byte aligned
+
+
+def test_static_workspace_status_rejects_bad_pointer(L):
+    assert L.kda_static_workspace_status(None, None) == INVALID
+    assert b"NULL" in L.kda_last_error()
+    assert L.kda_static_workspace_status(_fake(0x10002), None) == INVALID
+    assert b"aligned" in L.kda_last_error()
