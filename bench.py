@@ -483,7 +483,50 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
     out[f"prefill_d64_h{w64.H}_t{T64}"] = {
         "tensor_core_ms": t_tc, "tensor_core_tokens_per_s": T64 / (t_tc * 1e-3),
         "recurrent_ms": t_rec, "recurrent_tokens_per_s": T64 / (t_rec * 1e-3)}
+    del x64, ws64
+    out["segmented_prefill_t65536"] = measure_segmented(kda)
     return out
+
+
+def measure_segmented(kda, T: int = 65536):
+    """Segment-parallel prefill (kda_chunk_prefill_segmented) against the plain pass
+    (one segment) on B=1, T=65536, d=128 with few heads, where the plain state pass leaves
+    most SMs idle; per-kernel times from the library's profiling events."""
+    import torch
+    from dataclasses import replace
+    from gated_delta_rule_34_gb300.inputs import WORKLOADS, make_inputs
+    rows = {}
+    for H in (1, 4, 8, 16):
+        w = replace(WORKLOADS[2], H=H, seed=120 + H)
+        x = make_inputs(w, device="cuda", B=1, T=T)
+        G = kda.auto_segments(1, T, H, 128, 128)
+        row = {"auto_segments": G}
+        for g in sorted({1, G}):
+            ws = torch.empty(kda.segmented_workspace_size(1, T, H, 128, 128, g), dtype=torch.uint8,
+                             device="cuda")
+            o = torch.empty((1, T, H, 128), dtype=torch.bfloat16, device="cuda")
+            S = torch.empty((1, H, 128, 128), dtype=torch.float32, device="cuda")
+            run = lambda: kda.chunk_prefill_segmented(  # noqa: E731
+                x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], g, initial_state=x["S0"],
+                out=o, final_state=S, workspace=ws)
+            ms = _time_ms(run, iters=5, warm=2)
+            n_ev = 5 if g > 1 else 3
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            kda.set_profile_events(evs)
+            run()
+            kda.set_profile_events(None)
+            torch.cuda.synchronize()
+            parts = [evs[i].elapsed_time(evs[i + 1]) for i in range(n_ev - 1)]
+            names = (["chunk_prep", "trans_pass", "seg_combine", "state_pass"] if g > 1
+                     else ["chunk_prep", "state_pass"])
+            row[f"G{g}"] = {"ms": ms, "tokens_per_s": T / (ms * 1e-3),
+                            "kernel_ms": dict(zip(names, parts))}
+            del ws, o, S
+        if G > 1:
+            row["speedup"] = row["G1"]["ms"] / row[f"G{G}"]["ms"]
+        rows[f"H{H}"] = row
+        del x
+    return rows
 
 
 def e2e_prefill(kda, xp, wp, steps: int, segment_tokens: int = 8192):

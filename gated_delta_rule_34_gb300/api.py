@@ -71,6 +71,14 @@ def _declare(lib):
     lib.kda_set_profile_events.restype = i32
     lib.kda_selftest_bounded_wait.argtypes = [vp, i32, vp]
     lib.kda_selftest_bounded_wait.restype = i32
+    lib.kda_chunk_prefill_segmented.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
+                                                i32, i32, i32, i32, i32, vp, sz, vp]
+    lib.kda_chunk_prefill_segmented.restype = i32
+    lib.kda_chunk_prefill_segmented_workspace_size.argtypes = [i32, i64, i32, i32, i32, i32, i32,
+                                                               i32]
+    lib.kda_chunk_prefill_segmented_workspace_size.restype = sz
+    lib.kda_chunk_prefill_auto_segments.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    lib.kda_chunk_prefill_auto_segments.restype = i32
     lib.kda_static_workspace_status.argtypes = [vp, vp]
     lib.kda_static_workspace_status.restype = i32
     return lib
@@ -194,6 +202,42 @@ def chunk_prefill(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, chun
                 _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), n_seqs, B, T, H, dk, dv,
                 chunk, _dtype_code(q.dtype), _ptr(checkpoints), int(checkpoint_every),
                 checkpoints.shape[2], _ptr(workspace), ws_bytes, _stream(q.device)))
+    return out, final_state
+
+
+def auto_segments(B: int, T: int, H: int, d_k: int, d_v: int, chunk: int = 64,
+                  dtype: torch.dtype = torch.bfloat16) -> int:
+    """Segment count kda_chunk_prefill uses for a fixed-length batch on the current device."""
+    return int(lib().kda_chunk_prefill_auto_segments(B, T, H, d_k, d_v, chunk, _dtype_code(dtype)))
+
+
+def segmented_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int, n_segments: int,
+                             chunk: int = 64, dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(lib().kda_chunk_prefill_segmented_workspace_size(B, T, H, d_k, d_v, chunk,
+                                                                _dtype_code(dtype), n_segments))
+
+
+def chunk_prefill_segmented(q, k, v, z, beta, A, n_segments: int, initial_state=None,
+                            chunk: int = 64, out=None, final_state=None, workspace=None):
+    """Prefill through kda_chunk_prefill_segmented: each of the B fixed-length sequences is
+    split into ``n_segments`` segments whose state passes run in parallel.  Same tensors as
+    ``chunk_prefill`` without cu_seqlens.  Returns (o, final_state)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    need = segmented_workspace_size(B, T, H, dk, dv, n_segments, chunk, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need_cuda(q, k, v, z, beta, A, out, initial_state, final_state, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with _on(q.device):
+        _check(lib().kda_chunk_prefill_segmented(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(out),
+            _ptr(initial_state), _ptr(final_state), B, T, H, dk, dv, chunk, _dtype_code(q.dtype),
+            int(n_segments), _ptr(workspace), ws_bytes, _stream(q.device)))
     return out, final_state
 
 

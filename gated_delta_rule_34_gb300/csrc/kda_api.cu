@@ -124,11 +124,37 @@ kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype d
     return use_chunked_tc(d_k, d_v, chunk, dtype) ? KDA_PATH_CHUNKED_TC : KDA_PATH_RECURRENT;
 }
 
+// Segment count for kda_chunk_prefill: automatic for fixed-length batches on
+// the tensor-core path (n_seqs == B marks a fixed-length query), 1 otherwise.
+static int auto_segments(int n_seqs, int B, int64_t T, int H, int d_k, int d_v) {
+    if (n_seqs != B) return 1;
+    return kda::chunked_tc_auto_segments(B, T, H, d_k, d_v, device_sm_count());
+}
+
+static size_t tc_workspace(int n_seqs, int B, int64_t T, int H, int G) {
+    // T is the per-sequence length of a fixed-length batch, or the packed total
+    // with B = 1 (then G is 1).
+    return kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * T, H, T, G);
+}
+
 size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int d_k, int d_v,
                                         int chunk, kda_dtype dtype) {
     if (n_seqs <= 0 || B <= 0 || T < 0 || H <= 0) return 0;
     if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
-    return kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * T, H);
+    return tc_workspace(n_seqs, B, T, H, auto_segments(n_seqs, B, T, H, d_k, d_v));
+}
+
+size_t kda_chunk_prefill_segmented_workspace_size(int B, int64_t T, int H, int d_k, int d_v,
+                                                  int chunk, kda_dtype dtype, int n_segments) {
+    if (B <= 0 || T < 0 || H <= 0 || n_segments <= 0) return 0;
+    if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
+    return tc_workspace(B, B, T, H, n_segments);
+}
+
+int kda_chunk_prefill_auto_segments(int B, int64_t T, int H, int d_k, int d_v, int chunk,
+                                    kda_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || !use_chunked_tc(d_k, d_v, chunk, dtype)) return 1;
+    return kda::chunked_tc_segments_used(T, auto_segments(B, B, T, H, d_k, d_v));
 }
 
 static kda_status prefill_impl(const void* q, const void* k, const void* v, const void* z,
@@ -137,7 +163,7 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
                                const int32_t* cu_seqlens, int n_seqs, int B, int64_t T, int H,
                                int d_k, int d_v, int chunk, kda_dtype dtype, void* workspace,
                                size_t workspace_bytes, const kda::CheckpointSpec& ck,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int n_segments = 0) {
     if (!valid_dtype(dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B <= 0 || T < 0 || H <= 0 || d_k <= 0 || d_v <= 0 || n_seqs <= 0)
         return fail(KDA_ERR_INVALID_ARG, "bad sizes B=%d T=%lld H=%d d_k=%d d_v=%d n_seqs=%d", B,
@@ -176,7 +202,21 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         if (T_total > (int64_t)INT32_MAX - 64)
             return fail(KDA_ERR_UNSUPPORTED, "the tensor-core path takes fewer than 2^31 tokens (%lld)",
                         (long long)T_total);
-        const size_t need = kda::chunked_tc_workspace_bytes(n_seqs, T_total, H);
+        // Segments: n_segments > 0 asks for that many (fixed-length batches
+        // only); 0 picks them automatically, falling back to the plain pass when
+        // the workspace only covers that.
+        int G = 1;
+        if (n_segments > 0) {
+            if (cu_seqlens && n_segments > 1)
+                return fail(KDA_ERR_UNSUPPORTED, "segments need a fixed-length batch (cu_seqlens == NULL)");
+            if ((int64_t)B * kda::chunked_tc_segments_used(T, n_segments) > 65535)
+                return fail(KDA_ERR_UNSUPPORTED, "B x segments must be <= 65535");
+            G = n_segments;
+        } else if (!cu_seqlens) {
+            G = auto_segments(n_seqs, B, T, H, d_k, d_v);
+            if (G > 1 && workspace_bytes < tc_workspace(n_seqs, B, T, H, G)) G = 1;
+        }
+        const size_t need = tc_workspace(n_seqs, cu_seqlens ? 1 : B, cu_seqlens ? T_total : T, H, G);
         if (need > 0) {
             if (workspace == nullptr || workspace_bytes < need)
                 return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu at %p",
@@ -186,7 +226,8 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         }
         return cuda_status(kda::run_chunked_tc(q, k, v, z, beta, A, o, initial_state,
                                                final_state, cu_seqlens, n_seqs, T, T_total, H,
-                                               d_k, d_v, workspace, ck, stream, device_sm_count()),
+                                               d_k, d_v, workspace, ck, stream, device_sm_count(),
+                                               G),
                            "kda_chunk_prefill (chunked tensor-core path)");
     }
     kda::profile_event(0, stream);
@@ -206,6 +247,22 @@ kda_status kda_chunk_prefill(const void* q, const void* k, const void* v, const 
     return prefill_impl(q, k, v, z, beta, A, o, initial_state, final_state, cu_seqlens, n_seqs, B,
                         T, H, d_k, d_v, chunk, dtype, workspace, workspace_bytes,
                         kda::CheckpointSpec{}, stream);
+}
+
+kda_status kda_chunk_prefill_segmented(const void* q, const void* k, const void* v, const void* z,
+                                       const void* beta, const float* A, void* o,
+                                       const float* initial_state, float* final_state, int B,
+                                       int64_t T, int H, int d_k, int d_v, int chunk,
+                                       kda_dtype dtype, int n_segments, void* workspace,
+                                       size_t workspace_bytes, cudaStream_t stream) {
+    if (n_segments <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "n_segments must be >= 1 (got %d)", n_segments);
+    if (!use_chunked_tc(d_k, d_v, chunk, dtype))
+        return fail(KDA_ERR_UNSUPPORTED, "segments run on the tensor-core path only (bf16, chunk 64, "
+                                         "d_k a multiple of 16 and d_v a multiple of 32, both <= 128)");
+    return prefill_impl(q, k, v, z, beta, A, o, initial_state, final_state, nullptr, B, B, T, H,
+                        d_k, d_v, chunk, dtype, workspace, workspace_bytes, kda::CheckpointSpec{},
+                        stream, n_segments);
 }
 
 kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const void* v_h,
@@ -247,7 +304,7 @@ kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const v
     KDA_REQUIRE_PTR(beta_d);
     KDA_REQUIRE_PTR(o_d);
     const int64_t seg = segment_tokens < T ? segment_tokens : T;
-    const size_t need = kda::chunked_tc_workspace_bytes(1, seg, H);
+    const size_t need = tc_workspace(1, 1, seg, H, 1);
     if (workspace == nullptr || workspace_bytes < need)
         return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
                     workspace_bytes);
@@ -290,7 +347,7 @@ kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const v
                               static_cast<const char*>(beta_d) + tok * bb, A,
                               static_cast<char*>(o_d) + tok * vb, S_in, S, nullptr, 1, 1, len, H,
                               d_k, d_v, 64, dtype, workspace, workspace_bytes,
-                              kda::CheckpointSpec{}, stream);
+                              kda::CheckpointSpec{}, stream, 1);
             if (st != KDA_OK) break;
             if (e == cudaSuccess) e = cudaEventRecord(ev_out, stream);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h_stream, ev_out, 0);

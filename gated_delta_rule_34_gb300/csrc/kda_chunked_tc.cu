@@ -1071,6 +1071,84 @@ chunk_prep_kernel(const __grid_constant__ InputMaps maps, const __nv_bfloat16* _
 // X, O' and lam bypass shared memory: the warps that use them load their own
 // pieces straight into registers two chunks ahead.
 // ============================================================================
+// Update-warp fragment of a 128 x 32 tile of S (rows c, tile columns j): warp
+// w holds rows 32 q4 .. 32 q4 + 31 (q4 = w mod 4) and tile columns jh .. jh +
+// 15 (jh = 16 ((w / 4) mod 2)) in the layout of a 16x256b TMEM load: element e
+// (0..15) of a thread is
+//   row    32 q4 + 16 (e >> 3) + 8 ((e >> 1) & 1) + lane / 4,
+//   column jh + 8 ((e >> 2) & 1) + 2 (lane mod 4) + (e & 1),
+// so elements 2i and 2i + 1 are adjacent columns of one row.
+struct Frag {
+    int q4, jh, lane;
+    __device__ __forceinline__ Frag(int warp, int lane_)
+        : q4(warp & 3), jh(16 * ((warp >> 2) & 1)), lane(lane_) {}
+    __device__ __forceinline__ int row(int e) const {
+        return 32 * q4 + 16 * (e >> 3) + 8 * ((e >> 1) & 1) + (lane >> 2);
+    }
+    __device__ __forceinline__ int col(int e) const {
+        return jh + 8 * ((e >> 2) & 1) + 2 * (lane & 3) + (e & 1);
+    }
+};
+
+// Writes the fragment `st` as copy `p` of the tile's S^T, the bf16 B operand
+// of the state products (rows j, 128-byte-swizzled K-major over c; copies 8 KB
+// apart from `st_base`): per 16-row half hh one transposing stmatrix of the
+// four 8 x 8 matrices (m, k) = (i / 2, i mod 2), rows c = 32 q4 + 16 hh + 8 k ..,
+// columns j = jh + 8 m ..  Thread t gives stored row j = jh + 8 m + t mod 8 of
+// matrix i = t / 8.
+__device__ __forceinline__ void write_st_copy(uint8_t* st_base, int p, const Frag& f,
+                                              const float (&st)[16]) {
+    const int i = f.lane >> 3, m = i >> 1, k = i & 1, jrow = f.jh + 8 * m + (f.lane & 7);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 32 * f.q4 + 16 * hh + 8 * k;
+        uint32_t rg[4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+            const int e = 8 * hh + 4 * (ii >> 1) + 2 * (ii & 1);
+            rg[ii] = pack_bf16x2(st[e], st[e + 1]);
+        }
+        stmatrix_x4_trans(smem_u32(st_base + p * 8192 + (c0 >> 6) * 4096 + sw128(jrow, (c0 & 63) >> 3)), rg);
+    }
+}
+
+// X at a fragment's element pairs and lam at its four rows, for one chunk.
+struct XRegs {
+    uint32_t x[8];
+    float lam[4];
+};
+__device__ __forceinline__ void load_x_frag(const uint8_t* pk, int tile, const Frag& f, XRegs& r) {
+    const uint8_t* xt = pk + PKG_X + tile * 8192;
+    // row(8 hh + 2 k): columns 2w, 2w + 1 (m = 0) and 8 + 2w, 9 + 2w (m = 1) of
+    // the warp's 16-column group, 8 contiguous bytes in the package's pair
+    // order (w = lane mod 4)
+    const uint32_t xoff = 8u * (f.lane & 1);
+    const int xch = 2 * (f.jh >> 4) + ((f.lane & 3) >> 1);
+#pragma unroll
+    for (int hk = 0; hk < 4; ++hk) {
+        const int e = 8 * (hk >> 1) + 2 * (hk & 1);
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(xt + jtile_off(f.row(e), xch) + xoff));
+        r.x[e >> 1] = v.x;
+        r.x[(e + 4) >> 1] = v.y;
+    }
+#pragma unroll
+    for (int hk = 0; hk < 4; ++hk)
+        r.lam[hk] = __ldg(reinterpret_cast<const float*>(pk + PKG_LAM) + f.row(2 * hk + ((hk >> 1) * 4)));
+}
+
+// st <- lam (.) st + x - d on the fragment (x omitted when `with_x` is false).
+__device__ __forceinline__ void update_frag(float (&st)[16], const float (&d)[16], const XRegs& xr,
+                                            bool with_x) {
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+        const float2 x = with_x ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr.x[e >> 1]))
+                                : make_float2(0.f, 0.f);
+        const float lam = xr.lam[2 * (e >> 3) + ((e >> 1) & 1)];
+        st[e] = fmaf(lam, st[e], x.x - d[e]);
+        st[e + 1] = fmaf(lam, st[e + 1], x.y - d[e + 1]);
+    }
+}
+
 __device__ __forceinline__ void issue_stage(uint8_t* stg, const uint8_t* pkg, uint64_t* full) {
     mbar_expect_tx(full, ST_BYTES);
     bulk_g2s(stg, pkg + PKG_B0, ST_BYTES, full);
@@ -1096,17 +1174,30 @@ __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// Segments of the segment-parallel prefill: sequence n is split into G
+// segments of cps chunks; segment g starts from S_start[(n H + h)(G - 1) + g - 1]
+// (g >= 1) or from S0 (g = 0).  G = 1 is the plain pass.
+struct SegSpec {
+    int G = 1;
+    int cps = 0x7fffffff;           // chunks per segment
+    const float* S_start = nullptr;  // [N, H, G - 1, d_k, d_v] fp32
+};
+
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
-                  int dk, int dv, CheckpointSpec ck) {
-    const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
+                  int dk, int dv, CheckpointSpec ck, SegSpec seg) {
+    const int tile = blockIdx.x, n = blockIdx.y / seg.G, g = blockIdx.y % seg.G, h = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = tile * kJ;
 
     int64_t bos, eos;
-    const int64_t slot0 = seq_slot_base(map, n, bos, eos);
-    const int nc = (int)((eos - bos + kC - 1) / kC);
+    const int64_t slot_seq = seq_slot_base(map, n, bos, eos);
+    const int nc_seq = (int)((eos - bos + kC - 1) / kC);
+    const int c0 = (int)((int64_t)g * seg.cps < nc_seq ? (int64_t)g * seg.cps : nc_seq);
+    const int nc = (nc_seq - c0) < seg.cps ? (nc_seq - c0) : seg.cps;   // this segment's chunks
+    const int64_t slot0 = slot_seq + c0;
+    const bool last_seg = g == seg.G - 1;
     uint32_t* status = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(ws));
     const uint8_t* pkgs = ws + WS_HEADER;
     auto pkg_of = [&](int chunk) { return pkgs + ((size_t)(slot0 + chunk) * H + h) * PKG_BYTES; };
@@ -1122,62 +1213,35 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(dfree + 2);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
-    // Update warp w holds rows 32 q4 .. 32 q4 + 31 (q4 = w mod 4) and tile
-    // columns jh .. jh + 15 (jh = 16 (w / 4)) in the layout of a 16x256b TMEM
-    // load: element e (0..15) of a thread is
-    //   row    erow(e) = 32 q4 + 16 (e >> 3) + 8 ((e >> 1) & 1) + lane / 4,
-    //   column ecol(e) = jh + 8 ((e >> 2) & 1) + 2 (lane mod 4) + (e & 1),
-    // so elements 2i and 2i + 1 are adjacent columns of one row.
-    const int q4 = warp & 3;
-    const int jh = 16 * ((warp >> 2) & 1);
+    const Frag f(warp, lane);
     const bool upd = warp < kUpdWarps;
-    auto erow = [&](int e) { return 32 * q4 + 16 * (e >> 3) + 8 * ((e >> 1) & 1) + (lane >> 2); };
-    auto ecol = [&](int e) { return jh + 8 * ((e >> 2) & 1) + 2 * (lane & 3) + (e & 1); };
     // this tile of S0 / S1 ([d_k][d_v] per (n, h)); rows d_k .. 127 of a
     // narrower head stay 0 on chip and are neither read nor written
     const size_t smat = ((size_t)n * H + h) * dk * dv + j0;
+    const float* S_in = g == 0 ? (S0 ? S0 + smat : nullptr)
+                               : seg.S_start + (((size_t)n * H + h) * (seg.G - 1) + (g - 1)) * dk * dv + j0;
     float st[16];
     auto store_state = [&](float* mat) {                             // mat: S of (n, h) + j0
 #pragma unroll
         for (int e = 0; e < 16; e += 2)
-            if (erow(e) < dk)
-                *reinterpret_cast<float2*>(mat + (size_t)erow(e) * dv + ecol(e)) = make_float2(st[e], st[e + 1]);
+            if (f.row(e) < dk)
+                *reinterpret_cast<float2*>(mat + (size_t)f.row(e) * dv + f.col(e)) = make_float2(st[e], st[e + 1]);
     };
     if (upd) {
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-            const float2 v = S0 && erow(e) < dk
-                                 ? __ldg(reinterpret_cast<const float2*>(S0 + smat + (size_t)erow(e) * dv + ecol(e)))
+            const float2 v = S_in && f.row(e) < dk
+                                 ? __ldg(reinterpret_cast<const float2*>(S_in + (size_t)f.row(e) * dv + f.col(e)))
                                  : make_float2(0.f, 0.f);
             st[e] = v.x;
             st[e + 1] = v.y;
         }
     }
-    if (nc == 0 || (smem_u32(smem_raw) & 1023u) != 0) {
-        if (nc != 0 && tid == 0) set_status(status, kErrSmemAlign);
-        if (S1 && upd) store_state(S1 + smat);
+    if (nc <= 0 || (smem_u32(smem_raw) & 1023u) != 0) {
+        if (nc > 0 && tid == 0) set_status(status, kErrSmemAlign);
+        if (S1 && upd && last_seg) store_state(S1 + smat);
         return;
     }
-
-    // Copy p of the tile's S^T as the bf16 B operand (rows j, 128-byte-swizzled
-    // K-major over c): per 16-row half hh one transposing stmatrix of the four
-    // 8 x 8 matrices (m, k) = (i / 2, i mod 2): rows c = 32 q4 + 16 hh + 8 k ..,
-    // columns j = jh + 8 m ..  Thread t gives stored row j = jh + 8 m + t mod 8
-    // of matrix i = t / 8.
-    auto write_st = [&](int p) {
-        const int i = lane >> 3, m = i >> 1, k = i & 1, jrow = jh + 8 * m + (lane & 7);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int c0 = 32 * q4 + 16 * hh + 8 * k;
-            uint32_t rg[4];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const int e = 8 * hh + 4 * (ii >> 1) + 2 * (ii & 1);
-                rg[ii] = pack_bf16x2(st[e], st[e + 1]);
-            }
-            stmatrix_x4_trans(smem_u32(sm + S_ST + p * 8192 + (c0 >> 6) * 4096 + sw128(jrow, (c0 & 63) >> 3)), rg);
-        }
-    };
 
     if (warp == 0) tmem_alloc<kTmemCols>(tslot);
     if (tid == 32) {
@@ -1194,7 +1258,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
         *abort = 0;
         fence_mbar_init();
     }
-    if (upd) write_st(0);
+    if (upd) write_st_copy(sm + S_ST, 0, f, st);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1299,7 +1363,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dfree + b);
-            const int64_t t0 = bos + (int64_t)cc * kC;
+            const int64_t t0 = bos + (int64_t)(c0 + cc) * kC;
             if (act && t < eos - t0) {
                 uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(t0 + t) * H + h) * dv + j0);
 #pragma unroll
@@ -1326,29 +1390,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
         if (!ok) *abort = 1;
     } else {
         // ------------------------------- state S <- lam (.) S - (N S) + X
-        const uint32_t tl = tbase + ((uint32_t)(32 * q4) << 16) + jh;
-        // X at the thread's element pairs and lam at its four rows, of chunk m,
-        // loaded two chunks ahead of their use
-        struct XRegs { uint32_t x[8]; float lam[4]; };
-        auto load_x = [&](int m, XRegs& r) {
-            const uint8_t* pk = pkg_of(m);
-            const uint8_t* xt = pk + PKG_X + tile * 8192;
-            // row erow(8 hh + 2 k): columns 2w, 2w + 1 (m = 0) and 8 + 2w, 9 + 2w
-            // (m = 1) of the warp's 16-column group, 8 contiguous bytes in the
-            // package's pair order (w = lane mod 4)
-            const uint32_t xoff = 8u * (lane & 1);
-            const int xch = 2 * (jh >> 4) + ((lane & 3) >> 1);
-#pragma unroll
-            for (int hk = 0; hk < 4; ++hk) {
-                const int e = 8 * (hk >> 1) + 2 * (hk & 1);
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(xt + jtile_off(erow(e), xch) + xoff));
-                r.x[e >> 1] = v.x;
-                r.x[(e + 4) >> 1] = v.y;
-            }
-#pragma unroll
-            for (int hk = 0; hk < 4; ++hk)
-                r.lam[hk] = __ldg(reinterpret_cast<const float*>(pk + PKG_LAM) + erow(2 * hk + ((hk >> 1) * 4)));
-        };
+        const uint32_t tl = tbase + ((uint32_t)(32 * f.q4) << 16) + f.jh;
         auto step = [&](int cc, XRegs& xr) -> bool {
             const int b = cc & 1;
             ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
@@ -1358,17 +1400,11 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             tmem_ld_16x256b_x2(tl + b * kDBuf, *reinterpret_cast<float(*)[8]>(d));
             tmem_ld_16x256b_x2(tl + (16u << 16) + b * kDBuf, *reinterpret_cast<float(*)[8]>(d + 8));
             tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xr.x[e >> 1]));
-                const float lam = xr.lam[2 * (e >> 3) + ((e >> 1) & 1)];
-                st[e] = fmaf(lam, st[e], x.x - d[e]);
-                st[e + 1] = fmaf(lam, st[e + 1], x.y - d[e + 1]);
-            }
+            update_frag(st, d, xr, true);
             if (cc + 1 < nc) {
                 // S^T copy (cc + 1) & 1 is still read by chunk cc - 1's O product
                 if (cc >= 1) ok = role_wait(odone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1, abort) && ok;
-                write_st((cc + 1) & 1);
+                write_st_copy(sm + S_ST, (cc + 1) & 1, f, st);
             }
             fence_async_smem();
             tc_fence_before();
@@ -1377,24 +1413,24 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 if (cc + 1 < nc) mbar_arrive(stready + ((cc + 1) & 1));
                 mbar_arrive(dfree + b);
             }
-            if (cc + 2 < nc) load_x(cc + 2, xr);
+            if (cc + 2 < nc) load_x_frag(pkg_of(cc + 2), tile, f, xr);
             // Checkpoint: the state after every `ck.every` tokens of this sequence.
             if (ck.out) {
-                const int64_t done = (int64_t)(cc + 1) * kC;
+                const int64_t done = (int64_t)(c0 + cc + 1) * kC;
                 if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
                     store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv + j0);
             }
             return true;
         };
         XRegs xa, xb;
-        load_x(0, xa);
-        if (nc > 1) load_x(1, xb);
+        load_x_frag(pkg_of(0), tile, f, xa);
+        if (nc > 1) load_x_frag(pkg_of(1), tile, f, xb);
         for (int cc = 0; cc < nc; cc += 2) {
             if (!step(cc, xa)) break;
             if (cc + 1 < nc && !step(cc + 1, xb)) break;
         }
         if (!ok) *abort = 1;
-        if (S1) store_state(S1 + smat);
+        if (S1 && last_seg) store_state(S1 + smat);
     }
     if (!ok) set_status(status, kErrStateWait);
 
@@ -1403,6 +1439,264 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc<kTmemCols>(tbase);
+    }
+}
+
+// ============================================================================
+// Segment-parallel prefill ("Kimi K3 architecture: how an open model with a
+// million-token context competes with market leaders", section "GPU level: the
+// long-context scheduler": the segments of a long sequence are processed in
+// parallel and merged into the exact state; the pair kept per segment is the
+// context-parallel pair of "How Kimi K3 is built: 2.8 trillion parameters,
+// linear attention and agents for a million tokens", section "How to serve two
+// different caches").  Per chunk the state moves by S <- F_c S + X_c with
+// F_c = Diag(lam_c) - N_c, so over segment g the state goes to M_g S_in + X_g
+// with M_g = prod F_c and X_g = the segment's end state from a zero start.
+//   trans_pass   per (sequence, head, segment g < G - 1) the chain over
+//                Y = [X | M] (d_v + d_k columns) from Y0 = [0 | I]:
+//                Y <- Diag(lam) Y - N Y + [X_c | 0]; one CTA per 32-column tile
+//                of Y, no outputs.
+//   seg_combine  S_start(g + 1) = M_g S_start(g) + X_g in fp32, sequential over
+//                the segments (S_start(0) = the initial state).
+//   state_pass   the plain pass, one CTA per (segment, 32-column tile of S),
+//                from S_start(g): outputs of the segment's tokens, final state
+//                from the last segment.
+// The transition pass needs neither Q' nor O': only update warps, an MMA
+// issuer and a copy warp, with a two-stage ring of the N operand, so that two
+// of its CTAs share an SM.
+// ============================================================================
+constexpr int kTransThreads = 32 * 10;
+constexpr int kTStages = 2;
+constexpr uint32_t TST_BYTES = 32768;               // N only: two K-blocks of 128 rows
+constexpr uint32_t T_ST = kTStages * TST_BYTES;     // then two S^T copies of 8 KB
+constexpr uint32_t T_BAR = T_ST + 2 * 8192;
+constexpr uint32_t T_SMEM = T_BAR + 256 + 1024;     // + slack for aligning the base
+constexpr uint32_t kTTmemCols = 64;                 // two 32-column accumulators
+constexpr uint32_t SEG_Y_COLS = 256;                // row pitch of a stored [X | M] (fp32)
+constexpr size_t SEG_Y_BYTES = (size_t)128 * SEG_Y_COLS * 4;   // per (sequence, head, segment)
+constexpr size_t SEG_S_BYTES = (size_t)128 * 128 * 4;          // room for one start state
+static_assert(T_SMEM * 2 <= 232448, "two transition-pass CTAs per SM");
+
+__device__ __forceinline__ void issue_nstage(uint8_t* stg, const uint8_t* pkg, uint64_t* full) {
+    mbar_expect_tx(full, TST_BYTES);
+    bulk_g2s(stg, pkg + PKG_B0, 16384, full);                  // N rows of K-block 0
+    bulk_g2s(stg + 16384, pkg + PKG_B0 + PKG_BK, 16384, full);  // and of K-block 1
+}
+
+__global__ void __launch_bounds__(kTransThreads, 2)
+trans_pass_kernel(uint8_t* __restrict__ ws, float* __restrict__ Y_out, SeqMap map, int H, int dk,
+                  int dv, SegSpec seg) {
+    const int tile = blockIdx.x, n = blockIdx.y / (seg.G - 1), g = blockIdx.y % (seg.G - 1);
+    const int h = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nx = dv / kJ;                          // tiles of the X part; the rest are M
+    const bool mpart = tile >= nx;
+    const int m0 = kJ * (tile - nx);                 // first identity column of an M tile
+    const int ycol0 = mpart ? 128 + m0 : kJ * tile;  // its first column in the stored Y
+
+    int64_t bos, eos;
+    const int64_t slot_seq = seq_slot_base(map, n, bos, eos);
+    const int nc_seq = (int)((eos - bos + kC - 1) / kC);
+    const int c0 = (int)((int64_t)g * seg.cps < nc_seq ? (int64_t)g * seg.cps : nc_seq);
+    const int nc = (nc_seq - c0) < seg.cps ? (nc_seq - c0) : seg.cps;
+    const int64_t slot0 = slot_seq + c0;
+    uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+    const uint8_t* pkgs = ws + WS_HEADER;
+    auto pkg_of = [&](int chunk) { return pkgs + ((size_t)(slot0 + chunk) * H + h) * PKG_BYTES; };
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + T_BAR);        // [2]
+    uint64_t* sfree = full + kTStages;                                 // [2]
+    uint64_t* sdone = sfree + kTStages;                                // [2]
+    uint64_t* stready = sdone + 2;                                     // [2]
+    uint64_t* dfree = stready + 2;                                     // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dfree + 2);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const Frag f(warp, lane);
+    const bool upd = warp < kUpdWarps;
+    float st[16];
+    if (upd) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) st[e] = (mpart && f.row(e) == m0 + f.col(e)) ? 1.f : 0.f;
+    }
+    float* ydst = Y_out + (((size_t)n * H + h) * (seg.G - 1) + g) * 128 * SEG_Y_COLS + ycol0;
+    auto store_y = [&]() {
+#pragma unroll
+        for (int e = 0; e < 16; e += 2)
+            if (f.row(e) < dk)
+                *reinterpret_cast<float2*>(ydst + (size_t)f.row(e) * SEG_Y_COLS + f.col(e)) =
+                    make_float2(st[e], st[e + 1]);
+    };
+    if (nc <= 0) {
+        if (upd) store_y();
+        return;
+    }
+
+    if (warp == 0) tmem_alloc<kTTmemCols>(tslot);
+    if (tid == 32) {
+        for (int p = 0; p < kTStages; ++p) {
+            mbar_init(full + p, 1);
+            mbar_init(sfree + p, 1);
+        }
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(sdone + p, 1);
+            mbar_init(stready + p, kUpdWarps);
+            mbar_init(dfree + p, kUpdWarps);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (upd) write_st_copy(sm + T_ST, 0, f, st);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    bool ok = true;
+
+    if (warp == 9) {
+        // ------------------------------------------------ N operand copies
+        if (lane == 0) {
+            int m = 0;
+            for (; m < kTStages && m < nc; ++m) issue_nstage(sm + m * TST_BYTES, pkg_of(m), full + m);
+            for (int p = kTStages; p < kL2Ahead && p < nc; ++p) {
+                bulk_prefetch_l2(pkg_of(p) + PKG_B0, 16384);
+                bulk_prefetch_l2(pkg_of(p) + PKG_B0 + PKG_BK, 16384);
+            }
+            for (; m < nc; ++m) {
+                ok = role_wait(sfree + m % kTStages, ((m - kTStages) / kTStages) & 1, abort) && ok;
+                if (!ok) break;
+                issue_nstage(sm + (m % kTStages) * TST_BYTES, pkg_of(m), full + m % kTStages);
+                const int pf = m + kL2Ahead - kTStages;
+                if (pf < nc) {
+                    bulk_prefetch_l2(pkg_of(pf) + PKG_B0, 16384);
+                    bulk_prefetch_l2(pkg_of(pf) + PKG_B0 + PKG_BK, 16384);
+                }
+            }
+            if (!ok) {
+                *abort = 1;
+                for (int k = m > kTStages ? m - kTStages : 0; k < m; ++k)
+                    mbar_wait(full + k % kTStages, (k / kTStages) & 1);
+            }
+        }
+    } else if (warp == 8) {
+        // ----------------------------------------------- product D = N Y^T'
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, kJ);
+            int cc = 0;
+            for (; cc < nc; ++cc) {
+                const int b = cc & 1;
+                if (cc >= 2) ok = role_wait(dfree + b, ((cc - 2) >> 1) & 1, abort) && ok;
+                ok = role_wait(full + cc % kTStages, (cc / kTStages) & 1, abort) && ok;
+                if (cc >= 1) ok = role_wait(stready + b, ((cc - 1) >> 1) & 1, abort) && ok;
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t bdesc0 = desc_sw128(smem_u32(sm + T_ST + b * 8192));
+                const uint64_t adesc0 = desc_sw128(smem_u32(sm + (cc % kTStages) * TST_BYTES));
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + b * kJ, adesc0 + ((kb * 16384 + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, ks > 0);
+                }
+                mma_commit(sdone + b);
+                mma_commit(sfree + cc % kTStages);
+            }
+            if (!ok) {
+                *abort = 1;
+                if (cc > 0) mbar_wait(sdone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1);
+            }
+        }
+    } else if (upd) {
+        // -------------------------------- Y <- lam (.) Y - (N Y) + [X | 0]
+        const uint32_t tl = tbase + ((uint32_t)(32 * f.q4) << 16) + f.jh;
+        const int xtile = mpart ? 0 : tile;
+        auto step = [&](int cc, XRegs& xr) -> bool {
+            const int b = cc & 1;
+            ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
+            if (!ok) return false;
+            tc_fence_after();
+            float d[16];
+            tmem_ld_16x256b_x2(tl + b * kJ, *reinterpret_cast<float(*)[8]>(d));
+            tmem_ld_16x256b_x2(tl + (16u << 16) + b * kJ, *reinterpret_cast<float(*)[8]>(d + 8));
+            tmem_wait_ld();
+            update_frag(st, d, xr, !mpart);
+            // copy (cc + 1) & 1 was last read by chunk cc - 1's product, which
+            // completed before chunk cc's (sdone above)
+            if (cc + 1 < nc) write_st_copy(sm + T_ST, (cc + 1) & 1, f, st);
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (cc + 1 < nc) mbar_arrive(stready + ((cc + 1) & 1));
+                mbar_arrive(dfree + b);
+            }
+            if (cc + 2 < nc) load_x_frag(pkg_of(cc + 2), xtile, f, xr);
+            return true;
+        };
+        XRegs xa, xb;
+        load_x_frag(pkg_of(0), xtile, f, xa);
+        if (nc > 1) load_x_frag(pkg_of(1), xtile, f, xb);
+        for (int cc = 0; cc < nc; cc += 2) {
+            if (!step(cc, xa)) break;
+            if (cc + 1 < nc && !step(cc + 1, xb)) break;
+        }
+        if (!ok) *abort = 1;
+        store_y();
+    }
+    if (!ok) set_status(status, kErrStateWait);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<kTTmemCols>(tbase);
+    }
+}
+
+// S_start(g + 1) = M_g S_start(g) + X_g for g = 0 .. G - 2 in fp32, per
+// (sequence, head, 32-column tile of S); S_start(0) is the initial state (zeros
+// when there is none).  Thread = (row c, 16 columns).
+__global__ void __launch_bounds__(256)
+seg_combine_kernel(const float* __restrict__ Y, const float* __restrict__ S0,
+                   float* __restrict__ S_start, int H, int dk, int dv, int G) {
+    const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
+    const int j0 = tile * kJ, tid = threadIdx.x;
+    __shared__ float cur[128][kJ + 1];
+    for (int i = tid; i < 128 * kJ; i += blockDim.x) {
+        const int c = i / kJ, j = i % kJ;
+        cur[c][j] = (S0 && c < dk) ? S0[(((size_t)n * H + h) * dk + c) * dv + j0 + j] : 0.f;
+    }
+    __syncthreads();
+    const int c = tid >> 1, jb = 16 * (tid & 1);
+    for (int g = 0; g + 1 < G; ++g) {
+        const float* Yg = Y + (((size_t)n * H + h) * (G - 1) + g) * 128 * SEG_Y_COLS;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = c < dk ? Yg[(size_t)c * SEG_Y_COLS + j0 + jb + e] : 0.f;
+        if (c < dk) {
+            const float* mrow = Yg + (size_t)c * SEG_Y_COLS + 128;
+            for (int cp = 0; cp < dk; cp += 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(mrow + cp);
+                const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[e] = fmaf(mv[u], cur[cp + u][jb + e], acc[e]);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) cur[c][jb + e] = acc[e];
+        if (c < dk) {
+            float* dst = S_start + ((((size_t)n * H + h) * (G - 1) + g) * dk + c) * dv + j0 + jb;
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        }
+        __syncthreads();
     }
 }
 
@@ -1440,16 +1734,68 @@ static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, in
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H) {
+// Chunks per segment and the segment count actually used when a fixed-length
+// batch of T tokens per sequence is split into (at most) G segments.
+static void segment_shape(int64_t T, int G, int& cps, int& G_eff) {
+    const int64_t nc = (T + tc::kC - 1) / tc::kC;
+    if (G <= 1 || nc <= 1) {
+        cps = 0x7fffffff;
+        G_eff = 1;
+        return;
+    }
+    const int64_t c = (nc + G - 1) / G;
+    cps = (int)c;
+    G_eff = (int)((nc + c - 1) / c);
+}
+
+int chunked_tc_segments_used(int64_t T, int G) {
+    int cps, Ge;
+    segment_shape(T, G, cps, Ge);
+    return Ge;
+}
+
+size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H, int64_t T_seq, int G) {
     const int64_t slots = T_total / tc::kC + n_seqs + 1;
-    return tc::WS_HEADER + (size_t)slots * H * tc::PKG_BYTES;
+    size_t bytes = tc::WS_HEADER + (size_t)slots * H * tc::PKG_BYTES;
+    const int Ge = chunked_tc_segments_used(T_seq, G);
+    if (Ge > 1) bytes += (size_t)n_seqs * H * (Ge - 1) * (tc::SEG_Y_BYTES + tc::SEG_S_BYTES);
+    return bytes;
+}
+
+// The segment count kda_chunk_prefill picks for a fixed-length batch: more
+// than one only when the plain state pass would leave most SMs idle.  A
+// segmented pass costs the chain of one segment twice (transition pass, two
+// CTAs per SM; then the final pass, one per SM), in waves, plus about two
+// chain steps per segment for the combine; the plain pass costs the whole
+// chain once.  Segments keep at least 16 chunks.
+int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sms) {
+    if (B <= 0 || T <= 0 || H <= 0) return 1;
+    const int64_t nc = (T + tc::kC - 1) / tc::kC;
+    const int64_t nx = dv / tc::kJ, nm = (dk + tc::kJ - 1) / tc::kJ;
+    const int64_t plain = (int64_t)B * H * nx;
+    if (plain * 2 > num_sms) return 1;
+    auto waves = [](int64_t n, int64_t slots) { return (n + slots - 1) / slots; };
+    int best = 1;
+    int64_t best_cost = nc * waves(plain, num_sms);
+    for (int G = 2; G <= 64; ++G) {
+        int cps, Ge;
+        segment_shape(T, G, cps, Ge);
+        if (cps < 16 || (int64_t)B * Ge > 65535) break;
+        const int64_t ab = (int64_t)B * H * (Ge - 1) * (nx + nm), d = (int64_t)B * H * Ge * nx;
+        const int64_t cost = (int64_t)cps * (waves(ab, 2 * (int64_t)num_sms) + waves(d, num_sms)) + 2 * (Ge - 1);
+        if (cost < best_cost) {
+            best = Ge;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0, float* S1,
                            const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
                            int dk, int dv, void* workspace, const CheckpointSpec& ck,
-                           cudaStream_t stream, int num_sms) {
+                           cudaStream_t stream, int num_sms, int n_segments) {
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -1462,6 +1808,9 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(tc::state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::S_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::trans_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::T_SMEM);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
@@ -1485,11 +1834,33 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         if (e != cudaSuccess) return e;
     }
     profile_event(1, stream);
-    dim3 grid_s((unsigned)(dv / tc::kJ), (unsigned)n_seqs, (unsigned)H);
+    tc::SegSpec seg;
+    int cps = 0x7fffffff, Ge = 1;
+    if (cu == nullptr) segment_shape(T, n_segments, cps, Ge);
+    if (Ge > 1) {
+        // [X | M] per (sequence, head, segment < G - 1), then the start states
+        float* Y = reinterpret_cast<float*>(ws + tc::WS_HEADER + (size_t)slots * H * tc::PKG_BYTES);
+        float* S_start = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(Y) +
+                                                  (size_t)n_seqs * H * (Ge - 1) * tc::SEG_Y_BYTES);
+        seg.G = Ge;
+        seg.cps = cps;
+        seg.S_start = S_start;
+        const int nm = (dk + tc::kJ - 1) / tc::kJ;
+        dim3 grid_t((unsigned)(dv / tc::kJ + nm), (unsigned)(n_seqs * (Ge - 1)), (unsigned)H);
+        tc::trans_pass_kernel<<<grid_t, tc::kTransThreads, tc::T_SMEM, stream>>>(ws, Y, map, H, dk, dv, seg);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dim3 grid_c((unsigned)(dv / tc::kJ), (unsigned)n_seqs, (unsigned)H);
+        tc::seg_combine_kernel<<<grid_c, 256, 0, stream>>>(Y, S0, S_start, H, dk, dv, Ge);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        profile_event(2, stream);
+    }
+    dim3 grid_s((unsigned)(dv / tc::kJ), (unsigned)(n_seqs * Ge), (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
-        ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck);
+        ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck, seg);
     e = cudaGetLastError();
-    profile_event(2, stream);
+    profile_event(Ge > 1 ? 3 : 2, stream);
     return e;
 }
 

@@ -45,11 +45,18 @@ cudaError_t run_recurrent(const void* q, const void* k, const void* v, const voi
 
 // Chunked tensor-core path (bf16, chunk 64; d_k a multiple of 16 and d_v a
 // multiple of 32, both <= 128, zero-padded to 128 on chip).
-size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H);
+// A fixed-length batch (T tokens per sequence) may be split into segments
+// for the segment-parallel state pass; G = 1 is the plain pass.  The workspace
+// covers the packages plus, for G_eff > 1, the per-segment pairs and start
+// states (T_seq is the per-sequence length, G the requested segment count).
+size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H, int64_t T_seq, int G);
+int chunked_tc_segments_used(int64_t T_seq, int G);
+int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sms);
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0,
                            float* S1, const int32_t* cu, int n_seqs, int64_t T,
                            int64_t T_total, int H, int dk, int dv, void* workspace,
-                           const CheckpointSpec& ck, cudaStream_t stream, int num_sms);
+                           const CheckpointSpec& ck, cudaStream_t stream, int num_sms,
+                           int n_segments);
 
 }  // namespace kda

@@ -121,6 +121,11 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *                  nonzero means o and the states of that call are not valid.
  * T == 0 (or every sequence empty) writes only the final states (copies of the
  * initial ones, or zeros).
+ * A fixed-length batch whose (sequence, head) chains would leave most SMs idle
+ * in the state pass (few sequences and heads, long T) is split into segments
+ * automatically (see kda_chunk_prefill_segmented); the workspace size returned
+ * by kda_chunk_prefill_workspace_size includes what that needs, and a
+ * workspace that only covers the plain pass makes the call run unsegmented.
  */
 kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const void *z,
                              const void *beta, const float *A, void *o,
@@ -128,6 +133,50 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              const int32_t *cu_seqlens, int n_seqs, int B, int64_t T, int H,
                              int d_k, int d_v, int chunk, kda_dtype dtype, void *workspace,
                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kda_chunk_prefill_segmented -- kda_chunk_prefill for a fixed-length batch
+ * with each sequence split into n_segments segments whose state passes run in
+ * parallel ("Kimi K3 architecture: how an open model with a million-token
+ * context competes with market leaders", section "GPU level: the long-context
+ * scheduler": segments of a long sequence computed on otherwise idle SMs and
+ * merged into the exact final state; the per-segment pair of transition and
+ * state-from-zero is the context-parallel pair of "How Kimi K3 is built",
+ * section "How to serve two different caches").
+ *
+ * With F_c = Diag(lam_c) - N_c the per-chunk state map S <- F_c S + X_c of the
+ * chunked form, segment g maps its start state S_g to M_g S_g + X_g
+ * (M_g = product of its F_c, X_g = its end state from zero).  The call forms
+ * every (M_g, X_g) in parallel, scans S_{g+1} = M_g S_g + X_g in fp32 from the
+ * initial state, then runs every segment from its S_g, writing o and, from the
+ * last segment, the final state.  The result equals kda_chunk_prefill up to
+ * rounding.  It pays when B * H * d_v / 32 is well below the SM count and T is
+ * long: each segment's chain is walked twice, but the segments run at once.
+ *   n_segments  >= 1; segments hold ceil(ceil(T / 64) / n_segments) chunks, so
+ *               fewer may be used (kda_chunk_prefill_auto_segments reports the
+ *               count kda_chunk_prefill picks).  1 is the plain pass.
+ *   workspace   kda_chunk_prefill_segmented_workspace_size() bytes, 256-byte
+ *               aligned; word 0 is the device status as for kda_chunk_prefill.
+ * Other arguments as for kda_chunk_prefill with cu_seqlens == NULL and
+ * n_seqs == B.  Only the tensor-core shapes (bf16, chunk 64, d_k a multiple of
+ * 16 and d_v a multiple of 32, both <= 128) are taken (KDA_ERR_UNSUPPORTED
+ * otherwise), with B * segments <= 65535.
+ */
+kda_status kda_chunk_prefill_segmented(const void *q, const void *k, const void *v, const void *z,
+                                       const void *beta, const float *A, void *o,
+                                       const float *initial_state, float *final_state, int B,
+                                       int64_t T, int H, int d_k, int d_v, int chunk,
+                                       kda_dtype dtype, int n_segments, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of kda_chunk_prefill_segmented (0 for shapes it does not take). */
+size_t kda_chunk_prefill_segmented_workspace_size(int B, int64_t T, int H, int d_k, int d_v,
+                                                  int chunk, kda_dtype dtype, int n_segments);
+
+/* The segment count kda_chunk_prefill uses for a fixed-length batch of these
+ * sizes on the current device (1: unsegmented). */
+int kda_chunk_prefill_auto_segments(int B, int64_t T, int H, int d_k, int d_v, int chunk,
+                                    kda_dtype dtype);
 
 /*
  * kda_chunk_prefill_checkpoints -- kda_chunk_prefill that also emits

@@ -93,8 +93,12 @@ def test_prefill_tc_path_requires_workspace(L):
     assert need > 0
     rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=None, ws_bytes=0)
     assert rc == WORKSPACE
+    # The automatic segment split needs more than the plain pass and falls back to it
+    # when the workspace only covers that; below the plain size the call is refused.
+    plain = L.kda_chunk_prefill_segmented_workspace_size(1, 4096, 2, 128, 128, 64, 1, 1)
+    assert 0 < plain <= need
     rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=_fake(0x100000),
-                  ws_bytes=need - 1)
+                  ws_bytes=plain - 1)
     assert rc == WORKSPACE
     rc = _prefill(L, dk=128, dv=128, chunk=64, dtype=1, T=4096, ws=_fake(0x100010),
                   ws_bytes=need)
@@ -196,3 +200,38 @@ def test_static_workspace_status_rejects_bad_pointer(L):
     assert b"NULL" in L.kda_last_error()
     assert L.kda_static_workspace_status(_fake(0x10002), None) == INVALID
     assert b"aligned" in L.kda_last_error()
+
+
+def test_segmented_rejects_bad_arguments(L):
+    f = _fake()
+    args = lambda **kw: dict(dict(B=1, T=128, H=2, dk=128, dv=128, chunk=64, dtype=1, G=2,  # noqa: E731
+                                  ws=None, ws_bytes=0), **kw)
+
+    def call(a):
+        return L.kda_chunk_prefill_segmented(f, f, f, f, f, f, f, None, None, a["B"], a["T"],
+                                             a["H"], a["dk"], a["dv"], a["chunk"], a["dtype"],
+                                             a["G"], a["ws"], a["ws_bytes"], None)
+    assert call(args(G=0)) == INVALID
+    assert call(args(dtype=0)) == UNSUPPORTED           # fp32 stays on the recurrence
+    assert call(args(chunk=16)) == UNSUPPORTED
+    assert call(args()) == WORKSPACE                    # no workspace given
+    assert L.kda_chunk_prefill_segmented_workspace_size(1, 128, 2, 128, 128, 64, 1, 0) == 0
+
+
+def test_segment_policy_and_workspace(L):
+    # The long-context workload (32 heads) keeps the plain pass; few heads are segmented.
+    assert L.kda_chunk_prefill_auto_segments(1, 65536, 32, 128, 128, 64, 1) == 1
+    assert L.kda_chunk_prefill_auto_segments(2, 4096, 8, 128, 128, 64, 1) == 1
+    assert L.kda_chunk_prefill_auto_segments(1, 65536, 8, 128, 128, 64, 1) > 1
+    assert L.kda_chunk_prefill_auto_segments(1, 65536, 1, 128, 128, 64, 1) > 1
+    assert L.kda_chunk_prefill_auto_segments(1, 65536, 8, 128, 128, 64, 0) == 1   # fp32
+    plain = L.kda_chunk_prefill_segmented_workspace_size(1, 65536, 8, 128, 128, 64, 1, 1)
+    seg = L.kda_chunk_prefill_segmented_workspace_size(1, 65536, 8, 128, 128, 64, 1, 4)
+    # four segments add three (pair, start state) records per head: 3 x 8 x (128 + 64) KiB
+    assert seg - plain == 3 * 8 * (128 + 64) * 1024
+    # segments shorter than one chunk collapse: 130 tokens make three chunks
+    assert (L.kda_chunk_prefill_segmented_workspace_size(1, 130, 1, 128, 128, 64, 1, 50)
+            == L.kda_chunk_prefill_segmented_workspace_size(1, 130, 1, 128, 128, 64, 1, 3))
+    auto = L.kda_chunk_prefill_auto_segments(1, 65536, 8, 128, 128, 64, 1)
+    assert (L.kda_chunk_prefill_workspace_size(1, 1, 65536, 8, 128, 128, 64, 1)
+            == L.kda_chunk_prefill_segmented_workspace_size(1, 65536, 8, 128, 128, 64, 1, auto))

@@ -44,8 +44,17 @@ def test_slots_stay_in_bounds():
 
 
 def test_workspace_size_query_matches_bound():
-    kda.lib()
-    for n_seqs, B, T, H in [(1, 1, 4096, 8), (2, 2, 4096, 8), (64, 1, 1048576, 16), (3, 1, 1, 1)]:
+    # Packages of the plain pass (the segment-parallel records come on top of them for
+    # fixed-length batches that kda_chunk_prefill splits into segments).
+    L = kda.lib()
+    for n_seqs, B, T, H in [(1, 1, 4096, 8), (2, 2, 4096, 8), (64, 1, 1048576, 16), (3, 1, 1, 1),
+                            (1, 1, 65536, 32)]:
         slots = (B * T) // 64 + n_seqs + 1
-        got = kda.lib().kda_chunk_prefill_workspace_size(n_seqs, B, T, H, 128, 128, 64, 1)
-        assert got == HEADER + slots * H * PKG_BYTES
+        packages = HEADER + slots * H * PKG_BYTES
+        got = L.kda_chunk_prefill_workspace_size(n_seqs, B, T, H, 128, 128, 64, 1)
+        if n_seqs != B:                       # packed: never segmented
+            assert got == packages
+            continue
+        G = L.kda_chunk_prefill_auto_segments(B, T, H, 128, 128, 64, 1)
+        assert got == packages + n_seqs * H * (G - 1) * (128 + 64) * 1024
+        assert L.kda_chunk_prefill_segmented_workspace_size(B, T, H, 128, 128, 64, 1, 1) == packages
