@@ -467,8 +467,8 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
     out["prefill_checkpoint_every_512"] = {"ms": tck, "tokens_per_s": Bp * Tp / (tck * 1e-3),
                                            "checkpoint_bytes": ck.numel() * 4}
     del ck, ws
-    # A narrower head (d_k = d_v = 64, bf16) on the tensor cores, beside the same
-    # shape on the fp32 SIMT recurrence (chunk 16 keeps it there).
+    # A narrower head (d_k = d_v = 64) on both tensor-core paths (64- and 16-token chunks),
+    # beside the fp32 SIMT recurrence on the same shape with fp32 inputs.
     from dataclasses import replace
     T64 = 16384
     w64 = replace(WORKLOADS[2], dk=64, dv=64, seed=110)
@@ -478,11 +478,21 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
     args64 = (x64["q"], x64["k"], x64["v"], x64["z"], x64["beta"], x64["A"])
     t_tc = _time_ms(lambda: kda.chunk_prefill(*args64, initial_state=x64["S0"], chunk=64,
                                               workspace=ws64), iters=5, warm=2)
-    t_rec = _time_ms(lambda: kda.chunk_prefill(*args64, initial_state=x64["S0"], chunk=16),
+    t_16 = _time_ms(lambda: kda.chunk_prefill(*args64, initial_state=x64["S0"], chunk=16),
+                    iters=5, warm=2)
+    args32 = tuple(t.float() for t in args64[:5]) + (x64["A"],)
+    t_rec = _time_ms(lambda: kda.chunk_prefill(*args32, initial_state=x64["S0"], chunk=16),
                      iters=2, warm=1)
     out[f"prefill_d64_h{w64.H}_t{T64}"] = {
         "tensor_core_ms": t_tc, "tensor_core_tokens_per_s": T64 / (t_tc * 1e-3),
-        "recurrent_ms": t_rec, "recurrent_tokens_per_s": T64 / (t_rec * 1e-3)}
+        "chunk16_tensor_core_ms": t_16, "chunk16_tensor_core_tokens_per_s": T64 / (t_16 * 1e-3),
+        "recurrent_fp32_ms": t_rec, "recurrent_fp32_tokens_per_s": T64 / (t_rec * 1e-3)}
+    del args32
+    # The long-context workload itself at chunk 16 (the 16-token tensor-core path).
+    t_long16 = _time_ms(lambda: kda.chunk_prefill(xp["q"], xp["k"], xp["v"], xp["z"], xp["beta"],
+                                                  xp["A"], initial_state=xp["S0"], chunk=16),
+                        iters=3, warm=1)
+    out["long_prefill_chunk16"] = {"ms": t_long16, "tokens_per_s": Bp * Tp / (t_long16 * 1e-3)}
     del x64, ws64
     out["segmented_prefill_t65536"] = measure_segmented(kda)
     return out
@@ -512,6 +522,9 @@ def measure_segmented(kda, T: int = 65536):
             ms = _time_ms(run, iters=5, warm=2)
             n_ev = 5 if g > 1 else 3
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for e in evs:
+                e.record()              # creates the CUDA events before the library records them
+            torch.cuda.synchronize()
             kda.set_profile_events(evs)
             run()
             kda.set_profile_events(None)

@@ -18,7 +18,7 @@ _LIB = None
 
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
-PATH_NAMES = {0: "recurrent", 1: "chunked_tc"}
+PATH_NAMES = {0: "recurrent", 1: "chunked_tc", 2: "chunk16_tc"}
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
           4: "KDA_ERR_WORKSPACE"}
 

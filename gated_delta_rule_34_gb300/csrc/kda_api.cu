@@ -67,6 +67,13 @@ bool use_chunked_tc(int dk, int dv, int chunk, kda_dtype dtype) {
            dv >= 32 && dv <= 128 && dv % 32 == 0;
 }
 
+// The 16-token tensor-core path: bf16, chunk 16, d_k and d_v multiples of 16
+// in [16, 128].
+bool use_chunk16_tc(int dk, int dv, int chunk, kda_dtype dtype) {
+    return dtype == KDA_DTYPE_BF16 && chunk == 16 && dk >= 16 && dk <= 128 && dk % 16 == 0 &&
+           dv >= 16 && dv <= 128 && dv % 16 == 0;
+}
+
 }  // namespace
 
 namespace kda {
@@ -121,7 +128,9 @@ kda_status kda_gate(const void* z, const float* A, float* g, int64_t n_tokens, i
 }
 
 kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype dtype) {
-    return use_chunked_tc(d_k, d_v, chunk, dtype) ? KDA_PATH_CHUNKED_TC : KDA_PATH_RECURRENT;
+    if (use_chunked_tc(d_k, d_v, chunk, dtype)) return KDA_PATH_CHUNKED_TC;
+    if (use_chunk16_tc(d_k, d_v, chunk, dtype)) return KDA_PATH_CHUNK16_TC;
+    return KDA_PATH_RECURRENT;
 }
 
 // Segment count for kda_chunk_prefill: automatic for fixed-length batches on
@@ -140,6 +149,7 @@ static size_t tc_workspace(int n_seqs, int B, int64_t T, int H, int G) {
 size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int d_k, int d_v,
                                         int chunk, kda_dtype dtype) {
     if (n_seqs <= 0 || B <= 0 || T < 0 || H <= 0) return 0;
+    if (use_chunk16_tc(d_k, d_v, chunk, dtype)) return kda::CHUNK16_WORKSPACE_BYTES;
     if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
     return tc_workspace(n_seqs, B, T, H, auto_segments(n_seqs, B, T, H, d_k, d_v));
 }
@@ -229,6 +239,18 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
                                                d_k, d_v, workspace, ck, stream, device_sm_count(),
                                                G),
                            "kda_chunk_prefill (chunked tensor-core path)");
+    }
+    if (use_chunk16_tc(d_k, d_v, chunk, dtype)) {
+        if (workspace == nullptr || workspace_bytes < kda::CHUNK16_WORKSPACE_BYTES)
+            return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu at %p",
+                        kda::CHUNK16_WORKSPACE_BYTES, workspace_bytes, workspace);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+        if (n_segments > 1) return fail(KDA_ERR_UNSUPPORTED, "segments run on the 64-token path only");
+        return cuda_status(kda::run_chunk16_tc(q, k, v, z, beta, A, o, initial_state, final_state,
+                                               cu_seqlens, n_seqs, T, T_total, H, d_k, d_v,
+                                               workspace, ck, stream),
+                           "kda_chunk_prefill (16-token tensor-core path)");
     }
     kda::profile_event(0, stream);
     const cudaError_t e = kda::run_recurrent(q, k, v, z, beta, A, o, initial_state, final_state,

@@ -1,0 +1,483 @@
+// kda_chunk16_tc.cu -- chunked KDA prefill with 16-token chunks on the sm_103a
+// tensor cores (bf16 inputs; d_k and d_v multiples of 16, at most 128).
+//
+// The chunked form over 16-token chunks: inside a chunk the tokens are handled
+// together by tensor-core products, and the state is passed from chunk to
+// chunk ("Kimi K3 architecture: how an open model with a million-token context
+// competes with market leaders", section "Chip level: the specialised FlashKDA
+// kernel").  With g_min = -5 ("How Kimi K3 is built: 2.8 trillion parameters,
+// linear attention and agents for a million tokens", section "Sequence: three
+// KDA to one global MLA") the log-decay across 16 tokens spans at most 80, so
+// e^{+-L} fits in fp32 and bf16 and every causal block is one dense product:
+// there is no separate path for the diagonal.
+//
+// Per (sequence, head) and chunk of C <= 16 tokens, with L_t = running sum of
+// g from the chunk start (L_t in [-80, 0]), E_t = e^{L_t}, lam = e^{L_{C-1}},
+// the start state S and beta already folded where written:
+//   A_ts = b_t sum_c k_tc E_tc k_sc / E_sc  (s < t)     T = (I + A)^{-1}
+//   P_ts =     sum_c q_tc E_tc k_sc / E_sc  (s <= t)
+//   W = T Diag(b) (k E),  U~ = T Diag(b) V,  U = U~ - W S
+//   O = (q E) S + P U,    S <- Diag(lam) S + (k lam / E)^T U
+// which is the recurrence unrolled over the chunk (the same algebra as the
+// 64-token path, without its cross-block factoring).
+//
+// One CTA of eight warps per (sequence, head) walks the chunks in order.  All
+// products are arranged so that TMEM lane = state column j (or channel c), so
+// the fp32 state lives in registers as S^T[j][c] (thread = lane j, one half of
+// the channels per warp group) and its bf16 copy is written row by row:
+//   A/P    D[t][s]   = [kE ; qE] (k/E)^T           M=64  N=16  K=128
+//   W^T    D[c][t]   = (b kE)^T T^T                M=128 N=16  K=16   (A MN-major)
+//   U~^T   D[j][t]   = (b V)^T T^T                 M=128 N=16  K=16   (A MN-major)
+//   S^T W^T, S^T (qE)^T  D[j][t] = S^T [W ; qE]^T  M=128 N=32  K=128
+//   O^T   += U^T P^T                               M=128 N=16  K=16
+//   D[j][c] = U^T (k lam / E)                      M=128 N=128 K=16   (B MN-major)
+// and the fp32 update S^T <- S^T Diag(lam) + D on the registers.  The chunk
+// needs no workspace beyond the status word; two CTAs share an SM.
+#include <cuda_bf16.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "tc_util.cuh"
+
+namespace kda {
+namespace c16 {
+
+using namespace tc;
+
+constexpr int kC = 16;
+constexpr int kThreads = 256;
+
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr uint32_t R_ST = 0;          // S^T bf16 [128 j][128 c]: two K-blocks of 16 KB, swizzled
+constexpr uint32_t R_UT = 32768;      // U^T bf16 [128 j][16 t] (128-byte rows, K = 16 used)
+constexpr uint32_t R_APA = 49152;     // [kE ; qE ; 0] [64 rows][128 c]: two K-blocks of 8 KB
+constexpr uint32_t R_APB = 65536;     // k/E [16 s][128 c]: two K-blocks of 2 KB
+constexpr uint32_t R_SB = 69632;      // [W ; qE] [32 rows][128 c]: two K-blocks of 4 KB
+constexpr uint32_t R_BKG = 77824;     // b kE token rows, two 64-channel halves of 2 KB (MN-major)
+constexpr uint32_t R_BV = 81920;      // b V token rows, same layout
+constexpr uint32_t R_KC = 86016;      // k lam / E token rows, same layout
+constexpr uint32_t R_PB = 90112;      // P [16 t][16 s] (128-byte rows)
+constexpr uint32_t R_TB = 92160;      // T [16 t][16 s] (128-byte rows)
+constexpr uint32_t R_GS = 94208;      // g, then L: fp32 [16 t][128 c]
+constexpr uint32_t R_AF = 102400;     // A fp32 [16][17]
+constexpr uint32_t R_LAM = 103680;    // lam [128] fp32
+constexpr uint32_t R_EA = 104192;     // e^{A_h} [128] fp32
+constexpr uint32_t R_BETA = 104704;   // beta [16] fp32
+constexpr uint32_t R_BAR = 104768;    // mbarrier, TMEM slot
+constexpr uint32_t SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
+static_assert(SMEM * 2 <= 232448, "two CTAs per SM");
+
+// TMEM columns
+constexpr uint32_t T_AP = 0;      // A/P (M=64 layout: row r in lane 32 (r / 16) + r mod 16)
+constexpr uint32_t T_WT = 16;     // W^T
+constexpr uint32_t T_UT = 32;     // U~^T
+constexpr uint32_t T_ST = 64;     // [(W S)^T | O^T]
+constexpr uint32_t T_SU = 128;    // U^T (k lam / E)
+constexpr uint32_t kTmemCols = 256;
+
+constexpr uint32_t kErrWait = 8u;   // status bit: a bounded wait gave up
+
+__device__ __forceinline__ uint32_t idesc_bmn(uint32_t M, uint32_t N) {
+    return idesc_bf16(M, N) | (1u << 16);   // B MN-major
+}
+
+// Waits (bounded) for the next phase of `bar` and makes the whole CTA agree on
+// the outcome.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
+    const bool ok = mbar_wait(bar, phase);
+    phase ^= 1u;
+    tc_fence_after();
+    return __syncthreads_and(ok) != 0;
+}
+
+// Stores 8 bf16 values (channels 8 c8 .. 8 c8 + 7) as token row t of a [rows][128]
+// K-major operand split in two 64-channel K-blocks `kb_bytes` apart.
+__device__ __forceinline__ void store_row8(uint8_t* base, uint32_t kb_bytes, int row, int c8,
+                                           const float (&f)[8]) {
+    uint4 r;
+    r.x = pack_bf16x2(f[0], f[1]);
+    r.y = pack_bf16x2(f[2], f[3]);
+    r.z = pack_bf16x2(f[4], f[5]);
+    r.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(base + (c8 >> 3) * kb_bytes + sw128(row, c8 & 7)) = r;
+}
+
+__device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&raw);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(b[e]);
+}
+
+// 8 bf16 of row `row` of a [T_total][H][d] tensor, channels 8 c8 .. (zeros past d).
+__device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int64_t row, int H, int h,
+                                       int d, int c8) {
+    if (8 * c8 >= d) return make_uint4(0, 0, 0, 0);
+    return __ldg(reinterpret_cast<const uint4*>(x + ((size_t)row * H + h) * d + 8 * c8));
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+               const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
+               const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
+               __nv_bfloat16* __restrict__ o, const float* __restrict__ S0, float* __restrict__ S1,
+               const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H, int dk, int dv,
+               uint32_t* __restrict__ status, CheckpointSpec ck) {
+    const int n = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float* gs = reinterpret_cast<float*>(sm + R_GS);
+    float* af = reinterpret_cast<float*>(sm + R_AF);
+    float* lam = reinterpret_cast<float*>(sm + R_LAM);
+    float* ea = reinterpret_cast<float*>(sm + R_EA);
+    float* bs = reinterpret_cast<float*>(sm + R_BETA);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 8);
+
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_len, T_total, bos, eos);
+    const int64_t len_seq = eos - bos;
+
+    // Thread roles.  Row-side phases: token t = tid / 16, channels 8 c8 .. + 7.
+    // State phases: lane j = 32 (warp mod 4) + lane, channel half ch = warp / 4.
+    const int tt = tid >> 4, c8 = tid & 15;
+    const int j = 32 * (warp & 3) + lane, ch = warp >> 2;
+    const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;   // TMEM lane field of this warp
+
+    if (warp == 0) tmem_alloc<kTmemCols>(tslot);
+    if (tid == 32) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    // Rows 32..63 of the A/P operand stay zero; e^A of the head.
+    for (int i = tid; i < 4096; i += kThreads)
+        reinterpret_cast<uint32_t*>(sm + R_APA)[i] = 0u;
+    if (tid < 128) ea[tid] = tid < dk ? __expf(A[(size_t)h * dk + tid]) : 0.f;
+
+    // S^T[j][64 ch .. 64 ch + 63] in fp32 registers.
+    const size_t smat = ((size_t)n * H + h) * dk * dv;
+    float st[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+        const int c = 64 * ch + e;
+        st[e] = (S0 && c < dk && j < dv) ? __ldg(S0 + smat + (size_t)c * dv + j) : 0.f;
+    }
+    auto write_st = [&]() {
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            uint4 r;
+            r.x = pack_bf16x2(st[8 * q8 + 0], st[8 * q8 + 1]);
+            r.y = pack_bf16x2(st[8 * q8 + 2], st[8 * q8 + 3]);
+            r.z = pack_bf16x2(st[8 * q8 + 4], st[8 * q8 + 5]);
+            r.w = pack_bf16x2(st[8 * q8 + 6], st[8 * q8 + 7]);
+            *reinterpret_cast<uint4*>(sm + R_ST + ch * 16384 + sw128(j, q8)) = r;
+        }
+    };
+    auto store_state = [&](float* mat) {      // mat: [d_k][d_v] of (n, h)
+        if (j < dv) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+                const int c = 64 * ch + e;
+                if (c < dk) mat[(size_t)c * dv + j] = st[e];
+            }
+        }
+    };
+    write_st();
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    uint32_t phase = 0;
+    bool ok = true;
+
+    const int nchunks = (int)((len_seq + kC - 1) / kC);
+    for (int ci = 0; ci < nchunks && ok; ++ci) {
+        const int64_t t0 = bos + (int64_t)ci * kC;
+        const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
+        const bool live = tt < len;
+
+        // ---- inputs of token tt, channels 8 c8 .. 8 c8 + 7; gate -> gs
+        uint4 kr = make_uint4(0, 0, 0, 0), qr = kr, vr = kr, zr = kr;
+        if (live) {
+            kr = load8(k, t0 + tt, H, h, dk, c8);
+            qr = load8(q, t0 + tt, H, h, dk, c8);
+            vr = load8(v, t0 + tt, H, h, dv, c8);
+            zr = load8(z, t0 + tt, H, h, dk, c8);
+        }
+        if (tid < kC)
+            bs[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+        {
+            float zf[8], g[8];
+            unpack8(zr, zf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = 8 * c8 + e;
+                g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+            }
+            float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
+            gp[0] = make_float4(g[0], g[1], g[2], g[3]);
+            gp[1] = make_float4(g[4], g[5], g[6], g[7]);
+        }
+        __syncthreads();
+        // ---- L = running sum over the chunk, per channel; lam = e^{L_last}
+        if (tid < 128) {
+            float run = 0.f;
+#pragma unroll
+            for (int t = 0; t < kC; ++t) {
+                run += gs[t * 128 + tid];
+                gs[t * 128 + tid] = run;
+            }
+            lam[tid] = __expf(run);
+        }
+        __syncthreads();
+
+        // ---- decay-scaled operands of token tt (bf16)
+        {
+            float kf[8], qf[8], vf[8], E[8], R[8], o8[8];
+            unpack8(kr, kf);
+            unpack8(qr, qf);
+            unpack8(vr, vf);
+            const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
+            const float4 l0 = lp[0], l1 = lp[1];
+            const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                E[e] = __expf(L[e]);
+                R[e] = __fdividef(1.0f, E[e]);
+            }
+            const float bt = bs[tt];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+            store_row8(sm + R_APA, 8192, tt, c8, o8);                           // k E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
+            store_row8(sm + R_BKG, 2048, tt, c8, o8);                           // b k E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+            store_row8(sm + R_APA, 8192, 16 + tt, c8, o8);                      // q E
+            store_row8(sm + R_SB, 4096, 16 + tt, c8, o8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * R[e];
+            store_row8(sm + R_APB, 2048, tt, c8, o8);                           // k / E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = o8[e] * lam[8 * c8 + e];
+            store_row8(sm + R_KC, 2048, tt, c8, o8);                            // k lam / E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
+            store_row8(sm + R_BV, 2048, tt, c8, o8);                            // b V
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- A and P: D[t][s] = [kE ; qE] (k/E)^T, M=64 N=16 K=128
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(64, 16);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + R_APA + kb * 8192 + off)),
+                         desc_sw128(smem_u32(sm + R_APB + kb * 2048 + off)), idesc, ks > 0);
+            }
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        // rows 0..15 (A, lanes 0..15 of warp 0), rows 16..31 (P, lanes 32..47 of warp 1)
+        if (warp < 2) {
+            float d[16];
+            tmem_ld16(tbase + tl + T_AP, d);
+            tmem_wait_ld();
+            if (lane < kC) {
+                const int t = lane;
+                if (warp == 0) {
+                    const float bt = bs[t];
+#pragma unroll
+                    for (int s = 0; s < kC; ++s) af[t * 17 + s] = s < t ? bt * d[s] : 0.f;
+                } else {
+                    float p8[8];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
+                        uint4 r;
+                        r.x = pack_bf16x2(p8[0], p8[1]);
+                        r.y = pack_bf16x2(p8[2], p8[3]);
+                        r.z = pack_bf16x2(p8[4], p8[5]);
+                        r.w = pack_bf16x2(p8[6], p8[7]);
+                        *reinterpret_cast<uint4*>(sm + R_PB + sw128(t, hh)) = r;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- T = (I + A)^{-1}: column jc by forward substitution (16 threads)
+        if (tid < kC) {
+            const int jc = tid;
+            float x[kC];
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
+                x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+            }
+            // T[r][jc] -> row r, element jc of the K-major [t][s] operand
+#pragma unroll
+            for (int r = 0; r < kC; ++r)
+                *reinterpret_cast<__nv_bfloat16*>(sm + R_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
+                    __float2bfloat16_rn(x[r]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- W^T = (b kE)^T T^T and U~^T = (b V)^T T^T (M=128 N=16 K=16, A MN-major)
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16_amn(128, 16);
+            const uint64_t tb = desc_sw128(smem_u32(sm + R_TB));
+            mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + R_BKG), 2048, 1024), tb, idesc, false);
+            mma_bf16(tbase + T_UT, desc_sw128_mn(smem_u32(sm + R_BV), 2048, 1024), tb, idesc, false);
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        // W rows t of the [W ; qE] operand: lane c of warps 0..3 writes column c
+        if (warp < 4) {
+            float w[16];
+            tmem_ld16(tbase + tl + T_WT, w);
+            tmem_wait_ld();
+            const int c = j;
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                *reinterpret_cast<__nv_bfloat16*>(sm + R_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
+                                                   (c & 7) * 2) = __float2bfloat16_rn(w[t]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T, M=128 N=32 K=128
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 32);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + R_ST + kb * 16384 + off)),
+                         desc_sw128(smem_u32(sm + R_SB + kb * 4096 + off)), idesc, ks > 0);
+            }
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        // U^T[j][s] = U~^T[j][s] - (W S)^T[j][s] -> bf16 row j
+        if (warp < 4) {
+            float ws_[16], ut[16];
+            tmem_ld16(tbase + tl + T_ST, ws_);
+            tmem_ld16(tbase + tl + T_UT, ut);
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint4 r;
+                r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
+                r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
+                r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
+                r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
+                *reinterpret_cast<uint4*>(sm + R_UT + sw128(j, hh)) = r;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- O^T += U^T P^T (M=128 N=16 K=16); D = U^T (k lam / E) (M=128 N=128 K=16, B MN-major)
+        if (tid == 0) {
+            const uint64_t ua = desc_sw128(smem_u32(sm + R_UT));
+            mma_bf16(tbase + T_ST + 16, ua, desc_sw128(smem_u32(sm + R_PB)), idesc_bf16(128, 16), true);
+            mma_bf16(tbase + T_SU, ua, desc_sw128_mn(smem_u32(sm + R_KC), 2048, 1024), idesc_bmn(128, 128),
+                     false);
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+
+        // ---- outputs o[t0 + t][h][j] = O^T[j][t] (warps 0..3)
+        if (warp < 4 && j < dv) {
+            float ov[16];
+            tmem_ld16(tbase + tl + T_ST + 16, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                if (t < len) o[((size_t)(t0 + t) * H + h) * dv + j] = __float2bfloat16_rn(ov[t]);
+        }
+        // ---- S^T <- S^T Diag(lam) + D, then its bf16 copy
+#pragma unroll
+        for (int q16 = 0; q16 < 4; ++q16) {
+            float d[16];
+            tmem_ld16(tbase + tl + T_SU + 64 * ch + 16 * q16, d);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int idx = 16 * q16 + e;
+                st[idx] = fmaf(lam[64 * ch + idx], st[idx], d[e]);
+            }
+        }
+        write_st();
+        if (ck.out) {
+            const int64_t done = (int64_t)(ci + 1) * kC;
+            if (done <= len_seq && done % ck.every == 0 && done / ck.every <= ck.max_count)
+                store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!ok && tid == 0) atomicOr(status, kErrWait);
+    if (S1) store_state(S1 + smat);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<kTmemCols>(tbase);
+    }
+}
+
+}  // namespace c16
+
+cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const void* z,
+                           const void* beta, const float* A, void* o, const float* S0, float* S1,
+                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
+                           int dk, int dv, void* workspace, const CheckpointSpec& ck,
+                           cudaStream_t stream) {
+    constexpr int kMaxDevices = 64;
+    static bool attr_done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+        e = cudaFuncSetAttribute(c16::chunk16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)c16::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    e = cudaMemsetAsync(status, 0, CHUNK16_WORKSPACE_BYTES, stream);
+    if (e != cudaSuccess) return e;
+    using bf = __nv_bfloat16;
+    profile_event(0, stream);
+    dim3 grid((unsigned)n_seqs, (unsigned)H);
+    c16::chunk16_kernel<<<grid, c16::kThreads, c16::SMEM, stream>>>(
+        static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
+        static_cast<const bf*>(z), static_cast<const bf*>(beta), A, static_cast<bf*>(o), S0, S1, cu, T,
+        T_total, H, dk, dv, status, ck);
+    e = cudaGetLastError();
+    profile_event(1, stream);
+    return e;
+}
+
+}  // namespace kda

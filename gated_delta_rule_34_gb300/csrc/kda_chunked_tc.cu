@@ -1657,46 +1657,56 @@ trans_pass_kernel(uint8_t* __restrict__ ws, float* __restrict__ Y_out, SeqMap ma
 }
 
 // S_start(g + 1) = M_g S_start(g) + X_g for g = 0 .. G - 2 in fp32, per
-// (sequence, head, 32-column tile of S); S_start(0) is the initial state (zeros
-// when there is none).  Thread = (row c, 16 columns).
+// (sequence, head, 8-column tile of S); S_start(0) is the initial state (zeros
+// when there is none).  Each step stages M_g in shared memory (row pitch 132
+// floats) and every thread forms one row c times four columns.
+constexpr int kCombCols = 8;
+constexpr int kMPitch = 132;
+constexpr uint32_t COMB_SMEM = (128 * kMPitch + 128 * kCombCols) * 4;
+
 __global__ void __launch_bounds__(256)
 seg_combine_kernel(const float* __restrict__ Y, const float* __restrict__ S0,
                    float* __restrict__ S_start, int H, int dk, int dv, int G) {
-    const int tile = blockIdx.x, n = blockIdx.y, h = blockIdx.z;
-    const int j0 = tile * kJ, tid = threadIdx.x;
-    __shared__ float cur[128][kJ + 1];
-    for (int i = tid; i < 128 * kJ; i += blockDim.x) {
-        const int c = i / kJ, j = i % kJ;
-        cur[c][j] = (S0 && c < dk) ? S0[(((size_t)n * H + h) * dk + c) * dv + j0 + j] : 0.f;
-    }
-    __syncthreads();
-    const int c = tid >> 1, jb = 16 * (tid & 1);
+    const int j0 = blockIdx.x * kCombCols, n = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
+    extern __shared__ float comb_smem[];
+    float* Ms = comb_smem;                        // M_g [128][kMPitch]
+    float* cur = comb_smem + 128 * kMPitch;       // S_start(g) [128][8]
+    const int c = tid >> 1, jq = 4 * (tid & 1);
+    const bool row_ok = c < dk;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (S0 && row_ok)
+        s = *reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * dk + c) * dv + j0 + jq);
+    *reinterpret_cast<float4*>(cur + c * kCombCols + jq) = s;
     for (int g = 0; g + 1 < G; ++g) {
         const float* Yg = Y + (((size_t)n * H + h) * (G - 1) + g) * 128 * SEG_Y_COLS;
-        float acc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = c < dk ? Yg[(size_t)c * SEG_Y_COLS + j0 + jb + e] : 0.f;
-        if (c < dk) {
-            const float* mrow = Yg + (size_t)c * SEG_Y_COLS + 128;
+        for (int i = tid; i < 128 * 32; i += 256) {
+            const int row = i >> 5, c4 = i & 31;
+            if (row < dk && 4 * c4 < dk)
+                *reinterpret_cast<float4*>(Ms + row * kMPitch + 4 * c4) =
+                    *reinterpret_cast<const float4*>(Yg + (size_t)row * SEG_Y_COLS + 128 + 4 * c4);
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row_ok) acc = *reinterpret_cast<const float4*>(Yg + (size_t)c * SEG_Y_COLS + j0 + jq);
+        __syncthreads();                          // M_g and S_start(g) in place
+        if (row_ok) {
+            const float* mrow = Ms + c * kMPitch;
             for (int cp = 0; cp < dk; cp += 4) {
-                const float4 m4 = *reinterpret_cast<const float4*>(mrow + cp);
-                const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[e] = fmaf(mv[u], cur[cp + u][jb + e], acc[e]);
+                for (int u = 0; u < 4; ++u) {
+                    const float m = mrow[cp + u];
+                    const float4 x = *reinterpret_cast<const float4*>(cur + (cp + u) * kCombCols + jq);
+                    acc.x = fmaf(m, x.x, acc.x);
+                    acc.y = fmaf(m, x.y, acc.y);
+                    acc.z = fmaf(m, x.z, acc.z);
+                    acc.w = fmaf(m, x.w, acc.w);
+                }
             }
         }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) cur[c][jb + e] = acc[e];
-        if (c < dk) {
-            float* dst = S_start + ((((size_t)n * H + h) * (G - 1) + g) * dk + c) * dv + j0 + jb;
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        }
-        __syncthreads();
+        __syncthreads();                          // every read of M_g and S_start(g) done
+        *reinterpret_cast<float4*>(cur + c * kCombCols + jq) = acc;
+        if (row_ok)
+            *reinterpret_cast<float4*>(S_start + ((((size_t)n * H + h) * (G - 1) + g) * dk + c) * dv +
+                                       j0 + jq) = acc;
     }
 }
 
@@ -1763,11 +1773,13 @@ size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H, int64_t T_
 }
 
 // The segment count kda_chunk_prefill picks for a fixed-length batch: more
-// than one only when the plain state pass would leave most SMs idle.  A
-// segmented pass costs the chain of one segment twice (transition pass, two
-// CTAs per SM; then the final pass, one per SM), in waves, plus about two
-// chain steps per segment for the combine; the plain pass costs the whole
-// chain once.  Segments keep at least 16 chunks.
+// than one only when the plain state pass would leave most SMs idle.  Costs in
+// chain steps of the plain pass (measured on the long-context shapes): the
+// plain pass walks the whole chain once; a segmented one walks a segment's
+// chain in the transition pass (two CTAs per SM, each step about 1.5 times
+// slower than a plain step), then in the final pass (one CTA per SM), in waves,
+// plus about two steps per segment for the sequential combine.  Segments keep
+// at least 16 chunks.
 int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sms) {
     if (B <= 0 || T <= 0 || H <= 0) return 1;
     const int64_t nc = (T + tc::kC - 1) / tc::kC;
@@ -1782,7 +1794,8 @@ int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sm
         segment_shape(T, G, cps, Ge);
         if (cps < 16 || (int64_t)B * Ge > 65535) break;
         const int64_t ab = (int64_t)B * H * (Ge - 1) * (nx + nm), d = (int64_t)B * H * Ge * nx;
-        const int64_t cost = (int64_t)cps * (waves(ab, 2 * (int64_t)num_sms) + waves(d, num_sms)) + 2 * (Ge - 1);
+        const int64_t cost = (int64_t)cps * (3 * waves(ab, 2 * (int64_t)num_sms) + 2 * waves(d, num_sms)) / 2 +
+                             2 * (Ge - 1);
         if (cost < best_cost) {
             best = Ge;
             best_cost = cost;
@@ -1811,6 +1824,9 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(tc::trans_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)tc::T_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::COMB_SMEM);
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
@@ -1850,17 +1866,18 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         tc::trans_pass_kernel<<<grid_t, tc::kTransThreads, tc::T_SMEM, stream>>>(ws, Y, map, H, dk, dv, seg);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        dim3 grid_c((unsigned)(dv / tc::kJ), (unsigned)n_seqs, (unsigned)H);
-        tc::seg_combine_kernel<<<grid_c, 256, 0, stream>>>(Y, S0, S_start, H, dk, dv, Ge);
+        profile_event(2, stream);
+        dim3 grid_c((unsigned)(dv / tc::kCombCols), (unsigned)n_seqs, (unsigned)H);
+        tc::seg_combine_kernel<<<grid_c, 256, tc::COMB_SMEM, stream>>>(Y, S0, S_start, H, dk, dv, Ge);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        profile_event(2, stream);
+        profile_event(3, stream);
     }
     dim3 grid_s((unsigned)(dv / tc::kJ), (unsigned)(n_seqs * Ge), (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
         ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck, seg);
     e = cudaGetLastError();
-    profile_event(Ge > 1 ? 3 : 2, stream);
+    profile_event(Ge > 1 ? 4 : 2, stream);
     return e;
 }
 

@@ -59,4 +59,14 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
                            const CheckpointSpec& ck, cudaStream_t stream, int num_sms,
                            int n_segments);
 
+// Chunked tensor-core path with 16-token chunks (bf16; d_k and d_v multiples
+// of 16, at most 128): one fused kernel per (sequence, head), no package
+// workspace; the workspace holds only the device status word.
+constexpr size_t CHUNK16_WORKSPACE_BYTES = 1024;
+cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const void* z,
+                           const void* beta, const float* A, void* o, const float* S0, float* S1,
+                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
+                           int dk, int dv, void* workspace, const CheckpointSpec& ck,
+                           cudaStream_t stream);
+
 }  // namespace kda

@@ -62,9 +62,12 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 /* Which kernels kda_chunk_prefill runs for a given shape. */
 typedef enum {
     KDA_PATH_RECURRENT = 0,    /* SIMT fp32, token by token, any d_k, d_v <= 128     */
-    KDA_PATH_CHUNKED_TC = 1    /* chunked WY/UT form on tcgen05: bf16, chunk 64,
+    KDA_PATH_CHUNKED_TC = 1,   /* chunked WY/UT form on tcgen05: bf16, chunk 64,
                                   d_k a multiple of 16 and d_v a multiple of 32,
                                   both <= 128 (zero-padded to 128 on chip)      */
+    KDA_PATH_CHUNK16_TC = 2    /* the same form over 16-token chunks, one fused
+                                  tcgen05 kernel per (sequence, head): bf16,
+                                  chunk 16, d_k and d_v multiples of 16, <= 128 */
 } kda_prefill_path;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -106,10 +109,13 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *   o              [B, T, H, d_v] in `dtype` (written).
  *   chunk          16 or 64 (the exact result does not depend on it).
  *                  bf16 with chunk 64, d_k a multiple of 16 and d_v a multiple
- *                  of 32 (both <= 128) runs on the tensor cores
- *                  (kda_chunk_prefill_path says which path a shape takes);
- *                  everything else on the fp32 SIMT recurrence.  The
- *                  tensor-core path takes fewer than 2^31 tokens in all
+ *                  of 32 (both <= 128) runs on the 64-token tensor-core path;
+ *                  bf16 with chunk 16, d_k and d_v multiples of 16 (<= 128)
+ *                  on the 16-token tensor-core path (one fused kernel per
+ *                  (sequence, head), the state handed on every 16 tokens);
+ *                  everything else on the fp32 SIMT recurrence
+ *                  (kda_chunk_prefill_path says which path a shape takes).  The
+ *                  64-token path takes fewer than 2^31 tokens in all
  *                  (KDA_ERR_UNSUPPORTED otherwise).
  *   workspace      device scratch of at least kda_chunk_prefill_workspace_size()
  *                  bytes (may be NULL when that size is 0); 256-byte aligned;

@@ -120,7 +120,12 @@ def test_workspace_size_query(L):
 def test_path_query(L):
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(16, 16, 16, 0)] == "recurrent"
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 64, 0)] == "recurrent"   # fp32
-    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 16, 1)] == "recurrent"   # chunk 16
+    # chunk 16, bf16: the 16-token tensor-core path (d_k, d_v multiples of 16)
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 16, 1)] == "chunk16_tc"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(48, 16, 16, 1)] == "chunk16_tc"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(40, 64, 16, 1)] == "recurrent"
+    assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 16, 0)] == "recurrent"   # fp32
+    assert L.kda_chunk_prefill_workspace_size(1, 1, 4096, 8, 128, 128, 16, 1) == 1024
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(128, 128, 64, 1)] == "chunked_tc"
     # narrower bf16 heads: d_k a multiple of 16, d_v a multiple of 32
     assert api.PATH_NAMES[L.kda_chunk_prefill_path(64, 64, 64, 1)] == "chunked_tc"

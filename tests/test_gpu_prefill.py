@@ -120,7 +120,7 @@ def test_output_buffer_canaries():
 # ----------------------------------------------------------- tensor-core path
 def test_tensor_core_path_is_selected():
     assert kda.prefill_path(128, 128, 64, torch.bfloat16) == "chunked_tc"
-    assert kda.prefill_path(128, 128, 16, torch.bfloat16) == "recurrent"
+    assert kda.prefill_path(128, 128, 16, torch.bfloat16) == "chunk16_tc"
     assert kda.prefill_path(128, 128, 64, torch.float32) == "recurrent"
 
 
@@ -165,7 +165,7 @@ def test_tensor_core_zero_and_pure_decay_inputs():
     assert_parity(S, rS, torch.bfloat16, "beta=0 state")
 
 
-def _full_check(x, what, heads_per_batch):
+def _full_check(x, what, heads_per_batch, chunk=64):
     """Compares every (sequence, head) of one GPU call with the oracle, element by element.
 
     The oracle runs on batches of heads (every sequence of those heads at once), so that
@@ -173,7 +173,7 @@ def _full_check(x, what, heads_per_batch):
     state (max |gpu - oracle| over max |oracle| of the tensor); the worst single (sequence,
     head) pair, measured against its own maximum, is reported beside it.
     """
-    o, S, status = _run_with_status(x)
+    o, S, status = _run_with_status(x, chunk)
     assert status == 0
     q = x["q"]
     B, T, H = q.shape[:3]
