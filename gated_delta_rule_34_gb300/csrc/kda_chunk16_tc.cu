@@ -404,14 +404,17 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         }
         if (!(ok = cta_wait(bar, phase))) break;
 
-        // ---- outputs o[t0 + t][h][j] = O^T[j][t] (warps 0..3)
-        if (warp < 4 && j < dv) {
+        // ---- outputs o[t0 + t][h][j] = O^T[j][t] (warps 0..3; the TMEM load is
+        //      warp-collective, so every lane takes it and only the stores are masked)
+        if (warp < 4) {
             float ov[16];
             tmem_ld16(tbase + tl + T_ST + 16, ov);
             tmem_wait_ld();
+            if (j < dv) {
 #pragma unroll
-            for (int t = 0; t < kC; ++t)
-                if (t < len) o[((size_t)(t0 + t) * H + h) * dv + j] = __float2bfloat16_rn(ov[t]);
+                for (int t = 0; t < kC; ++t)
+                    if (t < len) o[((size_t)(t0 + t) * H + h) * dv + j] = __float2bfloat16_rn(ov[t]);
+            }
         }
         // ---- S^T <- S^T Diag(lam) + D, then its bf16 copy
 #pragma unroll
