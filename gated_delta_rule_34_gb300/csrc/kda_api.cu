@@ -133,17 +133,27 @@ kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype d
     return KDA_PATH_RECURRENT;
 }
 
+// Tokens of one window of the 64-token path (see kda::kWindowTokens).
+static int64_t window_span(int64_t T) { return T < kda::kWindowTokens ? T : kda::kWindowTokens; }
+
 // Segment count for kda_chunk_prefill: automatic for fixed-length batches on
 // the tensor-core path (n_seqs == B marks a fixed-length query), 1 otherwise.
 static int auto_segments(int n_seqs, int B, int64_t T, int H, int d_k, int d_v) {
     if (n_seqs != B) return 1;
-    return kda::chunked_tc_auto_segments(B, T, H, d_k, d_v, device_sm_count());
+    return kda::chunked_tc_auto_segments(B, window_span(T), H, d_k, d_v, device_sm_count());
 }
 
-static size_t tc_workspace(int n_seqs, int B, int64_t T, int H, int G) {
-    // T is the per-sequence length of a fixed-length batch, or the packed total
-    // with B = 1 (then G is 1).
-    return kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * T, H, T, G);
+// Workspace of the 64-token path for a fixed-length batch (`fixed`: B sequences
+// of T tokens) or a packed one (T tokens in all): one window's packages, the
+// segment records (fixed length only) and, when the call runs in several
+// windows, a carry area for the states between them (at the end).
+static size_t carry_bytes(int n_seqs, int H) { return (size_t)n_seqs * H * 128 * 128 * 4; }
+static size_t tc_workspace(bool fixed, int n_seqs, int B, int64_t T, int H, int G) {
+    const int64_t w = window_span(T);
+    size_t bytes = fixed ? kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * w, H, w, G)
+                         : kda::chunked_tc_workspace_bytes(n_seqs, w, H, w, 1);
+    if (T > kda::kWindowTokens) bytes += carry_bytes(n_seqs, H);
+    return bytes;
 }
 
 size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int d_k, int d_v,
@@ -151,20 +161,25 @@ size_t kda_chunk_prefill_workspace_size(int n_seqs, int B, int64_t T, int H, int
     if (n_seqs <= 0 || B <= 0 || T < 0 || H <= 0) return 0;
     if (use_chunk16_tc(d_k, d_v, chunk, dtype)) return kda::CHUNK16_WORKSPACE_BYTES;
     if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
-    return tc_workspace(n_seqs, B, T, H, auto_segments(n_seqs, B, T, H, d_k, d_v));
+    // n_seqs == B is read as a fixed-length batch; a packed batch's need is the
+    // larger one only when it holds a single sequence, so return the larger.
+    const size_t fixed = tc_workspace(n_seqs == B, n_seqs, B, T, H,
+                                      auto_segments(n_seqs, B, T, H, d_k, d_v));
+    const size_t packed = tc_workspace(false, n_seqs, 1, (int64_t)B * T, H, 1);
+    return n_seqs == B && B == 1 && packed > fixed ? packed : fixed;
 }
 
 size_t kda_chunk_prefill_segmented_workspace_size(int B, int64_t T, int H, int d_k, int d_v,
                                                   int chunk, kda_dtype dtype, int n_segments) {
     if (B <= 0 || T < 0 || H <= 0 || n_segments <= 0) return 0;
     if (!use_chunked_tc(d_k, d_v, chunk, dtype)) return 0;
-    return tc_workspace(B, B, T, H, n_segments);
+    return tc_workspace(true, B, B, T, H, n_segments);
 }
 
 int kda_chunk_prefill_auto_segments(int B, int64_t T, int H, int d_k, int d_v, int chunk,
                                     kda_dtype dtype) {
     if (B <= 0 || T <= 0 || H <= 0 || !use_chunked_tc(d_k, d_v, chunk, dtype)) return 1;
-    return kda::chunked_tc_segments_used(T, auto_segments(B, B, T, H, d_k, d_v));
+    return kda::chunked_tc_segments_used(window_span(T), auto_segments(B, B, T, H, d_k, d_v));
 }
 
 static kda_status prefill_impl(const void* q, const void* k, const void* v, const void* z,
@@ -215,30 +230,43 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         // Segments: n_segments > 0 asks for that many (fixed-length batches
         // only); 0 picks them automatically, falling back to the plain pass when
         // the workspace only covers that.
+        const bool fixed = cu_seqlens == nullptr;
         int G = 1;
         if (n_segments > 0) {
-            if (cu_seqlens && n_segments > 1)
+            if (!fixed && n_segments > 1)
                 return fail(KDA_ERR_UNSUPPORTED, "segments need a fixed-length batch (cu_seqlens == NULL)");
-            if ((int64_t)B * kda::chunked_tc_segments_used(T, n_segments) > 65535)
+            if ((int64_t)B * kda::chunked_tc_segments_used(window_span(T), n_segments) > 65535)
                 return fail(KDA_ERR_UNSUPPORTED, "B x segments must be <= 65535");
             G = n_segments;
-        } else if (!cu_seqlens) {
+        } else if (fixed) {
             G = auto_segments(n_seqs, B, T, H, d_k, d_v);
-            if (G > 1 && workspace_bytes < tc_workspace(n_seqs, B, T, H, G)) G = 1;
+            if (G > 1 && workspace_bytes < tc_workspace(true, n_seqs, B, T, H, G)) G = 1;
         }
-        const size_t need = tc_workspace(n_seqs, cu_seqlens ? 1 : B, cu_seqlens ? T_total : T, H, G);
-        if (need > 0) {
-            if (workspace == nullptr || workspace_bytes < need)
-                return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu at %p",
-                            need, workspace_bytes, workspace);
-            if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-                return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
-        }
-        return cuda_status(kda::run_chunked_tc(q, k, v, z, beta, A, o, initial_state,
-                                               final_state, cu_seqlens, n_seqs, T, T_total, H,
-                                               d_k, d_v, workspace, ck, stream, device_sm_count(),
-                                               G),
-                           "kda_chunk_prefill (chunked tensor-core path)");
+        const size_t need = fixed ? tc_workspace(true, n_seqs, B, T, H, G)
+                                  : tc_workspace(false, n_seqs, 1, T_total, H, 1);
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu at %p", need,
+                        workspace_bytes, workspace);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+        // Windows: at most kWindowTokens per launch (per sequence when fixed, in
+        // all when packed).  The states cross windows in final_state, or in the
+        // workspace's carry area when the caller wants no final state.
+        const int64_t span = fixed ? T : T_total;
+        float* carry = final_state;
+        if (span > kda::kWindowTokens && carry == nullptr)
+            carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + need -
+                                             carry_bytes(n_seqs, H));
+        int64_t w0 = 0;
+        do {
+            const int64_t w1 = span - w0 < kda::kWindowTokens ? span : w0 + kda::kWindowTokens;
+            const cudaError_t e = kda::run_chunked_tc(
+                q, k, v, z, beta, A, o, initial_state, carry, carry, cu_seqlens, n_seqs, T,
+                T_total, w0, w1, H, d_k, d_v, workspace, ck, stream, device_sm_count(), G);
+            if (e != cudaSuccess) return cuda_status(e, "kda_chunk_prefill (chunked tensor-core path)");
+            w0 = w1;
+        } while (w0 < span);
+        return ok();
     }
     if (use_chunk16_tc(d_k, d_v, chunk, dtype)) {
         if (workspace == nullptr || workspace_bytes < kda::CHUNK16_WORKSPACE_BYTES)
@@ -326,7 +354,7 @@ kda_status kda_chunk_prefill_from_host(const void* q_h, const void* k_h, const v
     KDA_REQUIRE_PTR(beta_d);
     KDA_REQUIRE_PTR(o_d);
     const int64_t seg = segment_tokens < T ? segment_tokens : T;
-    const size_t need = tc_workspace(1, 1, seg, H, 1);
+    const size_t need = tc_workspace(true, 1, 1, seg, H, 1);
     if (workspace == nullptr || workspace_bytes < need)
         return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
                     workspace_bytes);

@@ -176,19 +176,44 @@ static_assert(R_TF + 64 * F_LD * 4 <= R_TB && R_XS + 1024 * 4 <= R_BKT, "solve s
 static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions");
 static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
+// Sequences of one launch.  A launch covers a window of tokens: for a
+// fixed-length batch, positions [w0, w1) of every sequence; for a packed one,
+// rows [w0, w1) of the packed tensor, each sequence clipped to them (the
+// chunked form is exact whatever the chunk boundaries, so a window may cut a
+// sequence anywhere; the state carries over between windows).
 struct SeqMap {
     const int32_t* cu;  // nullable
     int64_t T;          // per-sequence length when cu == nullptr
-    int64_t T_total;
+    int64_t T_total;    // token rows of the input tensors
     int n_seqs;
+    int64_t w0, w1;     // the window
 };
 
-// First package slot of sequence n: floor(bos / 64) + n.  Slots of different
-// sequences never overlap, and every slot is below floor(T_total / 64) + n_seqs.
+// The rows of sequence n inside the window, [bos, eos), and its first row
+// bos_seq.  Returns the sequence's first package slot, floor(p / 64) + n with p
+// = bos counted from the window's start (packed) or n (w1 - w0) (fixed
+// length): slots of different sequences never overlap and every slot is below
+// floor(window tokens / 64) + n_seqs.
+__device__ __forceinline__ int64_t seq_slot_base(const SeqMap& m, int n, int64_t& bos,
+                                                 int64_t& eos, int64_t& bos_seq) {
+    if (m.cu) {
+        int64_t b, e;
+        seq_bounds(m.cu, n, m.T, m.T_total, b, e);
+        bos_seq = b;
+        bos = b > m.w0 ? b : m.w0;
+        eos = e < m.w1 ? e : m.w1;
+        if (eos < bos) eos = bos;
+        return (bos - m.w0) / kC + n;
+    }
+    bos_seq = (int64_t)n * m.T;
+    bos = bos_seq + m.w0;
+    eos = bos_seq + m.w1;
+    return (int64_t)n * (m.w1 - m.w0) / kC + n;
+}
 __device__ __forceinline__ int64_t seq_slot_base(const SeqMap& m, int n, int64_t& bos,
                                                  int64_t& eos) {
-    seq_bounds(m.cu, n, m.T, m.T_total, bos, eos);
-    return bos / kC + n;
+    int64_t bos_seq;
+    return seq_slot_base(m, n, bos, eos, bos_seq);
 }
 
 // Byte offset of 16-byte chunk q (0..3) of row `row` in a [rows][32] bf16 tile.
@@ -1186,13 +1211,13 @@ struct SegSpec {
 __global__ void __launch_bounds__(kStateThreads, 1)
 state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                   const float* __restrict__ S0, float* __restrict__ S1, SeqMap map, int H,
-                  int dk, int dv, CheckpointSpec ck, SegSpec seg) {
+                  int dk, int dv, CheckpointSpec ck, SegSpec seg, const float* __restrict__ Scarry) {
     const int tile = blockIdx.x, n = blockIdx.y / seg.G, g = blockIdx.y % seg.G, h = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j0 = tile * kJ;
 
-    int64_t bos, eos;
-    const int64_t slot_seq = seq_slot_base(map, n, bos, eos);
+    int64_t bos, eos, bos_seq;
+    const int64_t slot_seq = seq_slot_base(map, n, bos, eos, bos_seq);
     const int nc_seq = (int)((eos - bos + kC - 1) / kC);
     const int c0 = (int)((int64_t)g * seg.cps < nc_seq ? (int64_t)g * seg.cps : nc_seq);
     const int nc = (nc_seq - c0) < seg.cps ? (nc_seq - c0) : seg.cps;   // this segment's chunks
@@ -1218,7 +1243,9 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     // this tile of S0 / S1 ([d_k][d_v] per (n, h)); rows d_k .. 127 of a
     // narrower head stay 0 on chip and are neither read nor written
     const size_t smat = ((size_t)n * H + h) * dk * dv + j0;
-    const float* S_in = g == 0 ? (S0 ? S0 + smat : nullptr)
+    // A sequence that started in an earlier window continues from the carried state.
+    const float* S_first = bos == bos_seq ? S0 : Scarry;
+    const float* S_in = g == 0 ? (S_first ? S_first + smat : nullptr)
                                : seg.S_start + (((size_t)n * H + h) * (seg.G - 1) + (g - 1)) * dk * dv + j0;
     float st[16];
     auto store_state = [&](float* mat) {                             // mat: S of (n, h) + j0
@@ -1414,11 +1441,13 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 mbar_arrive(dfree + b);
             }
             if (cc + 2 < nc) load_x_frag(pkg_of(cc + 2), tile, f, xr);
-            // Checkpoint: the state after every `ck.every` tokens of this sequence.
+            // Checkpoint: the state after every `ck.every` tokens of this sequence
+            // (bos - bos_seq of them precede this window).
             if (ck.out) {
                 const int64_t done = (int64_t)(c0 + cc + 1) * kC;
-                if (done <= eos - bos && done % ck.every == 0 && done / ck.every <= ck.max_count)
-                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv + j0);
+                const int64_t at = (bos - bos_seq) + done;
+                if (done <= eos - bos && at % ck.every == 0 && at / ck.every <= ck.max_count)
+                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (at / ck.every - 1)) * dk * dv + j0);
             }
             return true;
         };
@@ -1806,9 +1835,10 @@ int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sm
 
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0, float* S1,
-                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
-                           int dk, int dv, void* workspace, const CheckpointSpec& ck,
-                           cudaStream_t stream, int num_sms, int n_segments) {
+                           const float* Scarry, const int32_t* cu, int n_seqs, int64_t T,
+                           int64_t rows, int64_t w0, int64_t w1, int H, int dk, int dv,
+                           void* workspace, const CheckpointSpec& ck, cudaStream_t stream,
+                           int num_sms, int n_segments) {
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
@@ -1833,14 +1863,15 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     e = cudaMemsetAsync(ws, 0, tc::WS_HEADER, stream);
     if (e != cudaSuccess) return e;
-    tc::SeqMap map{cu, T, T_total, n_seqs};
+    tc::SeqMap map{cu, T, rows, n_seqs, w0, w1};
     using bf = __nv_bfloat16;
     profile_event(0, stream);
-    const int64_t slots = T_total / tc::kC + n_seqs + 1;
-    if (T_total > 0) {
+    const int64_t win_tokens = cu ? (w1 - w0) : (int64_t)n_seqs * (w1 - w0);
+    const int64_t slots = win_tokens / tc::kC + n_seqs + 1;
+    if (win_tokens > 0) {
         tc::InputMaps maps;
-        if (!make_input_map(&maps.q, q, T_total, H, dk) || !make_input_map(&maps.k, k, T_total, H, dk) ||
-            !make_input_map(&maps.v, v, T_total, H, dv) || !make_input_map(&maps.z, z, T_total, H, dk))
+        if (!make_input_map(&maps.q, q, rows, H, dk) || !make_input_map(&maps.k, k, rows, H, dk) ||
+            !make_input_map(&maps.v, v, rows, H, dv) || !make_input_map(&maps.z, z, rows, H, dk))
             return cudaErrorInvalidValue;
         const int64_t n_items = slots * H;
         const int64_t grid = n_items < num_sms ? n_items : num_sms;
@@ -1852,7 +1883,7 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
     profile_event(1, stream);
     tc::SegSpec seg;
     int cps = 0x7fffffff, Ge = 1;
-    if (cu == nullptr) segment_shape(T, n_segments, cps, Ge);
+    if (cu == nullptr) segment_shape(w1 - w0, n_segments, cps, Ge);
     if (Ge > 1) {
         // [X | M] per (sequence, head, segment < G - 1), then the start states
         float* Y = reinterpret_cast<float*>(ws + tc::WS_HEADER + (size_t)slots * H * tc::PKG_BYTES);
@@ -1868,14 +1899,17 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
         if (e != cudaSuccess) return e;
         profile_event(2, stream);
         dim3 grid_c((unsigned)(dv / tc::kCombCols), (unsigned)n_seqs, (unsigned)H);
-        tc::seg_combine_kernel<<<grid_c, 256, tc::COMB_SMEM, stream>>>(Y, S0, S_start, H, dk, dv, Ge);
+        // Segments are for fixed-length batches, whose sequences all start in the
+        // first window: later windows start from the carried states.
+        tc::seg_combine_kernel<<<grid_c, 256, tc::COMB_SMEM, stream>>>(Y, w0 == 0 ? S0 : Scarry,
+                                                                       S_start, H, dk, dv, Ge);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         profile_event(3, stream);
     }
     dim3 grid_s((unsigned)(dv / tc::kJ), (unsigned)(n_seqs * Ge), (unsigned)H);
     tc::state_pass_kernel<<<grid_s, tc::kStateThreads, tc::S_SMEM, stream>>>(
-        ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck, seg);
+        ws, static_cast<bf*>(o), S0, S1, map, H, dk, dv, ck, seg, Scarry);
     e = cudaGetLastError();
     profile_event(Ge > 1 ? 4 : 2, stream);
     return e;

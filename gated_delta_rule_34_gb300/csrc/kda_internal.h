@@ -52,12 +52,22 @@ cudaError_t run_recurrent(const void* q, const void* k, const void* v, const voi
 size_t chunked_tc_workspace_bytes(int n_seqs, int64_t T_total, int H, int64_t T_seq, int G);
 int chunked_tc_segments_used(int64_t T_seq, int G);
 int chunked_tc_auto_segments(int B, int64_t T, int H, int dk, int dv, int num_sms);
+// One launch covers a window of tokens: positions [w0, w1) of every sequence
+// of a fixed-length batch (T tokens each), or rows [w0, w1) of a packed one
+// (`rows` token rows in all).  A sequence that starts inside the window reads
+// S0; one that started before reads Scarry (the state the previous window
+// left there); every sequence's state at the window's end goes to S1.
 cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const void* z,
                            const void* beta, const float* A, void* o, const float* S0,
-                           float* S1, const int32_t* cu, int n_seqs, int64_t T,
-                           int64_t T_total, int H, int dk, int dv, void* workspace,
-                           const CheckpointSpec& ck, cudaStream_t stream, int num_sms,
-                           int n_segments);
+                           float* S1, const float* Scarry, const int32_t* cu, int n_seqs,
+                           int64_t T, int64_t rows, int64_t w0, int64_t w1, int H, int dk,
+                           int dv, void* workspace, const CheckpointSpec& ck,
+                           cudaStream_t stream, int num_sms, int n_segments);
+
+// The 64-token path runs at most this many tokens at a time (per sequence of
+// a fixed-length batch, or in all of a packed one), the state carried from
+// window to window, so that its workspace is bounded by one window's packages.
+constexpr int64_t kWindowTokens = 65536;
 
 // Chunked tensor-core path with 16-token chunks (bf16; d_k and d_v multiples
 // of 16, at most 128): one fused kernel per (sequence, head), no package

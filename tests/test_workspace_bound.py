@@ -43,18 +43,44 @@ def test_slots_stay_in_bounds():
                 used |= run
 
 
+WINDOW = 65536          # tokens per launch of the 64-token path (per sequence when fixed)
+CARRY = 128 * 128 * 4   # bytes of carried state per (sequence, head) between windows
+
+
 def test_workspace_size_query_matches_bound():
-    # Packages of the plain pass (the segment-parallel records come on top of them for
-    # fixed-length batches that kda_chunk_prefill splits into segments).
+    # Packages of one window (the segment-parallel records come on top of them for
+    # fixed-length batches that kda_chunk_prefill splits into segments, and a carry area
+    # for calls that run in several windows).
     L = kda.lib()
     for n_seqs, B, T, H in [(1, 1, 4096, 8), (2, 2, 4096, 8), (64, 1, 1048576, 16), (3, 1, 1, 1),
-                            (1, 1, 65536, 32)]:
-        slots = (B * T) // 64 + n_seqs + 1
+                            (1, 1, 65536, 32), (1, 1, 1 << 20, 32), (2, 2, 200000, 4)]:
+        fixed = n_seqs == B
+        span = T if fixed else B * T
+        w = min(span, WINDOW)
+        slots = (B * w if fixed else w) // 64 + n_seqs + 1
         packages = HEADER + slots * H * PKG_BYTES
+        carry = n_seqs * H * CARRY if span > WINDOW else 0
         got = L.kda_chunk_prefill_workspace_size(n_seqs, B, T, H, 128, 128, 64, 1)
-        if n_seqs != B:                       # packed: never segmented
-            assert got == packages
+        if not fixed:                         # packed: never segmented
+            assert got == packages + carry
             continue
         G = L.kda_chunk_prefill_auto_segments(B, T, H, 128, 128, 64, 1)
-        assert got == packages + n_seqs * H * (G - 1) * (128 + 64) * 1024
-        assert L.kda_chunk_prefill_segmented_workspace_size(B, T, H, 128, 128, 64, 1, 1) == packages
+        seg = packages + n_seqs * H * (G - 1) * (128 + 64) * 1024 + carry
+        if B == 1 and span > WINDOW:          # a single sequence may also come packed
+            packed = HEADER + (w // 64 + 2) * H * PKG_BYTES + H * CARRY
+            assert got == max(seg, packed)
+        else:
+            assert got == seg
+        assert (L.kda_chunk_prefill_segmented_workspace_size(B, T, H, 128, 128, 64, 1, 1)
+                == packages + carry)
+
+
+def test_workspace_is_bounded_by_one_window():
+    # A million-token, 32-head prefill needs one 65,536-token window of packages
+    # (about 3.3 GB), not the ~52 GB its whole length would.
+    L = kda.lib()
+    big = L.kda_chunk_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 64, 1)
+    one = L.kda_chunk_prefill_workspace_size(1, 1, 65536, 32, 128, 128, 64, 1)
+    assert big < 3.5e9 and big <= one + 32 * CARRY + 2 * 32 * PKG_BYTES
+    packed = L.kda_chunk_prefill_workspace_size(64, 1, 1 << 20, 16, 128, 128, 64, 1)
+    assert packed < 2e9
