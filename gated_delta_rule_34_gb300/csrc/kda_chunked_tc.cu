@@ -177,10 +177,12 @@ static_assert(R_UT + 16384 <= R_BKT && R_PKG + PKG_BYTES <= R_G, "reuse regions"
 static_assert(R_G + 64 * G_LD * 4 <= R_K && R_P == R_KC + 16384, "layout");
 
 // Sequences of one launch.  A launch covers a window of tokens: for a
-// fixed-length batch, positions [w0, w1) of every sequence; for a packed one,
-// rows [w0, w1) of the packed tensor, each sequence clipped to them (the
-// chunked form is exact whatever the chunk boundaries, so a window may cut a
-// sequence anywhere; the state carries over between windows).
+// fixed-length batch, positions [w0, w1) of every sequence (window edges are
+// multiples of 64); for a packed one, the chunks of each sequence whose first
+// row lies in rows [w0, w1) of the packed tensor, chunks being counted from the
+// sequence's own start (so a sequence's last chunk in a window may reach up to
+// 63 rows past w1, and checkpoints keep falling on chunk ends).  The state
+// carries over between windows.
 struct SeqMap {
     const int32_t* cu;  // nullable
     int64_t T;          // per-sequence length when cu == nullptr
@@ -191,19 +193,24 @@ struct SeqMap {
 
 // The rows of sequence n inside the window, [bos, eos), and its first row
 // bos_seq.  Returns the sequence's first package slot, floor(p / 64) + n with p
-// = bos counted from the window's start (packed) or n (w1 - w0) (fixed
-// length): slots of different sequences never overlap and every slot is below
-// floor(window tokens / 64) + n_seqs.
+// = bos counted from the window's start (packed; at least 0) or n (w1 - w0)
+// (fixed length): slots of different sequences never overlap, and every slot
+// is below floor(window tokens / 64) + n_seqs + 1 (for a packed window of
+// 64-multiple length the overhang of the last chunks fits: the last slot is at
+// most floor((w1 - w0 + 126) / 64) - 1 + (n_seqs - 1)).
 __device__ __forceinline__ int64_t seq_slot_base(const SeqMap& m, int n, int64_t& bos,
                                                  int64_t& eos, int64_t& bos_seq) {
     if (m.cu) {
         int64_t b, e;
         seq_bounds(m.cu, n, m.T, m.T_total, b, e);
         bos_seq = b;
-        bos = b > m.w0 ? b : m.w0;
-        eos = e < m.w1 ? e : m.w1;
+        // first chunk start of the sequence at or after row w (chunks from b)
+        auto align = [&](int64_t w) { return w <= b ? b : b + (w - b + kC - 1) / kC * kC; };
+        const int64_t lo = align(m.w0), hi = align(m.w1);
+        bos = lo < e ? lo : e;
+        eos = hi < e ? hi : e;
         if (eos < bos) eos = bos;
-        return (bos - m.w0) / kC + n;
+        return ((bos > m.w0 ? bos : m.w0) - m.w0) / kC + n;
     }
     bos_seq = (int64_t)n * m.T;
     bos = bos_seq + m.w0;

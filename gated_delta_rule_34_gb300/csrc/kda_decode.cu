@@ -142,6 +142,10 @@ __device__ __forceinline__ void cp_async16_cg(void* dst_smem, const void* src) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async8_ca(void* dst_smem, const void* src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst_smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all_own() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -290,14 +294,30 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
 // accepted prefix.  "How Kimi K3 is built" (section "How to serve two
 // different caches") describes K3 keeping the small input projections of the
 // draft tokens instead of a copy of the state after each one, and recomputing
-// the accepted span on chip.  Both kernels read S once into registers (same
-// thread layout as decode_kernel) and step through up to kSpecMaxT tokens:
+// the accepted span on chip.  Both kernels read S once into registers and
+// step through up to kSpecMaxT tokens in fp32:
 //   verify  o_t for every draft token; S is not written.
 //   commit  S advanced by the first n_accept[b] tokens, written once in place.
+//
+// Decay factoring over the span: with gam_t = prod_{s <= t} a_s (per channel,
+// at least e^{-5 kSpecMaxT} = e^-80, inside the fp32 range) the registers hold
+// R = Diag(1 / gam) S, so that a token needs no rescaling of the state:
+//   S'^T k = R^T (gam_t k),  S'^T q = R^T (gam_t q),  u = b (v - S'^T k),
+//   R <- R + (k / gam_t) u^T,  o_t = S'^T q + u (k^T q),
+// and commit writes S = Diag(gam_T) R.  Thread layout: warp w owns columns
+// 16 w .. 16 w + 15; lane (rq = lane / 8, cq = lane % 8) holds rows
+// 32 rq .. 32 rq + 31 of columns 16 w + 2 cq, + 1 (64 registers), so the d_k
+// reductions are in-thread sums plus two xor-shuffles, and the per-row vectors
+// are read as float4 from shared memory rows whose quarters are skewed by four
+// floats (no bank conflict between the four row quarters).
 // ---------------------------------------------------------------------------
 namespace kda {
 
 constexpr int kSpecMaxT = 16;
+constexpr uint32_t kSpecStage = 32 * kDecodeThreads * 8;   // 64 KiB: the state, staged
+constexpr int kSpecPitch = 4 * 36;   // floats per token row: four 32-row quarters, each + 4 pad
+
+__device__ __forceinline__ int spec_row(int c) { return (c >> 5) * 36 + (c & 31); }
 
 template <typename T, bool kVerify>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
@@ -309,9 +329,9 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     const int b = bh / H, h = bh % H;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int rg = lane >> 2, cg = lane & 3;
-    const int j0 = warp * 16 + cg * 4;
-    const bool col_ok = j0 < dv;
+    const int rq = lane >> 3, cq = lane & 7;
+    const int r0 = 32 * rq, j0 = warp * 16 + 2 * cq;
+    const bool col_ok = j0 < dv;            // dv is a multiple of 4: both columns or neither
     float* Sbh = state + (size_t)bh * dk * dv;
     int n_steps = Tn;
     if (!kVerify) {
@@ -320,86 +340,123 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
         if (n_steps == 0) return;                       // nothing accepted: S unchanged
     }
 
-    float4 s[kDecodeRows];
+    // The state read starts first: each thread copies its own 32 x 8 bytes into
+    // its own shared-memory slots (cp.async, no registers held), so the read
+    // overlaps the per-token preparation below; rows past d_k read as zeros.
+    extern __shared__ float2 s_stage[];                 // [32][kDecodeThreads]
 #pragma unroll
-    for (int i = 0; i < kDecodeRows; ++i) {
-        const int r = rg + 8 * i;
-        s[i] = (col_ok && r < dk)
-                   ? __ldcs(reinterpret_cast<const float4*>(Sbh + (size_t)r * dv + j0))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 32; ++i) {
+        const int r = r0 + i;
+        if (col_ok && r < dk) cp_async8_ca(&s_stage[i * kDecodeThreads + tid], Sbh + (size_t)r * dv + j0);
+        else s_stage[i * kDecodeThreads + tid] = make_float2(0.f, 0.f);
     }
 
-    // Per-token vectors of the span: decay a (gate inline), k, q, v, beta.
-    __shared__ float s_a[kSpecMaxT][128], s_k[kSpecMaxT][128], s_q[kSpecMaxT][128];
-    __shared__ float s_v[kSpecMaxT][128], s_b[kSpecMaxT];
-    for (int idx = tid; idx < n_steps * 128; idx += kDecodeThreads) {
-        const int t = idx >> 7, c = idx & 127;
-        const size_t row = ((size_t)b * Tn + t) * H + h;
-        float kk = 0.f, qq = 0.f, aa = 1.f, vv = 0.f;
-        if (c < dk) {
-            kk = to_f32(k[row * dk + c]);
-            if (kVerify) qq = to_f32(q[row * dk + c]);
-            aa = expf(gate_accurate(expf(A[(size_t)h * dk + c]), to_f32(z[row * dk + c])));
+    // Per-token vectors: gam_t k, gam_t q, k / gam_t (rows skewed), v, beta, k^T q.
+    __shared__ __align__(16) float s_kg[kSpecMaxT][kSpecPitch], s_qg[kSpecMaxT][kSpecPitch];
+    __shared__ __align__(16) float s_kh[kSpecMaxT][kSpecPitch];
+    __shared__ __align__(16) float s_v[kSpecMaxT][128];
+    __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_gam[128];
+    if (tid < 128) {
+        const int c = tid;
+        const float ea = c < dk ? expf(A[(size_t)h * dk + c]) : 0.f;
+        float L = 0.f;                                   // log gam_t
+        for (int t = 0; t < n_steps; ++t) {
+            const size_t row = ((size_t)b * Tn + t) * H + h;
+            float kk = 0.f, qq = 0.f;
+            if (c < dk) {
+                kk = to_f32(k[row * dk + c]);
+                if (kVerify) qq = to_f32(q[row * dk + c]);
+                L += gate_accurate(ea, to_f32(z[row * dk + c]));
+            }
+            const float gam = expf(L), igam = expf(-L);
+            s_kg[t][spec_row(c)] = gam * kk;
+            s_qg[t][spec_row(c)] = gam * qq;
+            s_kh[t][spec_row(c)] = igam * kk;
+            s_v[t][c] = c < dv ? to_f32(v[row * dv + c]) : 0.f;
         }
-        if (c < dv) vv = to_f32(v[row * dv + c]);
-        s_a[t][c] = aa;
-        s_k[t][c] = kk;
-        s_q[t][c] = qq;
-        s_v[t][c] = vv;
+        s_gam[c] = expf(L);
+    } else if (tid < 128 + kSpecMaxT) {
+        const int t = tid - 128;
+        if (t < n_steps) s_b[t] = to_f32(beta[((size_t)b * Tn + t) * H + h]);
+    } else if (kVerify && tid >= 160 && tid < 160 + kSpecMaxT) {
+        // k^T q per token (unscaled), one thread per token
+        const int t = tid - 160;
+        if (t < n_steps) {
+            const size_t row = ((size_t)b * Tn + t) * H + h;
+            float acc = 0.f;
+            for (int c = 0; c < dk; ++c) acc = fmaf(to_f32(k[row * dk + c]), to_f32(q[row * dk + c]), acc);
+            s_kq[t] = acc;
+        }
     }
-    if (tid < n_steps) s_b[tid] = to_f32(beta[((size_t)b * Tn + tid) * H + h]);
     __syncthreads();
+    // R = S on entry (gam_0 = 1).
+    cp_async_wait_all_own();
+    float2 s[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s[i] = s_stage[i * kDecodeThreads + tid];
 
     for (int t = 0; t < n_steps; ++t) {
-        float kq = 0.f;
-        if (kVerify) {
+        float pk[2] = {0.f, 0.f}, pq[2] = {0.f, 0.f};
+        const float4* kg4 = reinterpret_cast<const float4*>(&s_kg[t][36 * rq]);
+        const float4* qg4 = reinterpret_cast<const float4*>(&s_qg[t][36 * rq]);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) kq += s_k[t][lane + 32 * m] * s_q[t][lane + 32 * m];
-            kq = warp_sum(kq);
-        }
-        float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 kg = kg4[i4];
+            const float kv[4] = {kg.x, kg.y, kg.z, kg.w};
 #pragma unroll
-        for (int i = 0; i < kDecodeRows; ++i) {
-            const int r = rg + 8 * i;
-            const float a = s_a[t][r], kr = s_k[t][r];
-            s[i].x *= a; s[i].y *= a; s[i].z *= a; s[i].w *= a;
-            pk[0] = fmaf(s[i].x, kr, pk[0]); pk[1] = fmaf(s[i].y, kr, pk[1]);
-            pk[2] = fmaf(s[i].z, kr, pk[2]); pk[3] = fmaf(s[i].w, kr, pk[3]);
+            for (int e = 0; e < 4; ++e) {
+                pk[0] = fmaf(s[4 * i4 + e].x, kv[e], pk[0]);
+                pk[1] = fmaf(s[4 * i4 + e].y, kv[e], pk[1]);
+            }
             if (kVerify) {
-                const float qr = s_q[t][r];
-                pq[0] = fmaf(s[i].x, qr, pq[0]); pq[1] = fmaf(s[i].y, qr, pq[1]);
-                pq[2] = fmaf(s[i].z, qr, pq[2]); pq[3] = fmaf(s[i].w, qr, pq[3]);
+                const float4 qg = qg4[i4];
+                const float qv[4] = {qg.x, qg.y, qg.z, qg.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    pq[0] = fmaf(s[4 * i4 + e].x, qv[e], pq[0]);
+                    pq[1] = fmaf(s[4 * i4 + e].y, qv[e], pq[1]);
+                }
             }
         }
 #pragma unroll
-        for (int m = 4; m <= 16; m <<= 1) {
+        for (int m = 8; m <= 16; m <<= 1) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
                 if (kVerify) pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
             }
         }
         const float bt = s_b[t];
-        float u[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) u[c] = bt * ((col_ok ? s_v[t][j0 + c] : 0.f) - pk[c]);
-        if (kVerify && col_ok && rg == 0) {
+        const float2 vv = col_ok ? *reinterpret_cast<const float2*>(&s_v[t][j0]) : make_float2(0.f, 0.f);
+        const float u0 = bt * (vv.x - pk[0]), u1 = bt * (vv.y - pk[1]);
+        if (kVerify && col_ok && rq == 0) {
+            const float kq = s_kq[t];
             T* ob = o + (((size_t)b * Tn + t) * H + h) * dv + j0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ob[c] = from_f32<T>(fmaf(u[c], kq, pq[c]));
+            ob[0] = from_f32<T>(fmaf(u0, kq, pq[0]));
+            ob[1] = from_f32<T>(fmaf(u1, kq, pq[1]));
         }
+        if (!kVerify || t + 1 < n_steps) {
+            const float4* kh4 = reinterpret_cast<const float4*>(&s_kh[t][36 * rq]);
 #pragma unroll
-        for (int i = 0; i < kDecodeRows; ++i) {
-            const float kr = s_k[t][rg + 8 * i];
-            s[i].x = fmaf(kr, u[0], s[i].x); s[i].y = fmaf(kr, u[1], s[i].y);
-            s[i].z = fmaf(kr, u[2], s[i].z); s[i].w = fmaf(kr, u[3], s[i].w);
+            for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 kh = kh4[i4];
+                const float kv[4] = {kh.x, kh.y, kh.z, kh.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[4 * i4 + e].x = fmaf(kv[e], u0, s[4 * i4 + e].x);
+                    s[4 * i4 + e].y = fmaf(kv[e], u1, s[4 * i4 + e].y);
+                }
+            }
         }
     }
     if (!kVerify) {
 #pragma unroll
-        for (int i = 0; i < kDecodeRows; ++i) {
-            const int r = rg + 8 * i;
-            if (col_ok && r < dk) __stcs(reinterpret_cast<float4*>(Sbh + (size_t)r * dv + j0), s[i]);
+        for (int i = 0; i < 32; ++i) {
+            const int r = r0 + i;
+            if (col_ok && r < dk) {
+                const float g = s_gam[r];
+                __stcs(reinterpret_cast<float2*>(Sbh + (size_t)r * dv + j0), make_float2(g * s[i].x, g * s[i].y));
+            }
         }
     }
 }
@@ -408,6 +465,22 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
                      const float* A, float* state, void* o, const int32_t* n_accept, int B, int Tn,
                      int H, int dk, int dv, bool bf16, bool verify, cudaStream_t stream) {
     const unsigned grid = (unsigned)((int64_t)B * H);
+    constexpr int kMaxDevices = 64;
+    static bool attr_done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+        const void* fns[4] = {(const void*)spec_kernel<__nv_bfloat16, true>,
+                              (const void*)spec_kernel<__nv_bfloat16, false>,
+                              (const void*)spec_kernel<float, true>, (const void*)spec_kernel<float, false>};
+        for (const void* fn : fns) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSpecStage);
+            if (e != cudaSuccess) return e;
+        }
+        attr_done[dev] = true;
+    }
     if (bf16) {
         using Tb = __nv_bfloat16;
         auto kq = static_cast<const Tb*>(q);
@@ -416,10 +489,10 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
         auto kz = static_cast<const Tb*>(z);
         auto kb = static_cast<const Tb*>(beta);
         if (verify)
-            spec_kernel<Tb, true><<<grid, kDecodeThreads, 0, stream>>>(
+            spec_kernel<Tb, true><<<grid, kDecodeThreads, kSpecStage, stream>>>(
                 kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
         else
-            spec_kernel<Tb, false><<<grid, kDecodeThreads, 0, stream>>>(
+            spec_kernel<Tb, false><<<grid, kDecodeThreads, kSpecStage, stream>>>(
                 kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
     } else {
         auto kq = static_cast<const float*>(q);
@@ -428,10 +501,10 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
         auto kz = static_cast<const float*>(z);
         auto kb = static_cast<const float*>(beta);
         if (verify)
-            spec_kernel<float, true><<<grid, kDecodeThreads, 0, stream>>>(
+            spec_kernel<float, true><<<grid, kDecodeThreads, kSpecStage, stream>>>(
                 kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
         else
-            spec_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
+            spec_kernel<float, false><<<grid, kDecodeThreads, kSpecStage, stream>>>(
                 kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
     }
     return cudaGetLastError();

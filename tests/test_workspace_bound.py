@@ -84,3 +84,51 @@ def test_workspace_is_bounded_by_one_window():
     assert big < 3.5e9 and big <= one + 32 * CARRY + 2 * 32 * PKG_BYTES
     packed = L.kda_chunk_prefill_workspace_size(64, 1, 1 << 20, 16, 128, 128, 64, 1)
     assert packed < 2e9
+
+
+def _window_part(b, e, w0, w1):
+    """A sequence's chunks whose first row lies in [w0, w1), chunks counted from b."""
+    def align(w):
+        return b if w <= b else b + (w - b + 63) // 64 * 64
+    lo, hi = align(w0), align(w1)
+    bos, eos = min(lo, e), min(hi, e)
+    return bos, max(eos, bos)
+
+
+def test_packed_window_slots_stay_in_bounds_and_cover_every_chunk_once():
+    rng = random.Random(1)
+    for _ in range(3000):
+        N = rng.randint(1, 9)
+        lens = [rng.choice([0, 1, 63, 64, 65, rng.randint(0, 3000)]) for _ in range(N)]
+        cu = [0]
+        for ln in lens:
+            cu.append(cu[-1] + ln)
+        T = cu[-1]
+        W = rng.choice([64, 128, 256, 1024])
+        seen = {n: set() for n in range(N)}
+        w0 = 0
+        while True:
+            w1 = min(T, w0 + W)
+            slots = W // 64 + N + 1          # the workspace holds one full window
+            used = set()
+            last = -1
+            for n in range(N):
+                b, e = cu[n], cu[n + 1]
+                bos, eos = _window_part(b, e, w0, w1)
+                base = (max(bos, w0) - w0) // 64 + n
+                assert base >= last, "slot bases rise with the sequence index"
+                last = base
+                nc = (eos - bos + 63) // 64
+                run = set(range(base, base + nc))
+                assert not (run & used) and all(0 <= s < slots for s in run)
+                used |= run
+                for c in range(nc):
+                    start = bos + 64 * c
+                    assert (start - b) % 64 == 0, "chunks stay on the sequence's own grid"
+                    assert start not in seen[n], "a chunk runs in one window only"
+                    seen[n].add(start)
+            w0 = w1
+            if w0 >= T:
+                break
+        for n in range(N):
+            assert seen[n] == set(range(cu[n], cu[n + 1], 64)), "every chunk runs once"
