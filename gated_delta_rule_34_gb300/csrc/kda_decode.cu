@@ -354,39 +354,52 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     // Per-token vectors: gam_t k, gam_t q, k / gam_t (rows skewed), v, beta, k^T q.
     __shared__ __align__(16) float s_kg[kSpecMaxT][kSpecPitch], s_qg[kSpecMaxT][kSpecPitch];
     __shared__ __align__(16) float s_kh[kSpecMaxT][kSpecPitch];
-    __shared__ __align__(16) float s_v[kSpecMaxT][128];
-    __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_gam[128];
+    __shared__ __align__(16) float s_v[kSpecMaxT][128], s_L[kSpecMaxT][128];
+    __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_kqp[kSpecMaxT][4], s_gam[128];
+    // (a) every (token, channel) at once: raw k and q, v, the gate g, and k^T q
+    //     partial sums over each warp's 32 channels.
+    for (int idx = tid; idx < n_steps * 128; idx += kDecodeThreads) {
+        const int t = idx >> 7, c = idx & 127;
+        const size_t row = ((size_t)b * Tn + t) * H + h;
+        float kk = 0.f, qq = 0.f, g = 0.f;
+        if (c < dk) {
+            kk = to_f32(k[row * dk + c]);
+            if (kVerify) qq = to_f32(q[row * dk + c]);
+            g = gate_accurate(expf(A[(size_t)h * dk + c]), to_f32(z[row * dk + c]));
+        }
+        s_kh[t][spec_row(c)] = kk;
+        s_qg[t][spec_row(c)] = qq;
+        s_L[t][c] = g;
+        s_v[t][c] = c < dv ? to_f32(v[row * dv + c]) : 0.f;
+        if (kVerify) {
+            const float p = warp_sum(kk * qq);
+            if (lane == 0) s_kqp[t][c >> 5] = p;
+        }
+    }
+    if (tid < n_steps) s_b[tid] = to_f32(beta[((size_t)b * Tn + tid) * H + h]);
+    __syncthreads();
+    // (b) the running log-decay per channel, in place; k^T q per token
     if (tid < 128) {
-        const int c = tid;
-        const float ea = c < dk ? expf(A[(size_t)h * dk + c]) : 0.f;
-        float L = 0.f;                                   // log gam_t
+        float L = 0.f;
         for (int t = 0; t < n_steps; ++t) {
-            const size_t row = ((size_t)b * Tn + t) * H + h;
-            float kk = 0.f, qq = 0.f;
-            if (c < dk) {
-                kk = to_f32(k[row * dk + c]);
-                if (kVerify) qq = to_f32(q[row * dk + c]);
-                L += gate_accurate(ea, to_f32(z[row * dk + c]));
-            }
-            const float gam = expf(L), igam = expf(-L);
-            s_kg[t][spec_row(c)] = gam * kk;
-            s_qg[t][spec_row(c)] = gam * qq;
-            s_kh[t][spec_row(c)] = igam * kk;
-            s_v[t][c] = c < dv ? to_f32(v[row * dv + c]) : 0.f;
+            L += s_L[t][tid];
+            s_L[t][tid] = L;
         }
-        s_gam[c] = expf(L);
-    } else if (tid < 128 + kSpecMaxT) {
+    } else if (kVerify && tid < 128 + kSpecMaxT && tid - 128 < n_steps) {
         const int t = tid - 128;
-        if (t < n_steps) s_b[t] = to_f32(beta[((size_t)b * Tn + t) * H + h]);
-    } else if (kVerify && tid >= 160 && tid < 160 + kSpecMaxT) {
-        // k^T q per token (unscaled), one thread per token
-        const int t = tid - 160;
-        if (t < n_steps) {
-            const size_t row = ((size_t)b * Tn + t) * H + h;
-            float acc = 0.f;
-            for (int c = 0; c < dk; ++c) acc = fmaf(to_f32(k[row * dk + c]), to_f32(q[row * dk + c]), acc);
-            s_kq[t] = acc;
-        }
+        s_kq[t] = (s_kqp[t][0] + s_kqp[t][1]) + (s_kqp[t][2] + s_kqp[t][3]);
+    }
+    __syncthreads();
+    // (c) the decay-scaled vectors, every (token, channel) at once
+    for (int idx = tid; idx < n_steps * 128; idx += kDecodeThreads) {
+        const int t = idx >> 7, c = idx & 127, r = spec_row(c);
+        const float L = s_L[t][c];
+        const float gam = expf(L), igam = expf(-L);
+        const float kk = s_kh[t][r];
+        s_kg[t][r] = gam * kk;
+        s_qg[t][r] = gam * s_qg[t][r];
+        s_kh[t][r] = igam * kk;
+        if (t == n_steps - 1) s_gam[c] = gam;
     }
     __syncthreads();
     // R = S on entry (gam_0 = 1).
