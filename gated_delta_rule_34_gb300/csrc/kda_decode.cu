@@ -409,44 +409,50 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     for (int i = 0; i < 32; ++i) s[i] = s_stage[i * kDecodeThreads + tid];
 
     for (int t = 0; t < n_steps; ++t) {
-        float pk[2] = {0.f, 0.f}, pq[2] = {0.f, 0.f};
+        // two partial sums per column and vector halve the dependent FMA chains
+        float pk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, pq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         const float4* kg4 = reinterpret_cast<const float4*>(&s_kg[t][36 * rq]);
         const float4* qg4 = reinterpret_cast<const float4*>(&s_qg[t][36 * rq]);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
+            const int hp = i4 & 1;
             const float4 kg = kg4[i4];
             const float kv[4] = {kg.x, kg.y, kg.z, kg.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                pk[0] = fmaf(s[4 * i4 + e].x, kv[e], pk[0]);
-                pk[1] = fmaf(s[4 * i4 + e].y, kv[e], pk[1]);
+                pk[hp][0] = fmaf(s[4 * i4 + e].x, kv[e], pk[hp][0]);
+                pk[hp][1] = fmaf(s[4 * i4 + e].y, kv[e], pk[hp][1]);
             }
             if (kVerify) {
                 const float4 qg = qg4[i4];
                 const float qv[4] = {qg.x, qg.y, qg.z, qg.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    pq[0] = fmaf(s[4 * i4 + e].x, qv[e], pq[0]);
-                    pq[1] = fmaf(s[4 * i4 + e].y, qv[e], pq[1]);
+                    pq[hp][0] = fmaf(s[4 * i4 + e].x, qv[e], pq[hp][0]);
+                    pq[hp][1] = fmaf(s[4 * i4 + e].y, qv[e], pq[hp][1]);
                 }
             }
         }
+        pk[0][0] += pk[1][0];
+        pk[0][1] += pk[1][1];
+        pq[0][0] += pq[1][0];
+        pq[0][1] += pq[1][1];
 #pragma unroll
         for (int m = 8; m <= 16; m <<= 1) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
-                if (kVerify) pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
+                pk[0][c] += __shfl_xor_sync(0xffffffffu, pk[0][c], m);
+                if (kVerify) pq[0][c] += __shfl_xor_sync(0xffffffffu, pq[0][c], m);
             }
         }
         const float bt = s_b[t];
         const float2 vv = col_ok ? *reinterpret_cast<const float2*>(&s_v[t][j0]) : make_float2(0.f, 0.f);
-        const float u0 = bt * (vv.x - pk[0]), u1 = bt * (vv.y - pk[1]);
+        const float u0 = bt * (vv.x - pk[0][0]), u1 = bt * (vv.y - pk[0][1]);
         if (kVerify && col_ok && rq == 0) {
             const float kq = s_kq[t];
             T* ob = o + (((size_t)b * Tn + t) * H + h) * dv + j0;
-            ob[0] = from_f32<T>(fmaf(u0, kq, pq[0]));
-            ob[1] = from_f32<T>(fmaf(u1, kq, pq[1]));
+            ob[0] = from_f32<T>(fmaf(u0, kq, pq[0][0]));
+            ob[1] = from_f32<T>(fmaf(u1, kq, pq[0][1]));
         }
         if (!kVerify || t + 1 < n_steps) {
             const float4* kh4 = reinterpret_cast<const float4*>(&s_kh[t][36 * rq]);
