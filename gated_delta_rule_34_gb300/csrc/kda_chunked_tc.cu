@@ -167,8 +167,7 @@ constexpr uint32_t S_ST = kStages * ST_BYTES;      // 2 x S^T tile [32 j][128 c]
 constexpr uint32_t S_BAR = S_ST + 2 * 8192;
 constexpr uint32_t S_SMEM = S_BAR + 256;           // the dynamic base is 1024-aligned
 constexpr uint32_t kDBuf = 64;                     // per accumulator buffer: D_S, then D_O at +32
-constexpr uint32_t kNBuf = 2 * kDBuf;               // the N operand in TMEM: two buffers of 64 columns
-constexpr uint32_t kTmemCols = kNBuf + 2 * 64;
+constexpr uint32_t kTmemCols = 2 * kDBuf;
 constexpr int kL2Ahead = 6;                        // packages prefetched into L2 this far ahead
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
@@ -1243,8 +1242,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
     uint64_t* odone = sdone + 2;                                       // [2]
     uint64_t* stready = odone + 2;                                     // [2]
     uint64_t* dfree = stready + 2;                                     // [2]
-    uint64_t* nready = dfree + 2;                                      // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(nready + 2);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dfree + 2);
     volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
 
     const Frag f(warp, lane);
@@ -1290,7 +1288,6 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             mbar_init(odone + p, 1);
             mbar_init(stready + p, kUpdWarps);
             mbar_init(dfree + p, kUpdWarps + kOutWarps);
-            mbar_init(nready + p, kOutWarps);
         }
         *abort = 0;
         fence_mbar_init();
@@ -1332,18 +1329,17 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 const int b = cc & 1;
                 // accumulator buffer b was last read for chunk cc - 2
                 if (cc >= 2) ok = role_wait(dfree + b, ((cc - 2) >> 1) & 1, abort) && ok;
-                // N of chunk cc in TMEM buffer cc & 1 (its stage has landed)
-                ok = role_wait(nready + b, (cc >> 1) & 1, abort) && ok;
+                ok = role_wait(full + cc % kStages, (cc / kStages) & 1, abort) && ok;
                 if (cc >= 1) ok = role_wait(stready + b, ((cc - 1) >> 1) & 1, abort) && ok;
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t bdesc0 = desc_sw128(smem_u32(sm + S_ST + b * 8192));
-                const uint32_t a_tmem = tbase + kNBuf + b * 64;
+                const uint64_t adesc0 = desc_sw128(smem_u32(sm + (cc % kStages) * ST_BYTES));
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                    mma_bf16_ta(tbase + b * kDBuf, a_tmem + 8 * ks, bdesc0 + ((kb * 4096 + off) >> 4), idesc,
-                                ks > 0);
+                    mma_bf16(tbase + b * kDBuf, adesc0 + ((kb * PKG_BK + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, ks > 0);
                 }
                 mma_commit(sdone + b);
             }
@@ -1379,34 +1375,10 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             }
         }
     } else if (!upd) {
-        // ------------------------------- outputs o = Q' S + O' (warps 8-11),
-        // and the N operand of the S product, copied from its landed stage into
-        // TMEM buffer m & 1 two chunks ahead (lane = row c of N, TMEM lane c).
+        // ------------------------------- outputs o = Q' S + O' (warps 8-11)
         const int t = 16 * (warp & 3) + lane;              // token row, lanes 0..15
         const bool act = lane < 16;
         const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
-        auto fill_n = [&](int m) -> bool {
-            ok = role_wait(full + m % kStages, (m / kStages) & 1, abort) && ok;
-            if (!ok) return false;
-            const uint8_t* stg = sm + (m % kStages) * ST_BYTES;
-            const uint32_t row = 32 * (warp & 3) + lane;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {                  // columns 16 i .. 16 i + 15
-                const uint32_t kb = i >> 1, q0 = 4 * (i & 1);
-                uint32_t w[16];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const uint4 v4 = *reinterpret_cast<const uint4*>(stg + kb * PKG_BK + sw128(row, q0 + qq));
-                    w[4 * qq] = v4.x; w[4 * qq + 1] = v4.y; w[4 * qq + 2] = v4.z; w[4 * qq + 3] = v4.w;
-                }
-                tmem_st16(tl + kNBuf + (m & 1) * 64 + 16 * i, w);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(nready + (m & 1));
-            return true;
-        };
         // O'[t][0 .. 31] of chunk m, loaded two chunks ahead of its use
         auto load_op = [&](int m, uint4 (&r)[4]) {
             const uint8_t* tp = pkg_of(m) + PKG_OP + tile * 4096;
@@ -1438,8 +1410,6 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 }
             }
             if (act && cc + 2 < nc) load_op(cc + 2, r);
-            // N buffer cc & 1 is free: chunk cc's S product finished before its O product
-            if (cc + 2 < nc && !fill_n(cc + 2)) return false;
             return true;
         };
         uint4 ra[4], rb[4];
@@ -1447,8 +1417,7 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             load_op(0, ra);
             if (nc > 1) load_op(1, rb);
         }
-        bool filled = fill_n(0) && (nc < 2 || fill_n(1));
-        for (int cc = 0; filled && cc < nc; cc += 2) {
+        for (int cc = 0; cc < nc; cc += 2) {
             if (!step(cc, ra)) break;
             if (cc + 1 < nc && !step(cc + 1, rb)) break;
         }
