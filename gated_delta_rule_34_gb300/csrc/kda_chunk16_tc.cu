@@ -196,16 +196,6 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         const int64_t t0 = bos + (int64_t)ci * kC;
         const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
         const bool live = tt < len;
-        // the next chunk's token rows (q, k, v, z) into L2 while this one runs
-        if (tid < 4 * kC) {
-            const int64_t tn = t0 + kC + (tid & (kC - 1));
-            if (tn < eos) {
-                const int which = tid >> 4;
-                const __nv_bfloat16* base = which == 0 ? q : which == 1 ? k : which == 2 ? v : z;
-                const int d = which == 2 ? dv : dk;
-                bulk_prefetch_l2(base + ((size_t)tn * H + h) * d, 2u * (uint32_t)d);
-            }
-        }
 
         // ---- inputs of token tt, channels 8 c8 .. 8 c8 + 7; gate -> gs
         uint4 kr = make_uint4(0, 0, 0, 0), qr = kr, vr = kr, zr = kr;
