@@ -588,10 +588,13 @@ def e2e_prefill(kda, xp, wp, steps: int, segment_tokens: int = 8192):
 def run_ncu_case(case: str) -> int:
     """A short, fixed launch sequence for targeted ncu captures.
 
-    prefill: B=1, H=32, T=16384 (0.54 GB of inputs, larger than L2), two calls;
-             the second call's chunk_prep / state_pass are the ones to capture
-             (ncu -s 1 -c 1 with -k regex:chunk_prep or regex:state_pass).
-    decode:  the full B=256, H=32 decode step (0.54 GB state), three calls.
+    prefill:   B=1, H=32, T=16384 (0.54 GB of inputs, larger than L2), two calls;
+               the second call's chunk_prep / state_pass are the ones to capture
+               (ncu -s 1 -c 1 with -k regex:chunk_prep or regex:state_pass).
+    decode:    the full B=256, H=32 decode step (0.54 GB state), three calls.
+    chunk16:   the 16-token path, B=1, H=32, T=4096, two calls.
+    segmented: B=1, H=1, T=65536 with automatic segments, two calls.
+    spec:      verify + commit of 16 draft tokens, B=256, H=32, twice.
     """
     import torch
     import gated_delta_rule_34_gb300 as kda
@@ -606,6 +609,31 @@ def run_ncu_case(case: str) -> int:
         for _ in range(2):
             kda.chunk_prefill(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
                               initial_state=x["S0"], chunk=64, workspace=ws)
+    elif case == "chunk16":
+        # the 16-token path on B=1, H=32, T=4096 (0.13 GB of inputs), two calls
+        w = WORKLOADS[2]
+        x = make_inputs(w, device="cuda", T=4096)
+        for _ in range(2):
+            kda.chunk_prefill(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                              initial_state=x["S0"], chunk=16)
+    elif case == "segmented":
+        # the segment-parallel pass on B=1, H=1, T=65536 (automatic segments), two calls
+        from dataclasses import replace
+        w = replace(WORKLOADS[2], H=1, seed=120)
+        x = make_inputs(w, device="cuda", T=65536)
+        for _ in range(2):
+            kda.chunk_prefill(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                              initial_state=x["S0"])
+    elif case == "spec":
+        # speculative verify then commit, B=256, H=32, T=16 draft tokens (0.54 GB of state), twice
+        from dataclasses import replace
+        w = replace(WORKLOADS[1], H=32, seed=116)
+        x = make_inputs(w, device="cuda", B=256, T=16)
+        st = make_inputs(WORKLOADS[3], device="cuda")["S0"]
+        n_acc = torch.full((256,), 16, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            kda.spec_verify(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], st)
+            kda.spec_commit(x["k"], x["v"], x["z"], x["beta"], x["A"], st, n_acc)
     else:
         w = WORKLOADS[3]
         x = make_inputs(w, device="cuda")
@@ -627,7 +655,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the speculative-decoding and checkpoint timings")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode"],
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "chunk16", "segmented", "spec"],
                     help="run a short fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
     if args.ncu_case:
