@@ -1694,38 +1694,60 @@ trans_pass_kernel(uint8_t* __restrict__ ws, float* __restrict__ Y_out, SeqMap ma
 
 // S_start(g + 1) = M_g S_start(g) + X_g for g = 0 .. G - 2 in fp32, per
 // (sequence, head, 8-column tile of S); S_start(0) is the initial state (zeros
-// when there is none).  Each step stages M_g in shared memory (row pitch 132
-// floats) and every thread forms one row c times four columns.
+// when there is none).  M_g and this tile of X_g are staged in shared memory
+// (M rows at a pitch of 132 floats), two buffers deep: the copies of step g + 1
+// (cp.async, each thread its own 16-byte pieces) run while step g multiplies,
+// so no step waits on global memory.  Every thread forms one row c times four
+// columns.
 constexpr int kCombCols = 8;
 constexpr int kMPitch = 132;
-constexpr uint32_t COMB_SMEM = (128 * kMPitch + 128 * kCombCols) * 4;
+constexpr uint32_t COMB_BUF = 128 * kMPitch + 128 * kCombCols;           // floats per buffer
+constexpr uint32_t COMB_SMEM = (2 * COMB_BUF + 128 * kCombCols) * 4;
+
+__device__ __forceinline__ void comb_issue(float* buf, const float* Yg, int dk, int j0, int tid) {
+    float* Ms = buf;
+    float* Xs = buf + 128 * kMPitch;
+    for (int i = tid; i < 128 * 32; i += 256) {
+        const int row = i >> 5, c4 = i & 31;
+        if (row < dk && 4 * c4 < dk)
+            cp_async16(Ms + row * kMPitch + 4 * c4, Yg + (size_t)row * SEG_Y_COLS + 128 + 4 * c4, 16);
+    }
+    {   // X_g[c][j0 .. j0 + 7]: two 16-byte pieces per row, one per thread
+        const int row = tid >> 1, half = tid & 1;
+        if (row < dk) cp_async16(Xs + row * kCombCols + 4 * half, Yg + (size_t)row * SEG_Y_COLS + j0 + 4 * half, 16);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(256)
 seg_combine_kernel(const float* __restrict__ Y, const float* __restrict__ S0,
                    float* __restrict__ S_start, int H, int dk, int dv, int G) {
     const int j0 = blockIdx.x * kCombCols, n = blockIdx.y, h = blockIdx.z, tid = threadIdx.x;
     extern __shared__ float comb_smem[];
-    float* Ms = comb_smem;                        // M_g [128][kMPitch]
-    float* cur = comb_smem + 128 * kMPitch;       // S_start(g) [128][8]
+    float* cur = comb_smem + 2 * COMB_BUF;                      // S_start(g) [128][8]
     const int c = tid >> 1, jq = 4 * (tid & 1);
     const bool row_ok = c < dk;
+    auto Yof = [&](int g) { return Y + (((size_t)n * H + h) * (G - 1) + g) * 128 * SEG_Y_COLS; };
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (S0 && row_ok)
         s = *reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * dk + c) * dv + j0 + jq);
     *reinterpret_cast<float4*>(cur + c * kCombCols + jq) = s;
+    if (G > 1) comb_issue(comb_smem, Yof(0), dk, j0, tid);
     for (int g = 0; g + 1 < G; ++g) {
-        const float* Yg = Y + (((size_t)n * H + h) * (G - 1) + g) * 128 * SEG_Y_COLS;
-        for (int i = tid; i < 128 * 32; i += 256) {
-            const int row = i >> 5, c4 = i & 31;
-            if (row < dk && 4 * c4 < dk)
-                *reinterpret_cast<float4*>(Ms + row * kMPitch + 4 * c4) =
-                    *reinterpret_cast<const float4*>(Yg + (size_t)row * SEG_Y_COLS + 128 + 4 * c4);
+        float* buf = comb_smem + (g & 1) * COMB_BUF;
+        // step g + 1's copies go to the other buffer, whose last reader (step
+        // g - 1) is behind the barrier that closed that step
+        if (g + 2 < G) {
+            comb_issue(comb_smem + ((g + 1) & 1) * COMB_BUF, Yof(g + 1), dk, j0, tid);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
+        __syncthreads();                          // M_g, X_g and S_start(g) in place
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row_ok) acc = *reinterpret_cast<const float4*>(Yg + (size_t)c * SEG_Y_COLS + j0 + jq);
-        __syncthreads();                          // M_g and S_start(g) in place
         if (row_ok) {
-            const float* mrow = Ms + c * kMPitch;
+            acc = *reinterpret_cast<const float4*>(buf + 128 * kMPitch + c * kCombCols + jq);
+            const float* mrow = buf + c * kMPitch;
             for (int cp = 0; cp < dk; cp += 4) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -1738,7 +1760,7 @@ seg_combine_kernel(const float* __restrict__ Y, const float* __restrict__ S0,
                 }
             }
         }
-        __syncthreads();                          // every read of M_g and S_start(g) done
+        __syncthreads();                          // every read of step g's buffers and S_start(g) done
         *reinterpret_cast<float4*>(cur + c * kCombCols + jq) = acc;
         if (row_ok)
             *reinterpret_cast<float4*>(S_start + ((((size_t)n * H + h) * (G - 1) + g) * dk + c) * dv +
