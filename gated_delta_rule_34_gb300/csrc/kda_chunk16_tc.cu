@@ -108,10 +108,6 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
     for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(b[e]);
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
 // 8 bf16 of row `row` of a [T_total][H][d] tensor, channels 8 c8 .. (zeros past d).
 __device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int64_t row, int H, int h,
                                        int d, int c8) {
@@ -201,23 +197,13 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
         const bool live = tt < len;
 
-        // ---- inputs of token tt, channels 8 c8 .. 8 c8 + 7; gate -> gs.  The
-        //      same pieces of the next chunk are asked into L1 meanwhile.
+        // ---- inputs of token tt, channels 8 c8 .. 8 c8 + 7; gate -> gs
         uint4 kr = make_uint4(0, 0, 0, 0), qr = kr, vr = kr, zr = kr;
         if (live) {
             kr = load8(k, t0 + tt, H, h, dk, c8);
             qr = load8(q, t0 + tt, H, h, dk, c8);
             vr = load8(v, t0 + tt, H, h, dv, c8);
             zr = load8(z, t0 + tt, H, h, dk, c8);
-        }
-        if (t0 + kC + tt < eos) {
-            const size_t rn = (size_t)(t0 + kC + tt) * H + h;
-            if (8 * c8 < dk) {
-                prefetch_l1(k + rn * dk + 8 * c8);
-                prefetch_l1(q + rn * dk + 8 * c8);
-                prefetch_l1(z + rn * dk + 8 * c8);
-            }
-            if (8 * c8 < dv) prefetch_l1(v + rn * dv + 8 * c8);
         }
         if (tid < kC)
             bs[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
