@@ -21,18 +21,24 @@
 // which is the recurrence unrolled over the chunk (the same algebra as the
 // 64-token path, without its cross-block factoring).
 //
-// One CTA of eight warps per (sequence, head) walks the chunks in order.  All
-// products are arranged so that TMEM lane = state column j (or channel c), so
-// the fp32 state lives in registers as S^T[j][c] (thread = lane j, one half of
-// the channels per warp group) and its bf16 copy is written row by row:
+// One CTA of sixteen warps per (sequence, head) walks the chunks in order, in
+// two warp groups: the preparation group (warps 0-7) builds, for the next
+// chunk, everything that does not depend on the state (gate, scan, operands,
+// A/P, the solve, W and U~), while the chain group (warps 8-15) runs the
+// current chunk's state products and update.  They hand chunks over through
+// double-buffered operands and two mbarriers (ready: prepared; freed: the
+// chain has consumed the buffers).  All products are arranged so that TMEM
+// lane = state column j (or channel c), so the fp32 state lives in registers
+// as S^T[j][c] (thread = lane j, one half of the channels per warp quartet)
+// and its bf16 copy is written row by row:
 //   A/P    D[t][s]   = [kE ; qE] (k/E)^T           M=64  N=16  K=128
 //   W^T    D[c][t]   = (b kE)^T T^T                M=128 N=16  K=16   (A MN-major)
 //   U~^T   D[j][t]   = (b V)^T T^T                 M=128 N=16  K=16   (A MN-major)
 //   S^T W^T, S^T (qE)^T  D[j][t] = S^T [W ; qE]^T  M=128 N=32  K=128
 //   O^T   += U^T P^T                               M=128 N=16  K=16
 //   D[j][c] = U^T (k lam / E)                      M=128 N=128 K=16   (B MN-major)
-// and the fp32 update S^T <- S^T Diag(lam) + D on the registers.  The chunk
-// needs no workspace beyond the status word; two CTAs share an SM.
+// and the fp32 update S^T <- S^T Diag(lam) + D on the registers.  The path
+// needs no workspace beyond the status word.
 #include <cuda_bf16.h>
 
 #include "kda_common.cuh"
@@ -45,34 +51,37 @@ namespace c16 {
 using namespace tc;
 
 constexpr int kC = 16;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kGroup = 256;             // threads per warp group
+constexpr uint32_t kBarPrep = 1, kBarChain = 2;   // named barriers of the two groups
 
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr uint32_t R_ST = 0;          // S^T bf16 [128 j][128 c]: two K-blocks of 16 KB, swizzled
-constexpr uint32_t R_UT = 32768;      // U^T bf16 [128 j][16 t] (128-byte rows, K = 16 used)
-constexpr uint32_t R_APA = 49152;     // [kE ; qE ; 0] [64 rows][128 c]: two K-blocks of 8 KB
-constexpr uint32_t R_APB = 65536;     // k/E [16 s][128 c]: two K-blocks of 2 KB
-constexpr uint32_t R_SB = 69632;      // [W ; qE] [32 rows][128 c]: two K-blocks of 4 KB
-constexpr uint32_t R_BKG = 77824;     // b kE token rows, two 64-channel halves of 2 KB (MN-major)
-constexpr uint32_t R_BV = 81920;      // b V token rows, same layout
-constexpr uint32_t R_KC = 86016;      // k lam / E token rows, same layout
-constexpr uint32_t R_PB = 90112;      // P [16 t][16 s] (128-byte rows)
-constexpr uint32_t R_TB = 92160;      // T [16 t][16 s] (128-byte rows)
-constexpr uint32_t R_GS = 94208;      // g, then L: fp32 [16 t][128 c]
-constexpr uint32_t R_AF = 102400;     // A fp32 [16][17]
-constexpr uint32_t R_LAM = 103680;    // lam [128] fp32
-constexpr uint32_t R_EA = 104192;     // e^{A_h} [128] fp32
-constexpr uint32_t R_BETA = 104704;   // beta [16] fp32
-constexpr uint32_t R_BAR = 104768;    // mbarrier, TMEM slot
+// shared memory (offsets from a 1024-byte aligned base); [P] preparation group
+// only, [C] chain group only, [P->C] double-buffered hand-over (buffer ci & 1)
+constexpr uint32_t R_ST = 0;          // [C] S^T bf16 [128 j][128 c]: two K-blocks of 16 KB, swizzled
+constexpr uint32_t R_UT = 32768;      // [C] U^T bf16 [128 j][16 t] (128-byte rows, K = 16 used)
+constexpr uint32_t R_APA = 49152;     // [P] [kE ; qE ; 0] [64 rows][128 c]: two K-blocks of 8 KB
+constexpr uint32_t R_APB = 65536;     // [P] k/E [16 s][128 c]: two K-blocks of 2 KB
+constexpr uint32_t R_SB = 69632;      // [P->C] [W ; qE] [32 rows][128 c]: two K-blocks of 4 KB; x2
+constexpr uint32_t R_BKG = 86016;     // [P] b kE token rows, two 64-channel halves of 2 KB (MN-major)
+constexpr uint32_t R_BV = 90112;      // [P] b V token rows, same layout
+constexpr uint32_t R_KC = 94208;      // [P->C] k lam / E token rows, same layout; x2
+constexpr uint32_t R_PB = 102400;     // [P->C] P [16 t][16 s] (128-byte rows); x2
+constexpr uint32_t R_TB = 106496;     // [P] T [16 t][16 s] (128-byte rows)
+constexpr uint32_t R_GS = 108544;     // [P] g, then L: fp32 [16 t][128 c]
+constexpr uint32_t R_AF = 116736;     // [P] A fp32 [16][17]
+constexpr uint32_t R_LAM = 118016;    // [P->C] lam [128] fp32; x2
+constexpr uint32_t R_EA = 119040;     // [P] e^{A_h} [128] fp32
+constexpr uint32_t R_BETA = 119552;   // [P] beta [16] fp32
+constexpr uint32_t R_BAR = 119616;    // mbarriers (prep MMA, chain MMA, ready x2, freed x2), TMEM slot
 constexpr uint32_t SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
-static_assert(SMEM * 2 <= 232448, "two CTAs per SM");
+static_assert(SMEM <= 232448, "shared memory");
 
 // TMEM columns
-constexpr uint32_t T_AP = 0;      // A/P (M=64 layout: row r in lane 32 (r / 16) + r mod 16)
-constexpr uint32_t T_WT = 16;     // W^T
-constexpr uint32_t T_UT = 32;     // U~^T
-constexpr uint32_t T_ST = 64;     // [(W S)^T | O^T]
-constexpr uint32_t T_SU = 128;    // U^T (k lam / E)
+constexpr uint32_t T_AP = 0;      // [P] A/P (M=64 layout: row r in lane 32 (r / 16) + r mod 16)
+constexpr uint32_t T_WT = 16;     // [P] W^T
+constexpr uint32_t T_UT = 32;     // [P->C] U~^T, two buffers of 16
+constexpr uint32_t T_ST = 64;     // [C] [(W S)^T | O^T]
+constexpr uint32_t T_SU = 128;    // [C] U^T (k lam / E)
 constexpr uint32_t kTmemCols = 256;
 
 constexpr uint32_t kErrWait = 8u;   // status bit: a bounded wait gave up
@@ -81,13 +90,27 @@ __device__ __forceinline__ uint32_t idesc_bmn(uint32_t M, uint32_t N) {
     return idesc_bf16(M, N) | (1u << 16);   // B MN-major
 }
 
-// Waits (bounded) for the next phase of `bar` and makes the whole CTA agree on
-// the outcome.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
-    const bool ok = mbar_wait(bar, phase);
-    phase ^= 1u;
+// Barrier over one warp group (named barrier `id`, kGroup threads) that also
+// returns whether every thread of the group passed ok.
+__device__ __forceinline__ bool group_and(uint32_t id, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(id), "n"(kGroup)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity, agreed on by the
+// whole warp group.
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, uint32_t id) {
+    const bool ok = mbar_wait(bar, parity);
     tc_fence_after();
-    return __syncthreads_and(ok) != 0;
+    return group_and(id, ok);
 }
 
 // Stores 8 bf16 values (channels 8 c8 .. 8 c8 + 7) as token row t of a [rows][128]
@@ -115,7 +138,7 @@ __device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int6
     return __ldg(reinterpret_cast<const uint4*>(x + ((size_t)row * H + h) * d + 8 * c8));
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
                const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
@@ -128,25 +151,29 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float* gs = reinterpret_cast<float*>(sm + R_GS);
     float* af = reinterpret_cast<float*>(sm + R_AF);
-    float* lam = reinterpret_cast<float*>(sm + R_LAM);
     float* ea = reinterpret_cast<float*>(sm + R_EA);
     float* bs = reinterpret_cast<float*>(sm + R_BETA);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + R_BAR);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 8);
+    uint64_t* bar_p = reinterpret_cast<uint64_t*>(sm + R_BAR);
+    uint64_t* bar_c = bar_p + 1;
+    uint64_t* ready = bar_p + 2;     // [2]
+    uint64_t* freed = bar_p + 4;     // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 48);
 
     int64_t bos, eos;
     seq_bounds(cu, n, T_len, T_total, bos, eos);
     const int64_t len_seq = eos - bos;
-
-    // Thread roles.  Row-side phases: token t = tid / 16, channels 8 c8 .. + 7.
-    // State phases: lane j = 32 (warp mod 4) + lane, channel half ch = warp / 4.
-    const int tt = tid >> 4, c8 = tid & 15;
-    const int j = 32 * (warp & 3) + lane, ch = warp >> 2;
+    const int nchunks = (int)((len_seq + kC - 1) / kC);
+    const bool prep = tid < kGroup;
     const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;   // TMEM lane field of this warp
 
     if (warp == 0) tmem_alloc<kTmemCols>(tslot);
     if (tid == 32) {
-        mbar_init(bar, 1);
+        mbar_init(bar_p, 1);
+        mbar_init(bar_c, 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(ready + p, 1);
+            mbar_init(freed + p, 1);
+        }
         fence_mbar_init();
     }
     // Rows 32..63 of the A/P operand stay zero; e^A of the head.
@@ -154,14 +181,12 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         reinterpret_cast<uint32_t*>(sm + R_APA)[i] = 0u;
     if (tid < 128) ea[tid] = tid < dk ? __expf(A[(size_t)h * dk + tid]) : 0.f;
 
+    // Chain group: lane j = 32 (warp mod 4) + lane, channel half ch; it holds
     // S^T[j][64 ch .. 64 ch + 63] in fp32 registers.
+    const int cw = warp - 8;
+    const int j = 32 * (warp & 3) + lane, ch = (cw >> 2) & 1;
     const size_t smat = ((size_t)n * H + h) * dk * dv;
     float st[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) {
-        const int c = 64 * ch + e;
-        st[e] = (S0 && c < dk && j < dv) ? __ldg(S0 + smat + (size_t)c * dv + j) : 0.f;
-    }
     auto write_st = [&]() {
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
@@ -182,267 +207,313 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
             }
         }
     };
-    write_st();
+    if (!prep) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const int c = 64 * ch + e;
+            st[e] = (S0 && c < dk && j < dv) ? __ldg(S0 + smat + (size_t)c * dv + j) : 0.f;
+        }
+        write_st();
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    uint32_t phase = 0;
     bool ok = true;
 
-    const int nchunks = (int)((len_seq + kC - 1) / kC);
-    for (int ci = 0; ci < nchunks && ok; ++ci) {
-        const int64_t t0 = bos + (int64_t)ci * kC;
-        const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
-        const bool live = tt < len;
-
-        // ---- inputs of token tt, channels 8 c8 .. 8 c8 + 7; gate -> gs
+    if (prep) {
+        // ============================================ preparation group
+        const int tt = tid >> 4, c8 = tid & 15;   // token tt, channels 8 c8 .. + 7
+        uint32_t phase = 0;
+        // inputs of chunk ci, loaded one chunk ahead
         uint4 kr = make_uint4(0, 0, 0, 0), qr = kr, vr = kr, zr = kr;
-        if (live) {
-            kr = load8(k, t0 + tt, H, h, dk, c8);
-            qr = load8(q, t0 + tt, H, h, dk, c8);
-            vr = load8(v, t0 + tt, H, h, dv, c8);
-            zr = load8(z, t0 + tt, H, h, dk, c8);
-        }
-        if (tid < kC)
-            bs[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
-        {
-            float zf[8], g[8];
-            unpack8(zr, zf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = 8 * c8 + e;
-                g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
-            }
-            float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
-            gp[0] = make_float4(g[0], g[1], g[2], g[3]);
-            gp[1] = make_float4(g[4], g[5], g[6], g[7]);
-        }
-        __syncthreads();
-        // ---- L = running sum over the chunk, per channel; lam = e^{L_last}
-        if (tid < 128) {
-            float run = 0.f;
-#pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                run += gs[t * 128 + tid];
-                gs[t * 128 + tid] = run;
-            }
-            lam[tid] = __expf(run);
-        }
-        __syncthreads();
+        float bnext = 0.f;
+        auto load_inputs = [&](int ci) {
+            const int64_t t0 = bos + (int64_t)ci * kC;
+            const bool live = t0 + tt < eos;
+            kr = live ? load8(k, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+            qr = live ? load8(q, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+            vr = live ? load8(v, t0 + tt, H, h, dv, c8) : make_uint4(0, 0, 0, 0);
+            zr = live ? load8(z, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+            if (tid < kC) bnext = t0 + tid < eos ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+        };
+        if (nchunks > 0) load_inputs(0);
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int p = ci & 1;
+            const int64_t t0 = bos + (int64_t)ci * kC;
+            const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
+            const bool live = tt < len;
+            uint8_t* sb = sm + R_SB + p * 8192;
+            uint8_t* kc = sm + R_KC + p * 4096;
+            uint8_t* pb = sm + R_PB + p * 2048;
+            float* lam = reinterpret_cast<float*>(sm + R_LAM + p * 512);
+            // buffers p were last used for chunk ci - 2
+            if (ci >= 2 && !(ok = group_wait(freed + p, ((ci - 2) >> 1) & 1, kBarPrep))) break;
 
-        // ---- decay-scaled operands of token tt (bf16)
-        {
-            float kf[8], qf[8], vf[8], E[8], R[8], o8[8];
-            unpack8(kr, kf);
-            unpack8(qr, qf);
-            unpack8(vr, vf);
-            const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
-            const float4 l0 = lp[0], l1 = lp[1];
-            const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+            // ---- gate -> gs (zeros past the chunk and past d_k)
+            {
+                float zf[8], g[8];
+                unpack8(zr, zf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                E[e] = __expf(L[e]);
-                R[e] = __fdividef(1.0f, E[e]);
+                for (int e = 0; e < 8; ++e) {
+                    const int c = 8 * c8 + e;
+                    g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+                }
+                float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
+                gp[0] = make_float4(g[0], g[1], g[2], g[3]);
+                gp[1] = make_float4(g[4], g[5], g[6], g[7]);
+                if (tid < kC) bs[tid] = bnext;
             }
-            const float bt = bs[tt];
+            named_bar_sync(kBarPrep, kGroup);
+            // ---- L = running sum over the chunk, per channel; lam = e^{L_last}
+            if (tid < 128) {
+                float run = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
-            store_row8(sm + R_APA, 8192, tt, c8, o8);                           // k E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
-            store_row8(sm + R_BKG, 2048, tt, c8, o8);                           // b k E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
-            store_row8(sm + R_APA, 8192, 16 + tt, c8, o8);                      // q E
-            store_row8(sm + R_SB, 4096, 16 + tt, c8, o8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * R[e];
-            store_row8(sm + R_APB, 2048, tt, c8, o8);                           // k / E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = o8[e] * lam[8 * c8 + e];
-            store_row8(sm + R_KC, 2048, tt, c8, o8);                            // k lam / E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
-            store_row8(sm + R_BV, 2048, tt, c8, o8);                            // b V
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+                for (int t = 0; t < kC; ++t) {
+                    run += gs[t * 128 + tid];
+                    gs[t * 128 + tid] = run;
+                }
+                lam[tid] = __expf(run);
+            }
+            named_bar_sync(kBarPrep, kGroup);
 
-        // ---- A and P: D[t][s] = [kE ; qE] (k/E)^T, M=64 N=16 K=128
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(64, 16);
+            // ---- decay-scaled operands of token tt (bf16)
+            {
+                float kf[8], qf[8], vf[8], E[8], R[8], o8[8];
+                unpack8(kr, kf);
+                unpack8(qr, qf);
+                unpack8(vr, vf);
+                const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
+                const float4 l0 = lp[0], l1 = lp[1];
+                const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + R_APA + kb * 8192 + off)),
-                         desc_sw128(smem_u32(sm + R_APB + kb * 2048 + off)), idesc, ks > 0);
+                for (int e = 0; e < 8; ++e) {
+                    E[e] = __expf(L[e]);
+                    R[e] = __fdividef(1.0f, E[e]);
+                }
+                const float bt = bs[tt];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+                store_row8(sm + R_APA, 8192, tt, c8, o8);                           // k E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
+                store_row8(sm + R_BKG, 2048, tt, c8, o8);                           // b k E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+                store_row8(sm + R_APA, 8192, 16 + tt, c8, o8);                      // q E
+                store_row8(sb, 4096, 16 + tt, c8, o8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * R[e];
+                store_row8(sm + R_APB, 2048, tt, c8, o8);                           // k / E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = o8[e] * lam[8 * c8 + e];
+                store_row8(kc, 2048, tt, c8, o8);                                   // k lam / E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
+                store_row8(sm + R_BV, 2048, tt, c8, o8);                            // b V
             }
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        // rows 0..15 (A, lanes 0..15 of warp 0), rows 16..31 (P, lanes 32..47 of warp 1)
-        if (warp < 2) {
-            float d[16];
-            tmem_ld16(tbase + tl + T_AP, d);
-            tmem_wait_ld();
-            if (lane < kC) {
-                const int t = lane;
-                if (warp == 0) {
-                    const float bt = bs[t];
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarPrep, kGroup);
+            tc_fence_after();
+
+            // ---- A and P: D[t][s] = [kE ; qE] (k/E)^T, M=64 N=16 K=128
+            if (tid == 0) {
+                const uint32_t idesc = idesc_bf16(64, 16);
 #pragma unroll
-                    for (int s = 0; s < kC; ++s) af[t * 17 + s] = s < t ? bt * d[s] : 0.f;
-                } else {
-                    float p8[8];
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + R_APA + kb * 8192 + off)),
+                             desc_sw128(smem_u32(sm + R_APB + kb * 2048 + off)), idesc, ks > 0);
+                }
+                mma_commit(bar_p);
+            }
+            ok = group_wait(bar_p, phase, kBarPrep);
+            phase ^= 1u;
+            if (!ok) break;
+            // rows 0..15 (A, lanes 0..15 of warp 0), rows 16..31 (P, lanes 32..47 of warp 1)
+            if (warp < 2) {
+                float d[16];
+                tmem_ld16(tbase + tl + T_AP, d);
+                tmem_wait_ld();
+                if (lane < kC) {
+                    const int t = lane;
+                    if (warp == 0) {
+                        const float bt = bs[t];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                        for (int s2 = 0; s2 < kC; ++s2) af[t * 17 + s2] = s2 < t ? bt * d[s2] : 0.f;
+                    } else {
+                        float p8[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
-                        uint4 r;
-                        r.x = pack_bf16x2(p8[0], p8[1]);
-                        r.y = pack_bf16x2(p8[2], p8[3]);
-                        r.z = pack_bf16x2(p8[4], p8[5]);
-                        r.w = pack_bf16x2(p8[6], p8[7]);
-                        *reinterpret_cast<uint4*>(sm + R_PB + sw128(t, hh)) = r;
+                        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
+                            uint4 r;
+                            r.x = pack_bf16x2(p8[0], p8[1]);
+                            r.y = pack_bf16x2(p8[2], p8[3]);
+                            r.z = pack_bf16x2(p8[4], p8[5]);
+                            r.w = pack_bf16x2(p8[6], p8[7]);
+                            *reinterpret_cast<uint4*>(pb + sw128(t, hh)) = r;
+                        }
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
+            tc_fence_before();
+            named_bar_sync(kBarPrep, kGroup);
 
-        // ---- T = (I + A)^{-1}: column jc by forward substitution (16 threads)
-        if (tid < kC) {
-            const int jc = tid;
-            float x[kC];
+            // ---- T = (I + A)^{-1}: column jc by forward substitution (16 threads)
+            if (tid < kC) {
+                const int jc = tid;
+                float x[kC];
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                float acc = 0.f;
+                for (int r = 0; r < kC; ++r) {
+                    float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
-                x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+                    for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
+                    x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+                }
+#pragma unroll
+                for (int r = 0; r < kC; ++r)
+                    *reinterpret_cast<__nv_bfloat16*>(sm + R_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
+                        __float2bfloat16_rn(x[r]);
             }
-            // T[r][jc] -> row r, element jc of the K-major [t][s] operand
-#pragma unroll
-            for (int r = 0; r < kC; ++r)
-                *reinterpret_cast<__nv_bfloat16*>(sm + R_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
-                    __float2bfloat16_rn(x[r]);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarPrep, kGroup);
+            tc_fence_after();
 
-        // ---- W^T = (b kE)^T T^T and U~^T = (b V)^T T^T (M=128 N=16 K=16, A MN-major)
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16_amn(128, 16);
-            const uint64_t tb = desc_sw128(smem_u32(sm + R_TB));
-            mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + R_BKG), 2048, 1024), tb, idesc, false);
-            mma_bf16(tbase + T_UT, desc_sw128_mn(smem_u32(sm + R_BV), 2048, 1024), tb, idesc, false);
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        // W rows t of the [W ; qE] operand: lane c of warps 0..3 writes column c
-        if (warp < 4) {
-            float w[16];
-            tmem_ld16(tbase + tl + T_WT, w);
-            tmem_wait_ld();
-            const int c = j;
-#pragma unroll
-            for (int t = 0; t < kC; ++t)
-                *reinterpret_cast<__nv_bfloat16*>(sm + R_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
-                                                   (c & 7) * 2) = __float2bfloat16_rn(w[t]);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T, M=128 N=32 K=128
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 32);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + R_ST + kb * 16384 + off)),
-                         desc_sw128(smem_u32(sm + R_SB + kb * 4096 + off)), idesc, ks > 0);
+            // ---- W^T = (b kE)^T T^T and U~^T = (b V)^T T^T (M=128 N=16 K=16, A MN-major)
+            if (tid == 0) {
+                const uint32_t idesc = idesc_bf16_amn(128, 16);
+                const uint64_t tb = desc_sw128(smem_u32(sm + R_TB));
+                mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + R_BKG), 2048, 1024), tb, idesc, false);
+                mma_bf16(tbase + T_UT + 16 * p, desc_sw128_mn(smem_u32(sm + R_BV), 2048, 1024), tb, idesc,
+                         false);
+                mma_commit(bar_p);
             }
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        // U^T[j][s] = U~^T[j][s] - (W S)^T[j][s] -> bf16 row j
-        if (warp < 4) {
-            float ws_[16], ut[16];
-            tmem_ld16(tbase + tl + T_ST, ws_);
-            tmem_ld16(tbase + tl + T_UT, ut);
-            tmem_wait_ld();
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint4 r;
-                r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
-                r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
-                r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
-                r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
-                *reinterpret_cast<uint4*>(sm + R_UT + sw128(j, hh)) = r;
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-
-        // ---- O^T += U^T P^T (M=128 N=16 K=16); D = U^T (k lam / E) (M=128 N=128 K=16, B MN-major)
-        if (tid == 0) {
-            const uint64_t ua = desc_sw128(smem_u32(sm + R_UT));
-            mma_bf16(tbase + T_ST + 16, ua, desc_sw128(smem_u32(sm + R_PB)), idesc_bf16(128, 16), true);
-            mma_bf16(tbase + T_SU, ua, desc_sw128_mn(smem_u32(sm + R_KC), 2048, 1024), idesc_bmn(128, 128),
-                     false);
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-
-        // ---- outputs o[t0 + t][h][j] = O^T[j][t] (warps 0..3; the TMEM load is
-        //      warp-collective, so every lane takes it and only the stores are masked)
-        if (warp < 4) {
-            float ov[16];
-            tmem_ld16(tbase + tl + T_ST + 16, ov);
-            tmem_wait_ld();
-            if (j < dv) {
+            ok = group_wait(bar_p, phase, kBarPrep);
+            phase ^= 1u;
+            if (!ok) break;
+            // W rows t of the [W ; qE] operand: lane c of warps 0..3 writes column c
+            if (warp < 4) {
+                float w[16];
+                tmem_ld16(tbase + tl + T_WT, w);
+                tmem_wait_ld();
+                const int c = 32 * warp + lane;
 #pragma unroll
                 for (int t = 0; t < kC; ++t)
-                    if (t < len) o[((size_t)(t0 + t) * H + h) * dv + j] = __float2bfloat16_rn(ov[t]);
+                    *reinterpret_cast<__nv_bfloat16*>(sb + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
+                                                       (c & 7) * 2) = __float2bfloat16_rn(w[t]);
             }
+            // the next chunk's inputs, in flight while the chain takes this one
+            if (ci + 1 < nchunks) load_inputs(ci + 1);
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarPrep, kGroup);
+            if (tid == 0) mbar_arrive(ready + p);
         }
-        // ---- S^T <- S^T Diag(lam) + D, then its bf16 copy
+    } else {
+        // ================================================== chain group
+        uint32_t phase = 0;
+        const bool lead = tid == kGroup;          // issues the chain's products
+        for (int ci = 0; ci < nchunks; ++ci) {
+            const int p = ci & 1;
+            const int64_t t0 = bos + (int64_t)ci * kC;
+            const int len = (int)((eos - t0) < kC ? (eos - t0) : kC);
+            const uint8_t* sb = sm + R_SB + p * 8192;
+            const uint8_t* kc = sm + R_KC + p * 4096;
+            const uint8_t* pb = sm + R_PB + p * 2048;
+            const float* lam = reinterpret_cast<const float*>(sm + R_LAM + p * 512);
+            if (!(ok = group_wait(ready + p, (ci >> 1) & 1, kBarChain))) break;
+
+            // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T, M=128 N=32 K=128
+            if (lead) {
+                const uint32_t idesc = idesc_bf16(128, 32);
 #pragma unroll
-        for (int q16 = 0; q16 < 4; ++q16) {
-            float d[16];
-            tmem_ld16(tbase + tl + T_SU + 64 * ch + 16 * q16, d);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int idx = 16 * q16 + e;
-                st[idx] = fmaf(lam[64 * ch + idx], st[idx], d[e]);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + R_ST + kb * 16384 + off)),
+                             desc_sw128(smem_u32(sb + kb * 4096 + off)), idesc, ks > 0);
+                }
+                mma_commit(bar_c);
             }
+            ok = group_wait(bar_c, phase, kBarChain);
+            phase ^= 1u;
+            if (!ok) break;
+            // U^T[j][s] = U~^T[j][s] - (W S)^T[j][s] -> bf16 row j (warps 8..11)
+            if (cw < 4) {
+                float ws_[16], ut[16];
+                tmem_ld16(tbase + tl + T_ST, ws_);
+                tmem_ld16(tbase + tl + T_UT + 16 * p, ut);
+                tmem_wait_ld();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint4 r;
+                    r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
+                    r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
+                    r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
+                    r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
+                    *reinterpret_cast<uint4*>(sm + R_UT + sw128(j, hh)) = r;
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarChain, kGroup);
+            tc_fence_after();
+
+            // ---- O^T += U^T P^T (M=128 N=16 K=16); D = U^T (k lam / E) (M=128 N=128 K=16, B MN-major)
+            if (lead) {
+                const uint64_t ua = desc_sw128(smem_u32(sm + R_UT));
+                mma_bf16(tbase + T_ST + 16, ua, desc_sw128(smem_u32(pb)), idesc_bf16(128, 16), true);
+                mma_bf16(tbase + T_SU, ua, desc_sw128_mn(smem_u32(kc), 2048, 1024), idesc_bmn(128, 128), false);
+                mma_commit(bar_c);
+            }
+            ok = group_wait(bar_c, phase, kBarChain);
+            phase ^= 1u;
+            if (!ok) break;
+
+            // ---- outputs o[t0 + t][h][j] = O^T[j][t] (warps 8..11; the TMEM load is
+            //      warp-collective, so every lane takes it and only the stores are masked)
+            if (cw < 4) {
+                float ov[16];
+                tmem_ld16(tbase + tl + T_ST + 16, ov);
+                tmem_wait_ld();
+                if (j < dv) {
+#pragma unroll
+                    for (int t = 0; t < kC; ++t)
+                        if (t < len) o[((size_t)(t0 + t) * H + h) * dv + j] = __float2bfloat16_rn(ov[t]);
+                }
+            }
+            // ---- S^T <- S^T Diag(lam) + D, then its bf16 copy
+#pragma unroll
+            for (int q16 = 0; q16 < 4; ++q16) {
+                float d[16];
+                tmem_ld16(tbase + tl + T_SU + 64 * ch + 16 * q16, d);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int idx = 16 * q16 + e;
+                    st[idx] = fmaf(lam[64 * ch + idx], st[idx], d[e]);
+                }
+            }
+            write_st();
+            if (ck.out) {
+                const int64_t done = (int64_t)(ci + 1) * kC;
+                if (done <= len_seq && done % ck.every == 0 && done / ck.every <= ck.max_count)
+                    store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarChain, kGroup);
+            // the chunk's hand-over buffers are consumed
+            if (lead) mbar_arrive(freed + p);
         }
-        write_st();
-        if (ck.out) {
-            const int64_t done = (int64_t)(ci + 1) * kC;
-            if (done <= len_seq && done % ck.every == 0 && done / ck.every <= ck.max_count)
-                store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
-    if (!ok && tid == 0) atomicOr(status, kErrWait);
-    if (S1) store_state(S1 + smat);
+    if (!ok) atomicOr(status, kErrWait);
     tc_fence_before();
     __syncthreads();
+    if (!prep && S1) store_state(S1 + smat);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc<kTmemCols>(tbase);
