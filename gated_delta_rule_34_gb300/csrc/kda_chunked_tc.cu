@@ -167,8 +167,7 @@ constexpr uint32_t S_ST = kStages * ST_BYTES;      // 2 x S^T tile [32 j][128 c]
 constexpr uint32_t S_BAR = S_ST + 2 * 8192;
 constexpr uint32_t S_SMEM = S_BAR + 256;           // the dynamic base is 1024-aligned
 constexpr uint32_t kDBuf = 64;                     // per accumulator buffer: D_S, then D_O at +32
-constexpr uint32_t kDS2 = 2 * kDBuf;               // second half-sum of D_S, per buffer 32 columns
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 2 * kDBuf;
 constexpr int kL2Ahead = 6;                        // packages prefetched into L2 this far ahead
 
 static_assert(S_SMEM <= 232448, "state_pass shared memory");
@@ -1336,17 +1335,11 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
                 tc_fence_after();
                 const uint64_t bdesc0 = desc_sw128(smem_u32(sm + S_ST + b * 8192));
                 const uint64_t adesc0 = desc_sw128(smem_u32(sm + (cc % kStages) * ST_BYTES));
-                // the two K-blocks into two accumulators, interleaved, so that
-                // consecutive products do not depend on each other
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {
-                        const uint32_t off = i * 32;
-                        mma_bf16(kb == 0 ? tbase + b * kDBuf : tbase + kDS2 + b * 32,
-                                 adesc0 + ((kb * PKG_BK + off) >> 4), bdesc0 + ((kb * 4096 + off) >> 4),
-                                 idesc, i > 0);
-                    }
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + b * kDBuf, adesc0 + ((kb * PKG_BK + off) >> 4),
+                             bdesc0 + ((kb * 4096 + off) >> 4), idesc, ks > 0);
                 }
                 mma_commit(sdone + b);
             }
@@ -1437,14 +1430,10 @@ state_pass_kernel(const uint8_t* __restrict__ ws, __nv_bfloat16* __restrict__ o,
             ok = role_wait(sdone + b, (cc >> 1) & 1, abort) && ok;
             if (!ok) return false;
             tc_fence_after();
-            float d[16], d2[16];
+            float d[16];
             tmem_ld_16x256b_x2(tl + b * kDBuf, *reinterpret_cast<float(*)[8]>(d));
             tmem_ld_16x256b_x2(tl + (16u << 16) + b * kDBuf, *reinterpret_cast<float(*)[8]>(d + 8));
-            tmem_ld_16x256b_x2(tl + kDS2 + b * 32, *reinterpret_cast<float(*)[8]>(d2));
-            tmem_ld_16x256b_x2(tl + (16u << 16) + kDS2 + b * 32, *reinterpret_cast<float(*)[8]>(d2 + 8));
             tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) d[e] += d2[e];
             update_frag(st, d, xr, true);
             if (cc + 1 < nc) {
                 // S^T copy (cc + 1) & 1 is still read by chunk cc - 1's O product
