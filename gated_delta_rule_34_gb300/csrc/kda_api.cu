@@ -501,8 +501,13 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
     KDA_REQUIRE_PTR(state);
     KDA_REQUIRE_PTR(o);
     kda::profile_event(0, stream);
-    const cudaError_t e = kda::run_spec(q, k, v, z, beta, A, const_cast<float*>(state), o, nullptr,
-                                        B, T, H, d_k, d_v, dtype == KDA_DTYPE_BF16, true, stream);
+    // bf16 heads with d_k and d_v multiples of 16: the draft span is one
+    // 16-token chunk on the tensor cores; otherwise token by token in fp32.
+    const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0;
+    const cudaError_t e =
+        tc ? kda::run_spec_verify_tc(q, k, v, z, beta, A, state, o, B, T, H, d_k, d_v, stream)
+           : kda::run_spec(q, k, v, z, beta, A, const_cast<float*>(state), o, nullptr, B, T, H, d_k,
+                           d_v, dtype == KDA_DTYPE_BF16, true, stream);
     kda::profile_event(1, stream);
     return cuda_status(e, "kda_spec_verify launch");
 }

@@ -520,6 +520,306 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Speculative verify on the tensor cores (bf16 inputs).  The T <= 16 draft
+// tokens of one (b, h) are one chunk of the 16-token form above, taken from
+// the state S read once ("How Kimi K3 is built", section "How to serve two
+// different caches": the draft tokens' projections are kept and recomputed on
+// chip instead of a state copy per token).  With L_t, E, P, T, W and U~ as
+// above and S the state before the span:
+//   U = U~ - W S,   O = (q E) S + P U
+// One CTA of eight warps per (b, h), two per SM: the state's 64 values per
+// thread are loaded first and land while the gate, scan, operands, A/P, the
+// solve and W^T, U~^T run; then S^T (bf16) [W ; qE]^T, U^T and O^T += U^T P^T.
+// The state is only read.  A bounded wait that gives up leaves NaN in that
+// (b, h)'s outputs.
+// ---------------------------------------------------------------------------
+constexpr int kVThreads = 256;
+constexpr uint32_t V_ST = 0;          // S^T bf16 [128 j][128 c]: two K-blocks of 16 KB, swizzled
+constexpr uint32_t V_UT = 32768;      // U^T bf16 [128 j][16 t]
+constexpr uint32_t V_APA = 49152;     // [kE ; qE ; 0] [64 rows][128 c]
+constexpr uint32_t V_APB = 65536;     // k/E [16 s][128 c]
+constexpr uint32_t V_SB = 69632;      // [W ; qE] [32 rows][128 c]
+constexpr uint32_t V_BKG = 77824;     // b kE token rows (MN-major)
+constexpr uint32_t V_BV = 81920;      // b V token rows (MN-major)
+constexpr uint32_t V_PB = 86016;      // P [16 t][16 s]
+constexpr uint32_t V_TB = 88064;      // T [16 t][16 s]
+constexpr uint32_t V_GS = 90112;      // g, then L: fp32 [16 t][128 c]
+constexpr uint32_t V_AF = 98304;      // A fp32 [16][17]
+constexpr uint32_t V_EA = 99584;      // e^{A_h} [128]
+constexpr uint32_t V_BETA = 100096;   // beta [16]
+constexpr uint32_t V_BAR = 100160;    // mbarrier, TMEM slot
+constexpr uint32_t V_SMEM = V_BAR + 64 + 1024;
+static_assert(2 * (V_SMEM + 1024) <= 233472, "two verify CTAs per SM");
+constexpr uint32_t kVTmemCols = 128;
+
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
+    const bool ok = mbar_wait(bar, phase);
+    phase ^= 1u;
+    tc_fence_after();
+    return __syncthreads_and(ok) != 0;
+}
+
+__global__ void __launch_bounds__(kVThreads, 2)
+spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
+                   const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
+                   const float* __restrict__ state, __nv_bfloat16* __restrict__ o, int Tn, int H,
+                   int dk, int dv) {
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float* gs = reinterpret_cast<float*>(sm + V_GS);
+    float* af = reinterpret_cast<float*>(sm + V_AF);
+    float* ea = reinterpret_cast<float*>(sm + V_EA);
+    float* bs = reinterpret_cast<float*>(sm + V_BETA);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + V_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + V_BAR + 8);
+    const int tt = tid >> 4, c8 = tid & 15;               // token tt, channels 8 c8 .. + 7
+    const int j = 32 * (warp & 3) + lane, ch = warp >> 2;  // state column j, channel half ch
+    const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;
+
+    // The state read first: S[64 ch + e][j], landing during the preparation.
+    const float* Sbh = state + (size_t)bh * dk * dv;
+    float st[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+        const int c = 64 * ch + e;
+        st[e] = (c < dk && j < dv) ? __ldcs(Sbh + (size_t)c * dv + j) : 0.f;
+    }
+    const bool live = tt < Tn;
+    const int64_t row = (int64_t)b * Tn + tt;             // token row of [B, Tn, H, d]
+    const uint4 kr = live ? load8(k, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+    const uint4 qr = live ? load8(q, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+    const uint4 vr = live ? load8(v, row, H, h, dv, c8) : make_uint4(0, 0, 0, 0);
+    const uint4 zr = live ? load8(z, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+
+    if (warp == 0) tmem_alloc<kVTmemCols>(tslot);
+    if (tid == 32) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    for (int i = tid; i < 4096; i += kVThreads) reinterpret_cast<uint32_t*>(sm + V_APA)[i] = 0u;
+    if (tid < 128) ea[tid] = tid < dk ? __expf(A[(size_t)h * dk + tid]) : 0.f;
+    if (tid < kC) bs[tid] = tid < Tn ? __bfloat162float(beta[((size_t)b * Tn + tid) * H + h]) : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    uint32_t phase = 0;
+    bool ok = true;
+
+    do {
+        // ---- gate -> gs; running sum per channel
+        {
+            float zf[8], g[8];
+            unpack8(zr, zf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = 8 * c8 + e;
+                g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+            }
+            float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
+            gp[0] = make_float4(g[0], g[1], g[2], g[3]);
+            gp[1] = make_float4(g[4], g[5], g[6], g[7]);
+        }
+        __syncthreads();
+        if (tid < 128) {
+            float run = 0.f;
+#pragma unroll
+            for (int t = 0; t < kC; ++t) {
+                run += gs[t * 128 + tid];
+                gs[t * 128 + tid] = run;
+            }
+        }
+        __syncthreads();
+        // ---- decay-scaled operands of token tt
+        {
+            float kf[8], qf[8], vf[8], E[8], o8[8];
+            unpack8(kr, kf);
+            unpack8(qr, qf);
+            unpack8(vr, vf);
+            const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
+            const float4 l0 = lp[0], l1 = lp[1];
+            const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) E[e] = __expf(L[e]);
+            const float bt = bs[tt];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+            store_row8(sm + V_APA, 8192, tt, c8, o8);                           // k E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
+            store_row8(sm + V_BKG, 2048, tt, c8, o8);                           // b k E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+            store_row8(sm + V_APA, 8192, 16 + tt, c8, o8);                      // q E
+            store_row8(sm + V_SB, 4096, 16 + tt, c8, o8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * __fdividef(1.0f, E[e]);
+            store_row8(sm + V_APB, 2048, tt, c8, o8);                           // k / E
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
+            store_row8(sm + V_BV, 2048, tt, c8, o8);                            // b V
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- A and P (M=64 N=16 K=128)
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(64, 16);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + V_APA + kb * 8192 + off)),
+                         desc_sw128(smem_u32(sm + V_APB + kb * 2048 + off)), idesc, ks > 0);
+            }
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        if (warp < 2) {
+            float d[16];
+            tmem_ld16(tbase + tl + T_AP, d);
+            tmem_wait_ld();
+            if (lane < kC) {
+                const int t = lane;
+                if (warp == 0) {
+                    const float bt = bs[t];
+#pragma unroll
+                    for (int s2 = 0; s2 < kC; ++s2) af[t * 17 + s2] = s2 < t ? bt * d[s2] : 0.f;
+                } else {
+                    float p8[8];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
+                        uint4 r;
+                        r.x = pack_bf16x2(p8[0], p8[1]);
+                        r.y = pack_bf16x2(p8[2], p8[3]);
+                        r.z = pack_bf16x2(p8[4], p8[5]);
+                        r.w = pack_bf16x2(p8[6], p8[7]);
+                        *reinterpret_cast<uint4*>(sm + V_PB + sw128(t, hh)) = r;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- T = (I + A)^{-1}
+        if (tid < kC) {
+            const int jc = tid;
+            float x[kC];
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
+                x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+            }
+#pragma unroll
+            for (int r = 0; r < kC; ++r)
+                *reinterpret_cast<__nv_bfloat16*>(sm + V_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
+                    __float2bfloat16_rn(x[r]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- W^T and U~^T (M=128 N=16 K=16, A MN-major)
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16_amn(128, 16);
+            const uint64_t tb = desc_sw128(smem_u32(sm + V_TB));
+            mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + V_BKG), 2048, 1024), tb, idesc, false);
+            mma_bf16(tbase + T_UT, desc_sw128_mn(smem_u32(sm + V_BV), 2048, 1024), tb, idesc, false);
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        if (warp < 4) {
+            float w[16];
+            tmem_ld16(tbase + tl + T_WT, w);
+            tmem_wait_ld();
+            const int c = 32 * warp + lane;
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                *reinterpret_cast<__nv_bfloat16*>(sm + V_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
+                                                   (c & 7) * 2) = __float2bfloat16_rn(w[t]);
+        }
+        // ---- the state's bf16 copy S^T, row j (its loads have landed by now)
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            uint4 r;
+            r.x = pack_bf16x2(st[8 * q8 + 0], st[8 * q8 + 1]);
+            r.y = pack_bf16x2(st[8 * q8 + 2], st[8 * q8 + 3]);
+            r.z = pack_bf16x2(st[8 * q8 + 4], st[8 * q8 + 5]);
+            r.w = pack_bf16x2(st[8 * q8 + 6], st[8 * q8 + 7]);
+            *reinterpret_cast<uint4*>(sm + V_ST + ch * 16384 + sw128(j, q8)) = r;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T (M=128 N=32 K=128)
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 32);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + V_ST + kb * 16384 + off)),
+                         desc_sw128(smem_u32(sm + V_SB + kb * 4096 + off)), idesc, ks > 0);
+            }
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+        if (warp < 4) {
+            float ws_[16], ut[16];
+            tmem_ld16(tbase + tl + T_ST, ws_);
+            tmem_ld16(tbase + tl + T_UT, ut);
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint4 r;
+                r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
+                r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
+                r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
+                r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
+                *reinterpret_cast<uint4*>(sm + V_UT + sw128(j, hh)) = r;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- O^T += U^T P^T (M=128 N=16 K=16)
+        if (tid == 0) {
+            mma_bf16(tbase + T_ST + 16, desc_sw128(smem_u32(sm + V_UT)), desc_sw128(smem_u32(sm + V_PB)),
+                     idesc_bf16(128, 16), true);
+            mma_commit(bar);
+        }
+        if (!(ok = cta_wait(bar, phase))) break;
+    } while (false);
+
+    // ---- outputs o[b][t][h][j] (warps 0..3); NaN if a wait gave up
+    if (warp < 4) {
+        float ov[16];
+        tmem_ld16(tbase + tl + T_ST + 16, ov);
+        tmem_wait_ld();
+        if (j < dv) {
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                if (t < Tn)
+                    o[(((size_t)b * Tn + t) * H + h) * dv + j] = __float2bfloat16_rn(ok ? ov[t] : __int_as_float(0x7fc00000));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<kVTmemCols>(tbase);
+    }
+}
+
 }  // namespace c16
 
 cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const void* z,
@@ -552,6 +852,29 @@ cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const vo
     e = cudaGetLastError();
     profile_event(1, stream);
     return e;
+}
+
+cudaError_t run_spec_verify_tc(const void* q, const void* k, const void* v, const void* z,
+                               const void* beta, const float* A, const float* state, void* o, int B,
+                               int Tn, int H, int dk, int dv, cudaStream_t stream) {
+    constexpr int kMaxDevices = 64;
+    static bool attr_done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+        e = cudaFuncSetAttribute(c16::spec_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)c16::V_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    using bf = __nv_bfloat16;
+    c16::spec_verify_kernel<<<(unsigned)((int64_t)B * H), c16::kVThreads, c16::V_SMEM, stream>>>(
+        static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
+        static_cast<const bf*>(z), static_cast<const bf*>(beta), A, state, static_cast<bf*>(o), Tn, H, dk,
+        dv);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

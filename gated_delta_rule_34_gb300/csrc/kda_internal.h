@@ -79,4 +79,11 @@ cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const vo
                            int dk, int dv, void* workspace, const CheckpointSpec& ck,
                            cudaStream_t stream);
 
+// Speculative verify on the tensor cores: bf16, Tn <= 16, d_k and d_v
+// multiples of 16 (<= 128); the Tn draft tokens are one 16-token chunk taken
+// from the state (read only).
+cudaError_t run_spec_verify_tc(const void* q, const void* k, const void* v, const void* z,
+                               const void* beta, const float* A, const float* state, void* o, int B,
+                               int Tn, int H, int dk, int dv, cudaStream_t stream);
+
 }  // namespace kda

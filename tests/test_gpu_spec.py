@@ -29,8 +29,11 @@ def test_verify_outputs_and_state_untouched(B, T, H, d, dtype):
     torch.cuda.synchronize()
     assert torch.equal(state, xc["S0"]), "verify must not modify the state"
     ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
+    # fp32 inputs: token by token in fp32.  bf16 inputs: the span as one 16-token chunk on
+    # the tensor cores, held to the layer's bf16 bound like the tensor-core prefill.
     assert_parity(o.reshape(ro.shape), ro, dtype, f"verify B={B} T={T} d={d}")
-    assert rel_err(o.reshape(ro.shape), ro) < (1e-5 if dtype == torch.float32 else 5e-3)
+    if dtype == torch.float32:
+        assert rel_err(o.reshape(ro.shape), ro) < 1e-5
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -89,3 +92,25 @@ def test_full_size_verify_commit_b256_h32():
         _, rS = oracle.recurrent(*(x[nm][b:b + 1, :n] for nm in ("q", "k", "v", "z", "beta")),
                                  x["A"], S0=x["S0"][b:b + 1])
         assert rel_err(got[b], rS[0]) < 1e-5
+
+
+def test_verify_falls_back_to_fp32_for_other_head_sizes():
+    # d_k = 40 is not a multiple of 16: bf16 verify runs token by token in fp32.
+    w = replace(WORKLOADS[1], H=2, dk=40, dv=40, seed=94, initial_state=True)
+    x = make_inputs(w, B=3, T=7)
+    xc = cuda(x)
+    o = kda.spec_verify(xc["q"], xc["k"], xc["v"], xc["z"], xc["beta"], xc["A"], xc["S0"])
+    torch.cuda.synchronize()
+    ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
+    assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "verify d=40 (fp32 path)")
+    assert rel_err(o.reshape(ro.shape), ro) < 5e-3
+
+
+def test_full_size_verify_t16_all_pairs():
+    B, T, H, d = 256, 16, 32, 128
+    x = _draft(B, T, H, d, torch.bfloat16, seed=95)
+    xc = cuda(x)
+    o = kda.spec_verify(xc["q"], xc["k"], xc["v"], xc["z"], xc["beta"], xc["A"], xc["S0"])
+    torch.cuda.synchronize()
+    ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
+    assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "verify B=256 H=32 T=16 (all pairs)")
