@@ -493,6 +493,20 @@ def measure_next_rows(kda, xp, wp, xd, wd, peaks):
                                                   xp["A"], initial_state=xp["S0"], chunk=16),
                         iters=3, warm=1)
     out["long_prefill_chunk16"] = {"ms": t_long16, "tokens_per_s": Bp * Tp / (t_long16 * 1e-3)}
+    # The packed workload: 64 sequences of U{1..32768} tokens, H=16 (windows of 65,536 rows).
+    w4 = WORKLOADS[4]
+    x4 = make_inputs(w4, device="cuda")
+    cu4 = x4["cu_seqlens"].cuda()
+    n4 = cu4.numel() - 1
+    T4 = x4["q"].shape[1]
+    ws4 = torch.empty(kda.workspace_size(n4, 1, T4, w4.H, 128, 128, 64, torch.bfloat16),
+                      dtype=torch.uint8, device="cuda")
+    t_p = _time_ms(lambda: kda.chunk_prefill(x4["q"], x4["k"], x4["v"], x4["z"], x4["beta"], x4["A"],
+                                             initial_state=x4["S0"], cu_seqlens=cu4, workspace=ws4),
+                   iters=3, warm=1)
+    out["packed_64seq_h16"] = {"ms": t_p, "tokens": T4, "tokens_per_s": T4 / (t_p * 1e-3),
+                               "workspace_bytes": ws4.numel()}
+    del x4, ws4
     del x64, ws64
     out["segmented_prefill_t65536"] = measure_segmented(kda)
     return out
