@@ -67,7 +67,7 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
 // The 64-token path runs at most this many tokens at a time (per sequence of
 // a fixed-length batch, or in all of a packed one), the state carried from
 // window to window, so that its workspace is bounded by one window's packages.
-constexpr int64_t kWindowTokens = 65536;
+constexpr int64_t kWindowTokens = 262144;
 
 // Chunked tensor-core path with 16-token chunks (bf16; d_k and d_v multiples
 // of 16, at most 128): one fused kernel per (sequence, head), no package

@@ -43,7 +43,7 @@ def test_slots_stay_in_bounds():
                 used |= run
 
 
-WINDOW = 65536          # tokens per launch of the 64-token path (per sequence when fixed)
+WINDOW = 262144         # tokens per launch of the 64-token path (per sequence when fixed)
 CARRY = 128 * 128 * 4   # bytes of carried state per (sequence, head) between windows
 
 
@@ -53,7 +53,7 @@ def test_workspace_size_query_matches_bound():
     # for calls that run in several windows).
     L = kda.lib()
     for n_seqs, B, T, H in [(1, 1, 4096, 8), (2, 2, 4096, 8), (64, 1, 1048576, 16), (3, 1, 1, 1),
-                            (1, 1, 65536, 32), (1, 1, 1 << 20, 32), (2, 2, 200000, 4)]:
+                            (1, 1, 65536, 32), (1, 1, 1 << 20, 32), (2, 2, 600000, 4)]:
         fixed = n_seqs == B
         span = T if fixed else B * T
         w = min(span, WINDOW)
@@ -76,14 +76,15 @@ def test_workspace_size_query_matches_bound():
 
 
 def test_workspace_is_bounded_by_one_window():
-    # A million-token, 32-head prefill needs one 65,536-token window of packages
-    # (about 3.3 GB), not the ~52 GB its whole length would.
+    # A million-token, 32-head prefill needs one 262,144-token window of packages
+    # (about 13 GB), not the ~52 GB its whole length would; four million tokens need no more.
     L = kda.lib()
     big = L.kda_chunk_prefill_workspace_size(1, 1, 1 << 20, 32, 128, 128, 64, 1)
-    one = L.kda_chunk_prefill_workspace_size(1, 1, 65536, 32, 128, 128, 64, 1)
-    assert big < 3.5e9 and big <= one + 32 * CARRY + 2 * 32 * PKG_BYTES
-    packed = L.kda_chunk_prefill_workspace_size(64, 1, 1 << 20, 16, 128, 128, 64, 1)
-    assert packed < 2e9
+    huge = L.kda_chunk_prefill_workspace_size(1, 1, 1 << 22, 32, 128, 128, 64, 1)
+    one = L.kda_chunk_prefill_workspace_size(1, 1, WINDOW, 32, 128, 128, 64, 1)
+    assert big < 14e9 and big == huge and big <= one + 32 * CARRY + 2 * 32 * PKG_BYTES
+    packed = L.kda_chunk_prefill_workspace_size(64, 1, 1 << 22, 16, 128, 128, 64, 1)
+    assert packed < 7e9
 
 
 def _window_part(b, e, w0, w1):
