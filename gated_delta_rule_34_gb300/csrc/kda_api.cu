@@ -133,14 +133,24 @@ kda_prefill_path kda_chunk_prefill_path(int d_k, int d_v, int chunk, kda_dtype d
     return KDA_PATH_RECURRENT;
 }
 
-// Tokens of one window of the 64-token path (see kda::kWindowTokens).
-static int64_t window_span(int64_t T) { return T < kda::kWindowTokens ? T : kda::kWindowTokens; }
+// Window of the 64-token path (see kda::kWindowTokens): for a fixed-length
+// batch of B sequences, the positions per sequence (a multiple of 64, so that
+// B of them hold at most kWindowTokens tokens); for a packed batch, rows.
+static int64_t window_len(bool fixed, int B) {
+    if (!fixed || B <= 1) return kda::kWindowTokens;
+    const int64_t w = kda::kWindowTokens / B / 64 * 64;
+    return w < 64 ? 64 : w;
+}
+static int64_t window_span(bool fixed, int B, int64_t T) {
+    const int64_t w = window_len(fixed, B);
+    return T < w ? T : w;
+}
 
 // Segment count for kda_chunk_prefill: automatic for fixed-length batches on
 // the tensor-core path (n_seqs == B marks a fixed-length query), 1 otherwise.
 static int auto_segments(int n_seqs, int B, int64_t T, int H, int d_k, int d_v) {
     if (n_seqs != B) return 1;
-    return kda::chunked_tc_auto_segments(B, window_span(T), H, d_k, d_v, device_sm_count());
+    return kda::chunked_tc_auto_segments(B, window_span(true, B, T), H, d_k, d_v, device_sm_count());
 }
 
 // Workspace of the 64-token path for a fixed-length batch (`fixed`: B sequences
@@ -149,10 +159,10 @@ static int auto_segments(int n_seqs, int B, int64_t T, int H, int d_k, int d_v) 
 // windows, a carry area for the states between them (at the end).
 static size_t carry_bytes(int n_seqs, int H) { return (size_t)n_seqs * H * 128 * 128 * 4; }
 static size_t tc_workspace(bool fixed, int n_seqs, int B, int64_t T, int H, int G) {
-    const int64_t w = window_span(T);
+    const int64_t w = window_span(fixed, B, T);
     size_t bytes = fixed ? kda::chunked_tc_workspace_bytes(n_seqs, (int64_t)B * w, H, w, G)
                          : kda::chunked_tc_workspace_bytes(n_seqs, w, H, w, 1);
-    if (T > kda::kWindowTokens) bytes += carry_bytes(n_seqs, H);
+    if (T > w) bytes += carry_bytes(n_seqs, H);
     return bytes;
 }
 
@@ -179,7 +189,7 @@ size_t kda_chunk_prefill_segmented_workspace_size(int B, int64_t T, int H, int d
 int kda_chunk_prefill_auto_segments(int B, int64_t T, int H, int d_k, int d_v, int chunk,
                                     kda_dtype dtype) {
     if (B <= 0 || T <= 0 || H <= 0 || !use_chunked_tc(d_k, d_v, chunk, dtype)) return 1;
-    return kda::chunked_tc_segments_used(window_span(T), auto_segments(B, B, T, H, d_k, d_v));
+    return kda::chunked_tc_segments_used(window_span(true, B, T), auto_segments(B, B, T, H, d_k, d_v));
 }
 
 static kda_status prefill_impl(const void* q, const void* k, const void* v, const void* z,
@@ -235,7 +245,7 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         if (n_segments > 0) {
             if (!fixed && n_segments > 1)
                 return fail(KDA_ERR_UNSUPPORTED, "segments need a fixed-length batch (cu_seqlens == NULL)");
-            if ((int64_t)B * kda::chunked_tc_segments_used(window_span(T), n_segments) > 65535)
+            if ((int64_t)B * kda::chunked_tc_segments_used(window_span(true, B, T), n_segments) > 65535)
                 return fail(KDA_ERR_UNSUPPORTED, "B x segments must be <= 65535");
             G = n_segments;
         } else if (fixed) {
@@ -249,17 +259,19 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
                         workspace_bytes, workspace);
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
-        // Windows: at most kWindowTokens per launch (per sequence when fixed, in
-        // all when packed).  The states cross windows in final_state, or in the
-        // workspace's carry area when the caller wants no final state.
+        // Windows: at most kWindowTokens tokens per launch pair (window_len
+        // positions of every sequence when fixed, rows when packed).  The states
+        // cross windows in final_state, or in the workspace's carry area when the
+        // caller wants no final state.
         const int64_t span = fixed ? T : T_total;
+        const int64_t W = window_len(fixed, B);
         float* carry = final_state;
-        if (span > kda::kWindowTokens && carry == nullptr)
+        if (span > W && carry == nullptr)
             carry = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + need -
                                              carry_bytes(n_seqs, H));
         int64_t w0 = 0;
         do {
-            const int64_t w1 = span - w0 < kda::kWindowTokens ? span : w0 + kda::kWindowTokens;
+            const int64_t w1 = span - w0 < W ? span : w0 + W;
             const cudaError_t e = kda::run_chunked_tc(
                 q, k, v, z, beta, A, o, initial_state, carry, carry, cu_seqlens, n_seqs, T,
                 T_total, w0, w1, H, d_k, d_v, workspace, ck, stream, device_sm_count(), G);

@@ -64,9 +64,10 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
                            int dv, void* workspace, const CheckpointSpec& ck,
                            cudaStream_t stream, int num_sms, int n_segments);
 
-// The 64-token path runs at most this many tokens at a time (per sequence of
-// a fixed-length batch, or in all of a packed one), the state carried from
-// window to window, so that its workspace is bounded by one window's packages.
+// The 64-token path runs at most this many tokens at a time (B sequences of a
+// fixed-length batch take kWindowTokens / B positions each, rounded down to a
+// multiple of 64; a packed batch takes rows), the state carried from window to
+// window, so that its workspace is bounded by one window's packages.
 constexpr int64_t kWindowTokens = 262144;
 
 // Chunked tensor-core path with 16-token chunks (bf16; d_k and d_v multiples

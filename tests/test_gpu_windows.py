@@ -106,3 +106,15 @@ def test_segmented_windows():
     ro, rS = run_oracle({n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in x.items()})
     assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "segmented windows o")
     assert_parity(S, rS, torch.bfloat16, "segmented windows state")
+
+
+def test_fixed_length_batch_windows():
+    # Eight sequences share a window: 262,144 / 8 = 32,768 positions each, so 40,000
+    # tokens per sequence run in two windows.
+    w = replace(WORKLOADS[2], H=2, dk=32, dv=32, seed=806)
+    x = make_inputs(w, device="cuda", B=8, T=40000)
+    o, S, status = _run_with_status(x)
+    assert status == 0
+    ro, rS = run_oracle({n: (t.cpu() if isinstance(t, torch.Tensor) else t) for n, t in x.items()})
+    assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "batch windows o")
+    assert_parity(S, rS, torch.bfloat16, "batch windows state")

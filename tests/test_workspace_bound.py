@@ -53,20 +53,22 @@ def test_workspace_size_query_matches_bound():
     # for calls that run in several windows).
     L = kda.lib()
     for n_seqs, B, T, H in [(1, 1, 4096, 8), (2, 2, 4096, 8), (64, 1, 1048576, 16), (3, 1, 1, 1),
-                            (1, 1, 65536, 32), (1, 1, 1 << 20, 32), (2, 2, 600000, 4)]:
+                            (1, 1, 65536, 32), (1, 1, 1 << 20, 32), (2, 2, 600000, 4),
+                            (64, 64, 65536, 32), (3, 3, 100000, 2), (5000, 5000, 100, 1)]:
         fixed = n_seqs == B
         span = T if fixed else B * T
-        w = min(span, WINDOW)
+        W = max(64, WINDOW // B // 64 * 64) if fixed and B > 1 else WINDOW
+        w = min(span, W)
         slots = (B * w if fixed else w) // 64 + n_seqs + 1
         packages = HEADER + slots * H * PKG_BYTES
-        carry = n_seqs * H * CARRY if span > WINDOW else 0
+        carry = n_seqs * H * CARRY if span > w else 0
         got = L.kda_chunk_prefill_workspace_size(n_seqs, B, T, H, 128, 128, 64, 1)
         if not fixed:                         # packed: never segmented
             assert got == packages + carry
             continue
         G = L.kda_chunk_prefill_auto_segments(B, T, H, 128, 128, 64, 1)
         seg = packages + n_seqs * H * (G - 1) * (128 + 64) * 1024 + carry
-        if B == 1 and span > WINDOW:          # a single sequence may also come packed
+        if B == 1 and span > w:               # a single sequence may also come packed
             packed = HEADER + (w // 64 + 2) * H * PKG_BYTES + H * CARRY
             assert got == max(seg, packed)
         else:
@@ -85,6 +87,9 @@ def test_workspace_is_bounded_by_one_window():
     assert big < 14e9 and big == huge and big <= one + 32 * CARRY + 2 * 32 * PKG_BYTES
     packed = L.kda_chunk_prefill_workspace_size(64, 1, 1 << 22, 16, 128, 128, 64, 1)
     assert packed < 7e9
+    # a large fixed-length batch is windowed over the batch's tokens, not per sequence
+    batch = L.kda_chunk_prefill_workspace_size(64, 64, 65536, 32, 128, 128, 64, 1)
+    assert batch < 14e9
 
 
 def _window_part(b, e, w0, w1):
