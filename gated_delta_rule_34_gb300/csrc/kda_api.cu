@@ -287,6 +287,9 @@ static kda_status prefill_impl(const void* q, const void* k, const void* v, cons
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return fail(KDA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
         if (n_segments > 1) return fail(KDA_ERR_UNSUPPORTED, "segments run on the 64-token path only");
+        if (T_total > (int64_t)INT32_MAX - 16)
+            return fail(KDA_ERR_UNSUPPORTED, "the tensor-core path takes fewer than 2^31 tokens (%lld)",
+                        (long long)T_total);
         return cuda_status(kda::run_chunk16_tc(q, k, v, z, beta, A, o, initial_state, final_state,
                                                cu_seqlens, n_seqs, T, T_total, H, d_k, d_v,
                                                workspace, ck, stream),

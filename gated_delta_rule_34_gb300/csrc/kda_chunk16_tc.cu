@@ -39,6 +39,8 @@
 //   D[j][c] = U^T (k lam / E)                      M=128 N=128 K=16   (B MN-major)
 // and the fp32 update S^T <- S^T Diag(lam) + D on the registers.  The path
 // needs no workspace beyond the status word.
+#include <cuda.h>
+#include <string.h>
 #include <cuda_bf16.h>
 
 #include "kda_common.cuh"
@@ -72,8 +74,12 @@ constexpr uint32_t R_AF = 116736;     // [P] A fp32 [16][17]
 constexpr uint32_t R_LAM = 118016;    // [P->C] lam [128] fp32; x2
 constexpr uint32_t R_EA = 119040;     // [P] e^{A_h} [128] fp32
 constexpr uint32_t R_BETA = 119552;   // [P] beta [16] fp32
-constexpr uint32_t R_BAR = 119616;    // mbarriers (prep MMA, chain MMA, ready x2, freed x2), TMEM slot
-constexpr uint32_t SMEM = R_BAR + 64 + 1024;   // + slack for aligning the base
+constexpr uint32_t R_IN = 120832;     // [P] input tiles z, k, q, v of a chunk, 4 KB each (256-byte
+                                      //     token rows, as the tensor maps land them); two stages
+constexpr uint32_t IN_STAGE = 16384;
+constexpr uint32_t R_BAR = R_IN + 2 * IN_STAGE;   // mbarriers (prep MMA, chain MMA, ready x2,
+                                                  // freed x2, inputs x2), TMEM slot
+constexpr uint32_t SMEM = R_BAR + 128 + 1024;   // + slack for aligning the base
 static_assert(SMEM <= 232448, "shared memory");
 
 // TMEM columns
@@ -138,10 +144,15 @@ __device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int6
     return __ldg(reinterpret_cast<const uint4*>(x + ((size_t)row * H + h) * d + 8 * c8));
 }
 
+// Tensor maps of the inputs [T_total][H][d] with boxes of 16 tokens x 1 head x
+// 128 channels (4 KB): a chunk's tile of each input is one TMA load.
+struct InputMaps16 {
+    CUtensorMap q, k, v, z;
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
-chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-               const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
-               const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
+chunk16_kernel(const __grid_constant__ InputMaps16 maps, const __nv_bfloat16* __restrict__ beta,
+               const float* __restrict__ A,
                __nv_bfloat16* __restrict__ o, const float* __restrict__ S0, float* __restrict__ S1,
                const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H, int dk, int dv,
                uint32_t* __restrict__ status, CheckpointSpec ck) {
@@ -157,7 +168,8 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
     uint64_t* bar_c = bar_p + 1;
     uint64_t* ready = bar_p + 2;     // [2]
     uint64_t* freed = bar_p + 4;     // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 48);
+    uint64_t* inb = bar_p + 6;       // [2] input tiles of chunk ci in stage ci & 1 landed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + R_BAR + 64);
 
     int64_t bos, eos;
     seq_bounds(cu, n, T_len, T_total, bos, eos);
@@ -173,6 +185,7 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         for (int p = 0; p < 2; ++p) {
             mbar_init(ready + p, 1);
             mbar_init(freed + p, 1);
+            mbar_init(inb + p, 1);
         }
         fence_mbar_init();
     }
@@ -226,19 +239,30 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
         // ============================================ preparation group
         const int tt = tid >> 4, c8 = tid & 15;   // token tt, channels 8 c8 .. + 7
         uint32_t phase = 0;
-        // inputs of chunk ci, loaded one chunk ahead
-        uint4 kr = make_uint4(0, 0, 0, 0), qr = kr, vr = kr, zr = kr;
-        float bnext = 0.f;
-        auto load_inputs = [&](int ci) {
+        // The input tiles of chunk ci land in stage ci & 1 by TMA, requested two
+        // chunks ahead by thread 0 (tokens past the sequence belong to the next
+        // one or read as zeros; `live` masks them).  beta is loaded one chunk
+        // ahead as raw bits and converted where it is used.
+        auto issue_inputs = [&](int ci) {
             const int64_t t0 = bos + (int64_t)ci * kC;
-            const bool live = t0 + tt < eos;
-            kr = live ? load8(k, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
-            qr = live ? load8(q, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
-            vr = live ? load8(v, t0 + tt, H, h, dv, c8) : make_uint4(0, 0, 0, 0);
-            zr = live ? load8(z, t0 + tt, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
-            if (tid < kC) bnext = t0 + tid < eos ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+            uint8_t* in = sm + R_IN + (ci & 1) * IN_STAGE;
+            uint64_t* bar = inb + (ci & 1);
+            mbar_expect_tx(bar, IN_STAGE);
+            tma_load_3d(in, &maps.z, 0, h, (int)t0, bar);
+            tma_load_3d(in + 4096, &maps.k, 0, h, (int)t0, bar);
+            tma_load_3d(in + 8192, &maps.q, 0, h, (int)t0, bar);
+            tma_load_3d(in + 12288, &maps.v, 0, h, (int)t0, bar);
         };
-        if (nchunks > 0) load_inputs(0);
+        auto load_beta_bits = [&](int ci) -> uint32_t {
+            const int64_t t0 = bos + (int64_t)ci * kC;
+            return (tid < kC && ci < nchunks && t0 + tid < eos)
+                       ? reinterpret_cast<const unsigned short*>(beta)[(size_t)(t0 + tid) * H + h]
+                       : 0u;
+        };
+        int issued = 0, landed = 0;               // input requests (thread 0) and completed waits
+        if (tid == 0)
+            for (; issued < 2 && issued < nchunks; ++issued) issue_inputs(issued);
+        uint32_t braw = load_beta_bits(0);
         for (int ci = 0; ci < nchunks; ++ci) {
             const int p = ci & 1;
             const int64_t t0 = bos + (int64_t)ci * kC;
@@ -248,8 +272,14 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
             uint8_t* kc = sm + R_KC + p * 4096;
             uint8_t* pb = sm + R_PB + p * 2048;
             float* lam = reinterpret_cast<float*>(sm + R_LAM + p * 512);
+            const uint8_t* in = sm + R_IN + p * IN_STAGE;
             // buffers p were last used for chunk ci - 2
             if (ci >= 2 && !(ok = group_wait(freed + p, ((ci - 2) >> 1) & 1, kBarPrep))) break;
+            if (!(ok = group_wait(inb + p, (ci >> 1) & 1, kBarPrep))) break;
+            ++landed;
+            const uint4 zr = live ? *reinterpret_cast<const uint4*>(in + tt * 256 + c8 * 16) : make_uint4(0, 0, 0, 0);
+            const float bnext = __uint_as_float(braw << 16);
+            braw = load_beta_bits(ci + 1);
 
             // ---- gate -> gs (zeros past the chunk and past d_k)
             {
@@ -281,9 +311,10 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
             // ---- decay-scaled operands of token tt (bf16)
             {
                 float kf[8], qf[8], vf[8], E[8], R[8], o8[8];
-                unpack8(kr, kf);
-                unpack8(qr, qf);
-                unpack8(vr, vf);
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                unpack8(live ? *reinterpret_cast<const uint4*>(in + 4096 + tt * 256 + c8 * 16) : zero, kf);
+                unpack8(live ? *reinterpret_cast<const uint4*>(in + 8192 + tt * 256 + c8 * 16) : zero, qf);
+                unpack8(live ? *reinterpret_cast<const uint4*>(in + 12288 + tt * 256 + c8 * 16) : zero, vf);
                 const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
                 const float4 l0 = lp[0], l1 = lp[1];
                 const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
@@ -317,6 +348,8 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
             tc_fence_before();
             named_bar_sync(kBarPrep, kGroup);
             tc_fence_after();
+            // Stage p has been read: it takes chunk ci + 2's inputs.
+            if (tid == 0 && issued < nchunks) issue_inputs(issued++);
 
             // ---- A and P: D[t][s] = [kE ; qE] (k/E)^T, M=64 N=16 K=128
             if (tid == 0) {
@@ -406,13 +439,15 @@ chunk16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restr
                     *reinterpret_cast<__nv_bfloat16*>(sb + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
                                                        (c & 7) * 2) = __float2bfloat16_rn(w[t]);
             }
-            // the next chunk's inputs, in flight while the chain takes this one
-            if (ci + 1 < nchunks) load_inputs(ci + 1);
             fence_async_smem();
             tc_fence_before();
             named_bar_sync(kBarPrep, kGroup);
             if (tid == 0) mbar_arrive(ready + p);
         }
+        // After a wait gave up, let the input copies still in flight land
+        // (bounded) before the CTA exits.
+        if (tid == 0)
+            for (int c = landed; c < issued; ++c) mbar_wait(inb + (c & 1), (c >> 1) & 1);
     } else {
         // ================================================== chain group
         uint32_t phase = 0;
@@ -842,13 +877,22 @@ cudaError_t run_chunk16_tc(const void* q, const void* k, const void* v, const vo
     uint32_t* status = static_cast<uint32_t*>(workspace);
     e = cudaMemsetAsync(status, 0, CHUNK16_WORKSPACE_BYTES, stream);
     if (e != cudaSuccess) return e;
+    // TMA token coordinates are 32-bit.  Without tokens no input is read (the
+    // kernel only passes the states through), so no map is built.
+    if (T_total > 0x7fffffffLL) return cudaErrorInvalidValue;
+    c16::InputMaps16 maps;
+    memset(&maps, 0, sizeof(maps));
+    if (T_total > 0 && (!make_rows_tensor_map(&maps.q, q, T_total, H, dk, c16::kC) ||
+                        !make_rows_tensor_map(&maps.k, k, T_total, H, dk, c16::kC) ||
+                        !make_rows_tensor_map(&maps.v, v, T_total, H, dv, c16::kC) ||
+                        !make_rows_tensor_map(&maps.z, z, T_total, H, dk, c16::kC)))
+        return cudaErrorInvalidValue;
     using bf = __nv_bfloat16;
     profile_event(0, stream);
     dim3 grid((unsigned)n_seqs, (unsigned)H);
     c16::chunk16_kernel<<<grid, c16::kThreads, c16::SMEM, stream>>>(
-        static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-        static_cast<const bf*>(z), static_cast<const bf*>(beta), A, static_cast<bf*>(o), S0, S1, cu, T,
-        T_total, H, dk, dv, status, ck);
+        maps, static_cast<const bf*>(beta), A, static_cast<bf*>(o), S0, S1, cu, T, T_total, H, dk, dv,
+        status, ck);
     e = cudaGetLastError();
     profile_event(1, stream);
     return e;

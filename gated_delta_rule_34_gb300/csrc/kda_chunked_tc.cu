@@ -1787,19 +1787,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor map of one [T_total][H][d] bf16 input (d <= 128, 2 d a multiple of
-// 16 bytes) with 64 x 1 x 128 boxes: channels d .. 127 of a box lie outside
-// the tensor and arrive as zeros.
-static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int d) {
+// 16 bytes) with box_rows x 1 x 128 boxes: channels d .. 127 of a box lie
+// outside the tensor and arrive as zeros.
+bool make_rows_tensor_map(void* map, const void* base, int64_t T_total, int H, int d, int box_rows) {
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T_total};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-    cuuint32_t box[3] = {128, 1, 64};
+    cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
-    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+static bool make_input_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int d) {
+    return make_rows_tensor_map(m, base, T_total, H, d, tc::kC);
 }
 
 // Chunks per segment and the segment count actually used when a fixed-length

@@ -70,6 +70,12 @@ cudaError_t run_chunked_tc(const void* q, const void* k, const void* v, const vo
 // window, so that its workspace is bounded by one window's packages.
 constexpr int64_t kWindowTokens = 262144;
 
+// Tensor map (a CUtensorMap, written to `map`) of a [T_total][H][d] bf16
+// tensor (2 d a multiple of 16 bytes) with boxes of box_rows tokens x 1 head x
+// 128 channels; channels d .. 127 and tokens past T_total read as zeros.
+// False if the driver's encoder is unavailable or rejects the description.
+bool make_rows_tensor_map(void* map, const void* base, int64_t T_total, int H, int d, int box_rows);
+
 // Chunked tensor-core path with 16-token chunks (bf16; d_k and d_v multiples
 // of 16, at most 128): one fused kernel per (sequence, head), no package
 // workspace; the workspace holds only the device status word.
