@@ -137,6 +137,13 @@ __device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
     for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(b[e]);
 }
 
+// 8 consecutive floats from 16-byte aligned shared memory.
+__device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 // 8 bf16 of row `row` of a [T_total][H][d] tensor, channels 8 c8 .. (zeros past d).
 __device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int64_t row, int H, int h,
                                        int d, int c8) {
@@ -283,12 +290,13 @@ chunk16_kernel(const __grid_constant__ InputMaps16 maps, const __nv_bfloat16* __
 
             // ---- gate -> gs (zeros past the chunk and past d_k)
             {
-                float zf[8], g[8];
+                float zf[8], g[8], eav[8];
                 unpack8(zr, zf);
+                load8f(ea + 8 * c8, eav);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = 8 * c8 + e;
-                    g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+                    g[e] = (live && c < dk) ? gate_fast(eav[e], zf[e]) : 0.f;
                 }
                 float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
                 gp[0] = make_float4(g[0], g[1], g[2], g[3]);
@@ -337,8 +345,10 @@ chunk16_kernel(const __grid_constant__ InputMaps16 maps, const __nv_bfloat16* __
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o8[e] = kf[e] * R[e];
                 store_row8(sm + R_APB, 2048, tt, c8, o8);                           // k / E
+                float lv[8];
+                load8f(lam + 8 * c8, lv);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = o8[e] * lam[8 * c8 + e];
+                for (int e = 0; e < 8; ++e) o8[e] = o8[e] * lv[e];
                 store_row8(kc, 2048, tt, c8, o8);                                   // k lam / E
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
@@ -526,10 +536,17 @@ chunk16_kernel(const __grid_constant__ InputMaps16 maps, const __nv_bfloat16* __
                 float d[16];
                 tmem_ld16(tbase + tl + T_SU + 64 * ch + 16 * q16, d);
                 tmem_wait_ld();
+                // lam of this slice's 16 channels as four 16-byte broadcasts
+                float lv[16];
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(lam + 64 * ch + 16 * q16 + 4 * e4);
+                    lv[4 * e4] = l4.x; lv[4 * e4 + 1] = l4.y; lv[4 * e4 + 2] = l4.z; lv[4 * e4 + 3] = l4.w;
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int idx = 16 * q16 + e;
-                    st[idx] = fmaf(lam[64 * ch + idx], st[idx], d[e]);
+                    st[idx] = fmaf(lv[e], st[idx], d[e]);
                 }
             }
             write_st();
