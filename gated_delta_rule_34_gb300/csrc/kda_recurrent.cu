@@ -64,31 +64,55 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         }
     }
 
+    // The next tile's raw inputs are loaded into registers while the current
+    // tile's tokens run: thread (row tt = tid / 128 + 2 i, channel c = tid mod
+    // 128) for q, k, z; (tt, column jj) pairs idx = tid + 256 i for v; beta by
+    // threads < 16.
+    float rq[kRecTile / 2], rk[kRecTile / 2], rz[kRecTile / 2], rv[2], rb = 0.f;
+    auto fetch = [&](int64_t t0) {
+        const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
+        const int c = tid & 127;
+#pragma unroll
+        for (int i = 0; i < kRecTile / 2; ++i) {
+            const int tt = (tid >> 7) + 2 * i;
+            rq[i] = rk[i] = rz[i] = 0.f;
+            if (tt < nt && c < dk) {
+                const size_t e = ((size_t)(t0 + tt) * H + h) * dk + c;
+                rq[i] = to_f32(q[e]);
+                rk[i] = to_f32(k[e]);
+                rz[i] = to_f32(z[e]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + kRecThreads * i, tt = idx / kRecCols, j = col0 + idx % kRecCols;
+            rv[i] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j]) : 0.f;
+        }
+        if (tid < kRecTile) rb = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    };
+    if (bos < eos) fetch(bos);
+
     for (int64_t t0 = bos; t0 < eos; t0 += kRecTile) {
         const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
         __syncthreads();   // previous tile fully consumed; s_expA visible
-        for (int idx = tid; idx < kRecTile * 128; idx += kRecThreads) {
-            const int tt = idx >> 7, c = idx & 127;
-            float qq = 0.f, kk = 0.f, aa = 1.f;
-            if (tt < nt && c < dk) {
-                const size_t e = ((size_t)(t0 + tt) * H + h) * dk + c;
-                qq = to_f32(q[e]);
-                kk = to_f32(k[e]);
-                aa = expf(gate_accurate(s_expA[c], to_f32(z[e])));
+        {
+            const int c = tid & 127;
+#pragma unroll
+            for (int i = 0; i < kRecTile / 2; ++i) {
+                const int tt = (tid >> 7) + 2 * i;
+                s_q[tt][c] = rq[i];
+                s_k[tt][c] = rk[i];
+                s_a[tt][c] = (tt < nt && c < dk) ? expf(gate_accurate(s_expA[c], rz[i])) : 1.f;
             }
-            s_q[tt][c] = qq;
-            s_k[tt][c] = kk;
-            s_a[tt][c] = aa;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int idx = tid + kRecThreads * i;
+                s_v[idx / kRecCols][idx % kRecCols] = rv[i];
+            }
+            if (tid < kRecTile) s_b[tid] = rb;
         }
-        for (int idx = tid; idx < kRecTile * kRecCols; idx += kRecThreads) {
-            const int tt = idx / kRecCols, jj = idx % kRecCols;
-            const int j = col0 + jj;
-            s_v[tt][jj] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j])
-                                              : 0.f;
-        }
-        if (tid < kRecTile)
-            s_b[tid] = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
         __syncthreads();
+        if (t0 + kRecTile < eos) fetch(t0 + kRecTile);
         // k^T q per token: warp w handles tokens w and w + 8.
         for (int tt = warp; tt < kRecTile; tt += kRecThreads / 32) {
             float acc = 0.f;
