@@ -1,23 +1,37 @@
 // kda_recurrent.cu -- token-by-token prefill in fp32 SIMT arithmetic.
 //
 // The path for fp32 inputs (tf32 tensor cores cannot meet a 1e-4 relative
-// bound) and for head sizes the tensor-core path does not cover.  It runs the
+// bound) and for head sizes the tensor-core paths do not cover.  It runs the
 // delta rule of "Kimi K3 architecture: how an open model with a million-token context competes with market leaders"
 // (section "How the Kimi K3 architecture holds a million tokens of context") with the
 // per-channel gate of "How Kimi K3 is built: 2.8 trillion parameters, linear attention and agents for a million tokens"
-// (section "Sequence: three KDA to one global MLA") exactly as written, token by token:
+// (section "Sequence: three KDA to one global MLA") token by token:
 //
 //   S' = Diag(a_t) S,  u = b_t (v_t - S'^T k_t),  S <- S' + k_t u^T,
 //   o_t = S'^T q_t + u (k_t^T q_t)
 //
+// Decay factoring.  Inside a run of at most 8 tokens the registers hold
+// R = Diag(1 / gam_t) S, with gam_t the running product of the decays since
+// the run started (per channel, >= e^-40, so R stays within e^40 of S), so a
+// token needs no rescaling of the state:
+//   S'^T k = R^T (gam_t k),  S'^T q = R^T (gam_t q),  R <- R + (k / gam_t) u^T,
+// and at the end of the run S = Diag(gam_last) R.  The scaled vectors come
+// from the running log-decay L_t (gam_t = e^{L_t}), computed per channel once
+// per CTA.  The result is the exact recurrence up to fp32 rounding and the
+// fast exponential's error (a few units in the last place, far inside the
+// 1e-4 bound for fp32 inputs).
+//
 // Columns of S evolve independently (column j only sees k, a, b and v[:, j]),
-// so the work splits over (sequence, head, 32-column group).  A CTA of eight
-// warps owns 32 columns; warp w owns 4 of them, lane l holds rows l, l+32,
-// l+64, l+96 of each (16 fp32 registers).  Tiles of 16 tokens are staged in
-// shared memory (q, k, the gate-derived decay a, beta, v for the 32 columns),
-// the decay is computed once per CTA per token and channel, and the d_k
-// reductions are warp butterflies.  The chunk size does not enter: the result
-// is the exact recurrence up to fp32 rounding.
+// so the work splits over (sequence, head, 64-column group).  A CTA of eight
+// warps owns 64 columns; warp w owns 8 of them, lane (rq = lane / 4, cq =
+// lane mod 4) holds rows 16 rq .. 16 rq + 15 of columns 8 w + 2 cq and
+// 8 w + 2 cq + 1 (32 registers, as row pairs on which packed two-lane FMAs
+// run), so the d_k reductions are in-thread sums of 16 plus three
+// xor-shuffles (lane bits 2..4).  Tiles of 16 tokens are staged
+// in shared memory; the next tile's raw inputs are loaded into registers while
+// the current tile's tokens run.  The per-row vectors sit in rows whose
+// 16-channel groups are 20 floats apart, so the eight row groups of a warp
+// read them as conflict-free 16-byte loads.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -25,7 +39,11 @@ namespace kda {
 
 constexpr int kRecThreads = 256;
 constexpr int kRecTile = 16;     // tokens staged per shared-memory tile
-constexpr int kRecCols = 32;     // state columns per CTA (4 per warp)
+constexpr int kRecRun = 8;       // tokens per factoring run (gam >= e^{-5 kRecRun})
+constexpr int kRecCols = 64;     // state columns per CTA (8 per warp)
+constexpr int kRecPitch = 160;   // floats per token row of the scaled vectors: 8 groups of 16 + 4
+
+__device__ __forceinline__ int rec_idx(int c) { return (c >> 4) * 20 + (c & 15); }
 
 template <typename T>
 __global__ void __launch_bounds__(kRecThreads)
@@ -37,13 +55,17 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  int dk, int dv, CheckpointSpec ck) {
     const int cgrp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int col0 = cgrp * kRecCols;           // first column of this CTA
-    const int wcol = warp * 4;                  // first column of this warp (CTA-local)
+    const int rq = lane >> 2, cq = lane & 3;
+    const int col0 = cgrp * kRecCols;                 // first column of this CTA
+    const int lcol = 8 * warp + 2 * cq;               // this lane's first column, CTA-local
+    const int r0 = 16 * rq;                           // this lane's first row
 
-    __shared__ float s_q[kRecTile][128], s_k[kRecTile][128], s_a[kRecTile][128];
-    __shared__ float s_v[kRecTile][kRecCols], s_o[kRecTile][kRecCols];
-    __shared__ float s_b[kRecTile], s_kq[kRecTile];
-    __shared__ float s_expA[128];
+    // s_kg holds g, then the running log-decay L, before gam k
+    __shared__ __align__(16) float s_kg[kRecTile * kRecPitch], s_qg[kRecTile * kRecPitch];
+    __shared__ __align__(16) float s_kh[kRecTile * kRecPitch];
+    __shared__ __align__(16) float s_v[kRecTile][kRecCols], s_o[kRecTile][kRecCols];
+    __shared__ __align__(16) float s_glast[kRecTile / kRecRun][kRecPitch];   // gam at each run's end
+    __shared__ float s_b[kRecTile], s_kq[kRecTile], s_kqp[kRecTile][4], s_expA[128];
 
     int64_t bos, eos;
     seq_bounds(cu, n, T_len, T_total, bos, eos);
@@ -51,111 +73,184 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     for (int c = tid; c < 128; c += kRecThreads)
         s_expA[c] = c < dk ? expf(A[(size_t)h * dk + c]) : 0.f;
 
-    // State registers: st[i][c] = S[lane + 32 i][col0 + wcol + c].
-    float st[4][4];
+    // State registers: st[p][u] = (S[r0 + 2p][j], S[r0 + 2p + 1][j]) with
+    // j = col0 + lcol + u (R inside a run).
+    uint64_t st[8][2];
     const size_t sbase = ((size_t)n * H + h) * dk * dv;
+    const bool okc[2] = {col0 + lcol < dv, col0 + lcol + 1 < dv};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int r = lane + 32 * i;
+    for (int p2 = 0; p2 < 8; ++p2) {
+        const int r = r0 + 2 * p2;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int j = col0 + wcol + c;
-            st[i][c] = (S0 && r < dk && j < dv) ? S0[sbase + (size_t)r * dv + j] : 0.f;
+        for (int u = 0; u < 2; ++u) {
+            const float* p = S0 ? S0 + sbase + (size_t)r * dv + col0 + lcol + u : nullptr;
+            st[p2][u] = f2_pack((p && r < dk && okc[u]) ? p[0] : 0.f, (p && r + 1 < dk && okc[u]) ? p[dv] : 0.f);
         }
     }
+    auto store_state = [&](float* mat) {      // mat: [d_k][d_v] of (n, h)
+#pragma unroll
+        for (int p2 = 0; p2 < 8; ++p2) {
+            const int r = r0 + 2 * p2;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float2 x = f2_unpack(st[p2][u]);
+                float* p = mat + (size_t)r * dv + col0 + lcol + u;
+                if (okc[u] && r < dk) p[0] = x.x;
+                if (okc[u] && r + 1 < dk) p[dv] = x.y;
+            }
+        }
+    };
 
-    // The next tile's raw inputs are loaded into registers while the current
+    // The next tile's raw inputs, loaded into registers while the current
     // tile's tokens run: thread (row tt = tid / 128 + 2 i, channel c = tid mod
-    // 128) for q, k, z; (tt, column jj) pairs idx = tid + 256 i for v; beta by
+    // 128) for q, k, z; (tt, column) pairs idx = tid + 256 i for v; beta by
     // threads < 16.
-    float rq[kRecTile / 2], rk[kRecTile / 2], rz[kRecTile / 2], rv[2], rb = 0.f;
+    constexpr int kVPer = kRecTile * kRecCols / kRecThreads;
+    float rq_[kRecTile / 2], rk_[kRecTile / 2], rz_[kRecTile / 2], rv_[kVPer];
+    float rb_ = 0.f;
     auto fetch = [&](int64_t t0) {
         const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
         const int c = tid & 127;
 #pragma unroll
         for (int i = 0; i < kRecTile / 2; ++i) {
             const int tt = (tid >> 7) + 2 * i;
-            rq[i] = rk[i] = rz[i] = 0.f;
+            rq_[i] = rk_[i] = rz_[i] = 0.f;
             if (tt < nt && c < dk) {
                 const size_t e = ((size_t)(t0 + tt) * H + h) * dk + c;
-                rq[i] = to_f32(q[e]);
-                rk[i] = to_f32(k[e]);
-                rz[i] = to_f32(z[e]);
+                rq_[i] = to_f32(q[e]);
+                rk_[i] = to_f32(k[e]);
+                rz_[i] = to_f32(z[e]);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kVPer; ++i) {
             const int idx = tid + kRecThreads * i, tt = idx / kRecCols, j = col0 + idx % kRecCols;
-            rv[i] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j]) : 0.f;
+            rv_[i] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j]) : 0.f;
         }
-        if (tid < kRecTile) rb = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+        if (tid < kRecTile) rb_ = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
     };
     if (bos < eos) fetch(bos);
 
     for (int64_t t0 = bos; t0 < eos; t0 += kRecTile) {
         const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
         __syncthreads();   // previous tile fully consumed; s_expA visible
+        // Thread (token tt = tid / 128 + 2 i, channel c = tid mod 128) keeps its
+        // raw k and q in registers: g goes to s_kg, and the warp's 32 channels
+        // of k^T q to s_kqp.
         {
             const int c = tid & 127;
 #pragma unroll
             for (int i = 0; i < kRecTile / 2; ++i) {
                 const int tt = (tid >> 7) + 2 * i;
-                s_q[tt][c] = rq[i];
-                s_k[tt][c] = rk[i];
-                s_a[tt][c] = (tt < nt && c < dk) ? expf(gate_accurate(s_expA[c], rz[i])) : 1.f;
+                s_kg[tt * kRecPitch + rec_idx(c)] = (tt < nt && c < dk) ? gate_fast(s_expA[c], rz_[i]) : 0.f;
+                const float p = warp_sum(rk_[i] * rq_[i]);
+                if (lane == 0) s_kqp[tt][(tid >> 5) & 3] = p;
             }
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kVPer; ++i) {
                 const int idx = tid + kRecThreads * i;
-                s_v[idx / kRecCols][idx % kRecCols] = rv[i];
+                s_v[idx / kRecCols][idx % kRecCols] = rv_[i];
             }
-            if (tid < kRecTile) s_b[tid] = rb;
+            if (tid < kRecTile) s_b[tid] = rb_;
         }
         __syncthreads();
-        if (t0 + kRecTile < eos) fetch(t0 + kRecTile);
-        // k^T q per token: warp w handles tokens w and w + 8.
-        for (int tt = warp; tt < kRecTile; tt += kRecThreads / 32) {
-            float acc = 0.f;
+        // The running log-decay inside each run of kRecRun tokens, per channel,
+        // in place, and gam at each run's end (g = 0 past the tile's live tokens).
+        if (tid < 128) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) acc += s_k[tt][lane + 32 * m] * s_q[tt][lane + 32 * m];
-            acc = warp_sum(acc);
-            if (lane == 0) s_kq[tt] = acc;
+            for (int run = 0; run < kRecTile / kRecRun; ++run) {
+                float L = 0.f;
+#pragma unroll
+                for (int i = 0; i < kRecRun; ++i) {
+                    const int ix = (run * kRecRun + i) * kRecPitch + rec_idx(tid);
+                    L += s_kg[ix];
+                    s_kg[ix] = L;
+                }
+                s_glast[run][rec_idx(tid)] = __expf(L);
+            }
+        } else if (tid < 128 + kRecTile) {
+            const int tt = tid - 128;
+            s_kq[tt] = (s_kqp[tt][0] + s_kqp[tt][1]) + (s_kqp[tt][2] + s_kqp[tt][3]);
         }
         __syncthreads();
+        // gam k (over L in place), gam q and k / gam for every (token, channel)
+        {
+            const int c = tid & 127;
+#pragma unroll
+            for (int i = 0; i < kRecTile / 2; ++i) {
+                const int tt = (tid >> 7) + 2 * i;
+                const int ix = tt * kRecPitch + rec_idx(c);
+                const float L = s_kg[ix];
+                const float g = __expf(L), ig = __expf(-L);
+                s_kg[ix] = g * rk_[i];
+                s_qg[ix] = g * rq_[i];
+                s_kh[ix] = ig * rk_[i];
+            }
+        }
+        __syncthreads();
+        // the raw registers are free: the next tile's inputs load during the tokens
+        if (t0 + kRecTile < eos) fetch(t0 + kRecTile);
 
         for (int tt = 0; tt < nt; ++tt) {
-            float a[4], kk[4], qq[4];
+            const int base = tt * kRecPitch + rq * 20;
+            // S'^T k and S'^T q on this lane's 16 rows: row pairs on packed
+            // FMAs, two accumulators per column and vector
+            uint64_t pk[2][2] = {{0ull, 0ull}, {0ull, 0ull}}, pq[2][2] = {{0ull, 0ull}, {0ull, 0ull}};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = s_a[tt][lane + 32 * i];
-                kk[i] = s_k[tt][lane + 32 * i];
-                qq[i] = s_q[tt][lane + 32 * i];
-            }
-            float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int x = 0; x < 4; ++x) {
+                const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&s_kg[base + 4 * x]);
+                const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&s_qg[base + 4 * x]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    st[i][c] *= a[i];
-                    pk[c] = fmaf(st[i][c], kk[i], pk[c]);
-                    pq[c] = fmaf(st[i][c], qq[i], pq[c]);
+                for (int u = 0; u < 2; ++u) {
+                    pk[0][u] = f2_fma(st[2 * x][u], a.x, pk[0][u]);
+                    pk[1][u] = f2_fma(st[2 * x + 1][u], a.y, pk[1][u]);
+                    pq[0][u] = f2_fma(st[2 * x][u], b.x, pq[0][u]);
+                    pq[1][u] = f2_fma(st[2 * x + 1][u], b.y, pq[1][u]);
                 }
             }
+            float sk[2], sq[2];
 #pragma unroll
-            for (int m = 16; m > 0; m >>= 1) {
+            for (int u = 0; u < 2; ++u) {
+                const float2 k0 = f2_unpack(pk[0][u]), k1 = f2_unpack(pk[1][u]);
+                const float2 q0 = f2_unpack(pq[0][u]), q1 = f2_unpack(pq[1][u]);
+                sk[u] = (k0.x + k0.y) + (k1.x + k1.y);
+                sq[u] = (q0.x + q0.y) + (q1.x + q1.y);
+            }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], m);
-                    pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], m);
+            for (int m = 4; m <= 16; m <<= 1) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], m);
+                    sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], m);
                 }
             }
             const float b = s_b[tt], kq = s_kq[tt];
+            const float2 vv = *reinterpret_cast<const float2*>(&s_v[tt][lcol]);
+            const float u0 = b * (vv.x - sk[0]), u1 = b * (vv.y - sk[1]);
+            if (rq == 0)
+                *reinterpret_cast<float2*>(&s_o[tt][lcol]) = make_float2(fmaf(u0, kq, sq[0]), fmaf(u1, kq, sq[1]));
+            const uint64_t uu[2] = {f2_pack(u0, u0), f2_pack(u1, u1)};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float u = b * (s_v[tt][wcol + c] - pk[c]);
+            for (int x = 0; x < 4; ++x) {
+                const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&s_kh[base + 4 * x]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) st[i][c] = fmaf(kk[i], u, st[i][c]);
-                if (lane == c) s_o[tt][wcol + c] = fmaf(u, kq, pq[c]);
+                for (int u = 0; u < 2; ++u) {
+                    st[2 * x][u] = f2_fma(a.x, uu[u], st[2 * x][u]);
+                    st[2 * x + 1][u] = f2_fma(a.y, uu[u], st[2 * x + 1][u]);
+                }
+            }
+            // end of a run: back from R to S
+            if ((tt & (kRecRun - 1)) == kRecRun - 1 || tt == nt - 1) {
+                const float* gl = &s_glast[tt / kRecRun][rq * 20];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(gl + 4 * x);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        st[2 * x][u] = f2_mul(st[2 * x][u], a.x);
+                        st[2 * x + 1][u] = f2_mul(st[2 * x + 1][u], a.y);
+                    }
+                }
             }
         }
         __syncthreads();
@@ -166,31 +261,11 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         }
         // Checkpoint: the state after every `ck.every` tokens of this sequence.
         const int64_t done = t0 + nt - bos;
-        if (ck.out && done % ck.every == 0 && done / ck.every <= ck.max_count) {
-            float* dst = ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = col0 + wcol + c;
-                    if (r < dk && j < dv) dst[(size_t)r * dv + j] = st[i][c];
-                }
-            }
-        }
+        if (ck.out && done % ck.every == 0 && done / ck.every <= ck.max_count)
+            store_state(ck.out + (((size_t)n * H + h) * ck.max_count + (done / ck.every - 1)) * dk * dv);
     }
 
-    if (S1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = lane + 32 * i;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int j = col0 + wcol + c;
-                if (r < dk && j < dv) S1[sbase + (size_t)r * dv + j] = st[i][c];
-            }
-        }
-    }
+    if (S1) store_state(S1 + sbase);
 }
 
 cudaError_t run_recurrent(const void* q, const void* k, const void* v, const void* z,
