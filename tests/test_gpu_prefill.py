@@ -52,7 +52,7 @@ def test_tiny_fp32_workload():
 
 @pytest.mark.parametrize("chunk", [16, 64])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (32, 64), (20, 12), (64, 128)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (32, 64), (20, 12), (64, 128), (17, 13), (128, 65)])
 def test_fixed_length_shapes(dtype, dk, dv, chunk):
     w = replace(WORKLOADS[1], dk=dk, dv=dv, dtype=dtype, H=3, seed=dk + dv + chunk,
                 initial_state=True)
