@@ -402,80 +402,88 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
         if (t == n_steps - 1) s_gam[c] = gam;
     }
     __syncthreads();
-    // R = S on entry (gam_0 = 1).
+    // R = S on entry (gam_0 = 1), held as row pairs sp[p][u] = (R[r0 + 2p][j0 + u],
+    // R[r0 + 2p + 1][j0 + u]) on which packed two-lane FMAs run.
     cp_async_wait_all_own();
-    float2 s[32];
+    uint64_t sp[16][2];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) s[i] = s_stage[i * kDecodeThreads + tid];
+    for (int p = 0; p < 16; ++p) {
+        const float2 a = s_stage[(2 * p) * kDecodeThreads + tid], c = s_stage[(2 * p + 1) * kDecodeThreads + tid];
+        sp[p][0] = f2_pack(a.x, c.x);
+        sp[p][1] = f2_pack(a.y, c.y);
+    }
 
     for (int t = 0; t < n_steps; ++t) {
-        // two partial sums per column and vector halve the dependent FMA chains
-        float pk[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, pq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        const float4* kg4 = reinterpret_cast<const float4*>(&s_kg[t][36 * rq]);
-        const float4* qg4 = reinterpret_cast<const float4*>(&s_qg[t][36 * rq]);
+        // two accumulators per column and vector halve the dependent FMA chains
+        uint64_t pk[2][2] = {{0ull, 0ull}, {0ull, 0ull}}, pq[2][2] = {{0ull, 0ull}, {0ull, 0ull}};
+        const ulonglong2* kg2 = reinterpret_cast<const ulonglong2*>(&s_kg[t][36 * rq]);
+        const ulonglong2* qg2 = reinterpret_cast<const ulonglong2*>(&s_qg[t][36 * rq]);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-            const int hp = i4 & 1;
-            const float4 kg = kg4[i4];
-            const float kv[4] = {kg.x, kg.y, kg.z, kg.w};
+            const ulonglong2 kg = kg2[i4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                pk[hp][0] = fmaf(s[4 * i4 + e].x, kv[e], pk[hp][0]);
-                pk[hp][1] = fmaf(s[4 * i4 + e].y, kv[e], pk[hp][1]);
+            for (int u = 0; u < 2; ++u) {
+                pk[0][u] = f2_fma(sp[2 * i4][u], kg.x, pk[0][u]);
+                pk[1][u] = f2_fma(sp[2 * i4 + 1][u], kg.y, pk[1][u]);
             }
             if (kVerify) {
-                const float4 qg = qg4[i4];
-                const float qv[4] = {qg.x, qg.y, qg.z, qg.w};
+                const ulonglong2 qg = qg2[i4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    pq[hp][0] = fmaf(s[4 * i4 + e].x, qv[e], pq[hp][0]);
-                    pq[hp][1] = fmaf(s[4 * i4 + e].y, qv[e], pq[hp][1]);
+                for (int u = 0; u < 2; ++u) {
+                    pq[0][u] = f2_fma(sp[2 * i4][u], qg.x, pq[0][u]);
+                    pq[1][u] = f2_fma(sp[2 * i4 + 1][u], qg.y, pq[1][u]);
                 }
             }
         }
-        pk[0][0] += pk[1][0];
-        pk[0][1] += pk[1][1];
-        pq[0][0] += pq[1][0];
-        pq[0][1] += pq[1][1];
+        float sk[2], sq[2] = {0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float2 k0 = f2_unpack(pk[0][u]), k1 = f2_unpack(pk[1][u]);
+            sk[u] = (k0.x + k0.y) + (k1.x + k1.y);
+            if (kVerify) {
+                const float2 q0 = f2_unpack(pq[0][u]), q1 = f2_unpack(pq[1][u]);
+                sq[u] = (q0.x + q0.y) + (q1.x + q1.y);
+            }
+        }
 #pragma unroll
         for (int m = 8; m <= 16; m <<= 1) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                pk[0][c] += __shfl_xor_sync(0xffffffffu, pk[0][c], m);
-                if (kVerify) pq[0][c] += __shfl_xor_sync(0xffffffffu, pq[0][c], m);
+                sk[c] += __shfl_xor_sync(0xffffffffu, sk[c], m);
+                if (kVerify) sq[c] += __shfl_xor_sync(0xffffffffu, sq[c], m);
             }
         }
         const float bt = s_b[t];
         const float2 vv = col_ok ? *reinterpret_cast<const float2*>(&s_v[t][j0]) : make_float2(0.f, 0.f);
-        const float u0 = bt * (vv.x - pk[0][0]), u1 = bt * (vv.y - pk[0][1]);
+        const float u0 = bt * (vv.x - sk[0]), u1 = bt * (vv.y - sk[1]);
         if (kVerify && col_ok && rq == 0) {
             const float kq = s_kq[t];
             T* ob = o + (((size_t)b * Tn + t) * H + h) * dv + j0;
-            ob[0] = from_f32<T>(fmaf(u0, kq, pq[0][0]));
-            ob[1] = from_f32<T>(fmaf(u1, kq, pq[0][1]));
+            ob[0] = from_f32<T>(fmaf(u0, kq, sq[0]));
+            ob[1] = from_f32<T>(fmaf(u1, kq, sq[1]));
         }
         if (!kVerify || t + 1 < n_steps) {
-            const float4* kh4 = reinterpret_cast<const float4*>(&s_kh[t][36 * rq]);
+            const ulonglong2* kh2 = reinterpret_cast<const ulonglong2*>(&s_kh[t][36 * rq]);
+            const uint64_t uu[2] = {f2_pack(u0, u0), f2_pack(u1, u1)};
 #pragma unroll
             for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 kh = kh4[i4];
-                const float kv[4] = {kh.x, kh.y, kh.z, kh.w};
+                const ulonglong2 kh = kh2[i4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s[4 * i4 + e].x = fmaf(kv[e], u0, s[4 * i4 + e].x);
-                    s[4 * i4 + e].y = fmaf(kv[e], u1, s[4 * i4 + e].y);
+                for (int u = 0; u < 2; ++u) {
+                    sp[2 * i4][u] = f2_fma(kh.x, uu[u], sp[2 * i4][u]);
+                    sp[2 * i4 + 1][u] = f2_fma(kh.y, uu[u], sp[2 * i4 + 1][u]);
                 }
             }
         }
     }
     if (!kVerify) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = r0 + i;
-            if (col_ok && r < dk) {
-                const float g = s_gam[r];
-                __stcs(reinterpret_cast<float2*>(Sbh + (size_t)r * dv + j0), make_float2(g * s[i].x, g * s[i].y));
-            }
+        for (int p = 0; p < 16; ++p) {
+            const int r = r0 + 2 * p;
+            const uint64_t g = f2_pack(s_gam[r & 127], s_gam[(r + 1) & 127]);
+            const float2 a = f2_unpack(f2_mul(sp[p][0], g)), c = f2_unpack(f2_mul(sp[p][1], g));
+            if (col_ok && r < dk) __stcs(reinterpret_cast<float2*>(Sbh + (size_t)r * dv + j0), make_float2(a.x, c.x));
+            if (col_ok && r + 1 < dk) __stcs(reinterpret_cast<float2*>(Sbh + (size_t)(r + 1) * dv + j0), make_float2(a.y, c.y));
         }
     }
 }
