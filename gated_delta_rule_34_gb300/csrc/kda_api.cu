@@ -516,9 +516,11 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
     KDA_REQUIRE_PTR(state);
     KDA_REQUIRE_PTR(o);
     kda::profile_event(0, stream);
-    // bf16 heads with d_k and d_v multiples of 16: the draft span is one
-    // 16-token chunk on the tensor cores; otherwise token by token in fp32.
-    const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0;
+    // bf16 heads with d_k and d_v multiples of 16 and more than 4 draft tokens:
+    // the draft span is one 16-token chunk on the tensor cores; otherwise token
+    // by token in fp32 (up to 4 tokens that is as fast or faster: 0.156 against
+    // 0.232 ms at T = 1, 0.230 against 0.236 ms at T = 4, for B = 256, H = 32).
+    const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0 && T > 4;
     const cudaError_t e =
         tc ? kda::run_spec_verify_tc(q, k, v, z, beta, A, state, o, B, T, H, d_k, d_v, stream)
            : kda::run_spec(q, k, v, z, beta, A, const_cast<float*>(state), o, nullptr, B, T, H, d_k,
