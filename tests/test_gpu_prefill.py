@@ -67,6 +67,17 @@ def test_packed_sequences(lengths):
     check_full(x, 64, torch.bfloat16, f"packed {lengths}")
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 128), (torch.bfloat16, 48)])
+def test_packed_sequences_recurrent(dtype, d):
+    # The fp32 recurrence on a packed batch (empty, one-token and ragged sequences;
+    # runs of 8 tokens and 16-token tiles cut at every sequence start).
+    lengths = [1, 64, 65, 130, 0, 7, 23]
+    w = replace(WORKLOADS[4], H=2, dk=d, dv=d, dtype=dtype, seed=90 + d)
+    x = make_inputs(w, lengths=lengths)
+    assert kda.prefill_path(d, d, 64, dtype) == "recurrent"
+    check_full(x, 64, dtype, f"packed {lengths} {dtype} d={d}")
+
+
 def test_no_initial_state_and_no_final_state():
     w = replace(WORKLOADS[1], H=2, seed=77)
     x = make_inputs(w, B=1, T=90)
