@@ -357,23 +357,36 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     __shared__ __align__(16) float s_v[kSpecMaxT][128], s_L[kSpecMaxT][128];
     __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_kqp[kSpecMaxT][4], s_gam[128];
     // (a) every (token, channel) at once: raw k and q, v, the gate g, and k^T q
-    //     partial sums over each warp's 32 channels.
-    for (int idx = tid; idx < n_steps * 128; idx += kDecodeThreads) {
-        const int t = idx >> 7, c = idx & 127;
-        const size_t row = ((size_t)b * Tn + t) * H + h;
-        float kk = 0.f, qq = 0.f, g = 0.f;
-        if (c < dk) {
-            kk = to_f32(k[row * dk + c]);
-            if (kVerify) qq = to_f32(q[row * dk + c]);
-            g = gate_accurate(expf(A[(size_t)h * dk + c]), to_f32(z[row * dk + c]));
-        }
-        s_kh[t][spec_row(c)] = kk;
-        s_qg[t][spec_row(c)] = qq;
-        s_L[t][c] = g;
-        s_v[t][c] = c < dv ? to_f32(v[row * dv + c]) : 0.f;
+    //     partial sums over each warp's 32 channels.  Thread (token
+    //     tid / 128 + 2 i, channel tid mod 128) issues all of its loads first,
+    //     so that one memory round trip covers the span.
+    constexpr int kPer = kSpecMaxT * 128 / kDecodeThreads;
+    const int ch = tid & 127;
+    T xk[kPer], xq[kPer], xz[kPer], xv[kPer];
+    const float eA = ch < dk ? A[(size_t)h * dk + ch] : 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int t = (tid >> 7) + 2 * i;
+        const size_t row = ((size_t)b * Tn + (t < n_steps ? t : 0)) * H + h;
+        const bool live = t < n_steps;
+        xk[i] = (live && ch < dk) ? k[row * dk + ch] : from_f32<T>(0.f);
+        xq[i] = (kVerify && live && ch < dk) ? q[row * dk + ch] : from_f32<T>(0.f);
+        xz[i] = (live && ch < dk) ? z[row * dk + ch] : from_f32<T>(0.f);
+        xv[i] = (live && ch < dv) ? v[row * dv + ch] : from_f32<T>(0.f);
+    }
+    const float expA = expf(eA);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int t = (tid >> 7) + 2 * i;
+        if (t >= n_steps) continue;                     // uniform per warp
+        const float kk = to_f32(xk[i]), qq = to_f32(xq[i]);
+        s_kh[t][spec_row(ch)] = kk;
+        s_qg[t][spec_row(ch)] = qq;
+        s_L[t][ch] = ch < dk ? gate_accurate(expA, to_f32(xz[i])) : 0.f;
+        s_v[t][ch] = to_f32(xv[i]);
         if (kVerify) {
             const float p = warp_sum(kk * qq);
-            if (lane == 0) s_kqp[t][c >> 5] = p;
+            if (lane == 0) s_kqp[t][ch >> 5] = p;
         }
     }
     if (tid < n_steps) s_b[tid] = to_f32(beta[((size_t)b * Tn + tid) * H + h]);
