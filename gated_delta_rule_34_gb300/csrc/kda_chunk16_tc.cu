@@ -144,13 +144,6 @@ __device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// 8 bf16 of row `row` of a [T_total][H][d] tensor, channels 8 c8 .. (zeros past d).
-__device__ __forceinline__ uint4 load8(const __nv_bfloat16* __restrict__ x, int64_t row, int H, int h,
-                                       int d, int c8) {
-    if (8 * c8 >= d) return make_uint4(0, 0, 0, 0);
-    return __ldg(reinterpret_cast<const uint4*>(x + ((size_t)row * H + h) * d + 8 * c8));
-}
-
 // Tensor maps of the inputs [T_total][H][d] with boxes of 16 tokens x 1 head x
 // 128 channels (4 KB): a chunk's tile of each input is one TMA load.
 struct InputMaps16 {
@@ -580,23 +573,27 @@ chunk16_kernel(const __grid_constant__ InputMaps16 maps, const __nv_bfloat16* __
 // chip instead of a state copy per token).  With L_t, E, P, T, W and U~ as
 // above and S the state before the span:
 //   U = U~ - W S,   O = (q E) S + P U
-// One CTA of eight warps per (b, h), two per SM: the state's 64 values per
-// thread are loaded first and land while the gate, scan, operands, A/P, the
-// solve and W^T, U~^T run; then S^T (bf16) [W ; qE]^T, U^T and O^T += U^T P^T.
-// The state is only read.  A bounded wait that gives up leaves NaN in that
-// (b, h)'s outputs.
+// Persistent: CTAs of eight warps, two per SM, each walking the (b, h) pairs
+// blockIdx.x, blockIdx.x + gridDim.x, ...  Per pair: the gate and its running
+// sum, the operands, A/P, the solve and W^T, U~^T, then S^T (bf16) [W ; qE]^T,
+// U^T and O^T += U^T P^T.  The next pair's loads are issued as soon as their
+// buffers are free, so that they land while this pair computes: its draft
+// inputs (cp.async, each thread its own 16-byte slots) once the operands are
+// built, its state (64 values per thread, in registers) once S^T is copied.
+// The state is only read.  A bounded wait that gives up leaves NaN in the
+// outputs of that pair and of the CTA's remaining pairs.
 // ---------------------------------------------------------------------------
 constexpr int kVThreads = 256;
 constexpr uint32_t V_ST = 0;          // S^T bf16 [128 j][128 c]: two K-blocks of 16 KB, swizzled
 constexpr uint32_t V_UT = 32768;      // U^T bf16 [128 j][16 t]
-constexpr uint32_t V_APA = 49152;     // [kE ; qE ; 0] [64 rows][128 c]
+constexpr uint32_t V_APA = 49152;     // [kE ; qE ; *] [64 rows][128 c]
 constexpr uint32_t V_APB = 65536;     // k/E [16 s][128 c]
 constexpr uint32_t V_SB = 69632;      // [W ; qE] [32 rows][128 c]
 constexpr uint32_t V_BKG = 77824;     // b kE token rows (MN-major)
 constexpr uint32_t V_BV = 81920;      // b V token rows (MN-major)
 constexpr uint32_t V_PB = 86016;      // P [16 t][16 s]
 constexpr uint32_t V_TB = 88064;      // T [16 t][16 s]
-constexpr uint32_t V_GS = 90112;      // g, then L: fp32 [16 t][128 c]
+constexpr uint32_t V_IN2 = 90112;     // next pair's v and z: 256 threads x 16 B each
 constexpr uint32_t V_AF = 98304;      // A fp32 [16][17]
 constexpr uint32_t V_EA = 99584;      // e^{A_h} [128]
 constexpr uint32_t V_BETA = 100096;   // beta [16]
@@ -604,6 +601,14 @@ constexpr uint32_t V_BAR = 100160;    // mbarrier, TMEM slot
 constexpr uint32_t V_SMEM = V_BAR + 64 + 1024;
 static_assert(2 * (V_SMEM + 1024) <= 233472, "two verify CTAs per SM");
 constexpr uint32_t kVTmemCols = 128;
+// The next pair's k and q sit in rows 32..63 of the A/P operand (4 KB in each
+// K-block).  Those rows only feed accumulator rows 32..63 (TMEM lanes 64..79
+// and 96..111 of columns T_AP..T_AP + 15), which are never read, so whatever
+// they hold while the A/P product runs leaves A and P unchanged.
+constexpr uint32_t V_IN_K = V_APA + 4096;
+constexpr uint32_t V_IN_Q = V_APA + 8192 + 4096;
+constexpr uint32_t V_IN_V = V_IN2;
+constexpr uint32_t V_IN_Z = V_IN2 + 4096;
 
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
     const bool ok = mbar_wait(bar, phase);
@@ -612,49 +617,74 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
     return __syncthreads_and(ok) != 0;
 }
 
+// Copies this thread's 16 bytes of token row `row`, channels 8 c8 .. + 7, of
+// one [rows][H][d] input into its own slot; zeros where the row or the
+// channels are absent.
+__device__ __forceinline__ void fetch8(uint8_t* slot, const __nv_bfloat16* __restrict__ x, int64_t row,
+                                       bool live, int H, int h, int d, int c8) {
+    const bool in = live && 8 * c8 < d;
+    const __nv_bfloat16* src = in ? x + ((size_t)row * H + h) * d + 8 * c8 : x;
+    cp_async16(slot, src, in ? 16u : 0u);
+}
+
 __global__ void __launch_bounds__(kVThreads, 2)
 spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ z,
                    const __nv_bfloat16* __restrict__ beta, const float* __restrict__ A,
-                   const float* __restrict__ state, __nv_bfloat16* __restrict__ o, int Tn, int H,
-                   int dk, int dv) {
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+                   const float* __restrict__ state, __nv_bfloat16* __restrict__ o, int n_pairs,
+                   int Tn, int H, int dk, int dv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float* gs = reinterpret_cast<float*>(sm + V_GS);
     float* af = reinterpret_cast<float*>(sm + V_AF);
     float* ea = reinterpret_cast<float*>(sm + V_EA);
     float* bs = reinterpret_cast<float*>(sm + V_BETA);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + V_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + V_BAR + 8);
-    const int tt = tid >> 4, c8 = tid & 15;               // token tt, channels 8 c8 .. + 7
+    // token tt, channels 8 c8 .. + 7: a warp holds all 16 tokens of two channel
+    // groups, so the running sum over the span is a 16-lane shuffle scan
+    const int tt = lane & 15, c8 = 2 * warp + (lane >> 4);
     const int j = 32 * (warp & 3) + lane, ch = warp >> 2;  // state column j, channel half ch
     const uint32_t tl = (uint32_t)(32 * (warp & 3)) << 16;
-
-    // The state read first: S[64 ch + e][j], landing during the preparation.
-    const float* Sbh = state + (size_t)bh * dk * dv;
-    float st[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) {
-        const int c = 64 * ch + e;
-        st[e] = (c < dk && j < dv) ? __ldcs(Sbh + (size_t)c * dv + j) : 0.f;
-    }
     const bool live = tt < Tn;
-    const int64_t row = (int64_t)b * Tn + tt;             // token row of [B, Tn, H, d]
-    const uint4 kr = live ? load8(k, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
-    const uint4 qr = live ? load8(q, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
-    const uint4 vr = live ? load8(v, row, H, h, dv, c8) : make_uint4(0, 0, 0, 0);
-    const uint4 zr = live ? load8(z, row, H, h, dk, c8) : make_uint4(0, 0, 0, 0);
+    uint8_t* const slot_k = sm + V_IN_K + 16 * tid;
+    uint8_t* const slot_q = sm + V_IN_Q + 16 * tid;
+    uint8_t* const slot_v = sm + V_IN_V + 16 * tid;
+    uint8_t* const slot_z = sm + V_IN_Z + 16 * tid;
 
     if (warp == 0) tmem_alloc<kVTmemCols>(tslot);
     if (tid == 32) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < 4096; i += kVThreads) reinterpret_cast<uint32_t*>(sm + V_APA)[i] = 0u;
-    if (tid < 128) ea[tid] = tid < dk ? __expf(A[(size_t)h * dk + tid]) : 0.f;
-    if (tid < kC) bs[tid] = tid < Tn ? __bfloat162float(beta[((size_t)b * Tn + tid) * H + h]) : 0.f;
+
+    // The first pair's loads: its draft inputs first, so that they do not queue
+    // behind the state, then the state S[64 ch + e][j].
+    int pair = blockIdx.x;
+    float a_h = 0.f, b_t = 0.f;                 // the pair's e^{A} exponent and beta, per thread
+    float st[64];
+    auto fetch_inputs = [&](int p) {
+        const int pb = p / H, ph = p - pb * H;
+        const int64_t row = (int64_t)pb * Tn + tt;        // token row of [B, Tn, H, d]
+        fetch8(slot_k, k, row, live, H, ph, dk, c8);
+        fetch8(slot_q, q, row, live, H, ph, dk, c8);
+        fetch8(slot_v, v, row, live, H, ph, dv, c8);
+        fetch8(slot_z, z, row, live, H, ph, dk, c8);
+        a_h = (tid < 128 && tid < dk) ? A[(size_t)ph * dk + tid] : 0.f;
+        b_t = (tid < kC && tid < Tn) ? __bfloat162float(beta[((size_t)pb * Tn + tid) * H + ph]) : 0.f;
+    };
+    auto fetch_state = [&](int p) {
+        const float* Sp = state + (size_t)p * dk * dv;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const int c = 64 * ch + e;
+            st[e] = (c < dk && j < dv) ? __ldcs(Sp + (size_t)c * dv + j) : 0.f;
+        }
+    };
+    if (pair < n_pairs) {
+        fetch_inputs(pair);
+        fetch_state(pair);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -662,208 +692,222 @@ spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     uint32_t phase = 0;
     bool ok = true;
 
-    do {
-        // ---- gate -> gs; running sum per channel
-        {
-            float zf[8], g[8];
-            unpack8(zr, zf);
+    for (; pair < n_pairs; pair += gridDim.x) {
+        const int b = pair / H, h = pair - b * H;
+        const int next = pair + gridDim.x;
+        if (ok) do {
+            if (tid < 128) ea[tid] = tid < dk ? __expf(a_h) : 0.f;
+            if (tid < kC) bs[tid] = b_t;
+            cp_async_wait_all();                    // this thread's own slots have landed
+            __syncthreads();
+            // ---- gate, and its running sum L over the span (inclusive shuffle scan)
+            {
+                const uint4 zr = *reinterpret_cast<const uint4*>(slot_z);
+                float zf[8], L[8];
+                unpack8(zr, zf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = 8 * c8 + e;
-                g[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const int c = 8 * c8 + e;
+                    L[e] = (live && c < dk) ? gate_fast(ea[c], zf[e]) : 0.f;
+                }
+#pragma unroll
+                for (int off = 1; off < kC; off <<= 1) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float y = __shfl_up_sync(0xffffffffu, L[e], off, kC);
+                        if (tt >= off) L[e] += y;
+                    }
+                }
+                // ---- decay-scaled operands of token tt
+                const uint4 kr = *reinterpret_cast<const uint4*>(slot_k);
+                const uint4 qr = *reinterpret_cast<const uint4*>(slot_q);
+                const uint4 vr = *reinterpret_cast<const uint4*>(slot_v);
+                float kf[8], qf[8], vf[8], E[8], o8[8];
+                unpack8(kr, kf);
+                unpack8(qr, qf);
+                unpack8(vr, vf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) E[e] = __expf(L[e]);
+                const float bt = bs[tt];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
+                store_row8(sm + V_APA, 8192, tt, c8, o8);                           // k E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
+                store_row8(sm + V_BKG, 2048, tt, c8, o8);                           // b k E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
+                store_row8(sm + V_APA, 8192, 16 + tt, c8, o8);                      // q E
+                store_row8(sm + V_SB, 4096, 16 + tt, c8, o8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = kf[e] * __fdividef(1.0f, E[e]);
+                store_row8(sm + V_APB, 2048, tt, c8, o8);                           // k / E
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
+                store_row8(sm + V_BV, 2048, tt, c8, o8);                            // b V
             }
-            float4* gp = reinterpret_cast<float4*>(gs + tt * 128 + 8 * c8);
-            gp[0] = make_float4(g[0], g[1], g[2], g[3]);
-            gp[1] = make_float4(g[4], g[5], g[6], g[7]);
-        }
-        __syncthreads();
-        if (tid < 128) {
-            float run = 0.f;
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // every slot has been read: the next pair's inputs start now
+            if (next < n_pairs) fetch_inputs(next);
+            // ---- A and P (M=64 N=16 K=128)
+            if (tid == 0) {
+                const uint32_t idesc = idesc_bf16(64, 16);
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                run += gs[t * 128 + tid];
-                gs[t * 128 + tid] = run;
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + V_APA + kb * 8192 + off)),
+                             desc_sw128(smem_u32(sm + V_APB + kb * 2048 + off)), idesc, ks > 0);
+                }
+                mma_commit(bar);
             }
-        }
-        __syncthreads();
-        // ---- decay-scaled operands of token tt
-        {
-            float kf[8], qf[8], vf[8], E[8], o8[8];
-            unpack8(kr, kf);
-            unpack8(qr, qf);
-            unpack8(vr, vf);
-            const float4* lp = reinterpret_cast<const float4*>(gs + tt * 128 + 8 * c8);
-            const float4 l0 = lp[0], l1 = lp[1];
-            const float L[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+            if (!(ok = cta_wait(bar, phase))) break;
+            if (warp < 2) {
+                float d[16];
+                tmem_ld16(tbase + tl + T_AP, d);
+                tmem_wait_ld();
+                if (lane < kC) {
+                    const int t = lane;
+                    if (warp == 0) {
+                        const float bt = bs[t];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) E[e] = __expf(L[e]);
-            const float bt = bs[tt];
+                        for (int s2 = 0; s2 < kC; ++s2) af[t * 17 + s2] = s2 < t ? bt * d[s2] : 0.f;
+                    } else {
+                        float p8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * E[e];
-            store_row8(sm + V_APA, 8192, tt, c8, o8);                           // k E
+                        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = bt * o8[e];
-            store_row8(sm + V_BKG, 2048, tt, c8, o8);                           // b k E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = qf[e] * E[e];
-            store_row8(sm + V_APA, 8192, 16 + tt, c8, o8);                      // q E
-            store_row8(sm + V_SB, 4096, 16 + tt, c8, o8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = kf[e] * __fdividef(1.0f, E[e]);
-            store_row8(sm + V_APB, 2048, tt, c8, o8);                           // k / E
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = bt * vf[e];
-            store_row8(sm + V_BV, 2048, tt, c8, o8);                            // b V
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // ---- A and P (M=64 N=16 K=128)
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(64, 16);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                mma_bf16(tbase + T_AP, desc_sw128(smem_u32(sm + V_APA + kb * 8192 + off)),
-                         desc_sw128(smem_u32(sm + V_APB + kb * 2048 + off)), idesc, ks > 0);
-            }
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        if (warp < 2) {
-            float d[16];
-            tmem_ld16(tbase + tl + T_AP, d);
-            tmem_wait_ld();
-            if (lane < kC) {
-                const int t = lane;
-                if (warp == 0) {
-                    const float bt = bs[t];
-#pragma unroll
-                    for (int s2 = 0; s2 < kC; ++s2) af[t * 17 + s2] = s2 < t ? bt * d[s2] : 0.f;
-                } else {
-                    float p8[8];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
-                        uint4 r;
-                        r.x = pack_bf16x2(p8[0], p8[1]);
-                        r.y = pack_bf16x2(p8[2], p8[3]);
-                        r.z = pack_bf16x2(p8[4], p8[5]);
-                        r.w = pack_bf16x2(p8[6], p8[7]);
-                        *reinterpret_cast<uint4*>(sm + V_PB + sw128(t, hh)) = r;
+                            for (int e = 0; e < 8; ++e) p8[e] = (8 * hh + e <= t) ? d[8 * hh + e] : 0.f;
+                            uint4 r;
+                            r.x = pack_bf16x2(p8[0], p8[1]);
+                            r.y = pack_bf16x2(p8[2], p8[3]);
+                            r.z = pack_bf16x2(p8[4], p8[5]);
+                            r.w = pack_bf16x2(p8[6], p8[7]);
+                            *reinterpret_cast<uint4*>(sm + V_PB + sw128(t, hh)) = r;
+                        }
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-        // ---- T = (I + A)^{-1}
-        if (tid < kC) {
-            const int jc = tid;
-            float x[kC];
+            tc_fence_before();
+            __syncthreads();
+            // ---- T = (I + A)^{-1}
+            if (tid < kC) {
+                const int jc = tid;
+                float x[kC];
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                float acc = 0.f;
+                for (int r = 0; r < kC; ++r) {
+                    float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
-                x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+                    for (int m = 0; m < r; ++m) acc = fmaf(af[r * 17 + m], x[m], acc);
+                    x[r] = (r < jc) ? 0.f : (r == jc ? 1.f : -acc);
+                }
+#pragma unroll
+                for (int r = 0; r < kC; ++r)
+                    *reinterpret_cast<__nv_bfloat16*>(sm + V_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
+                        __float2bfloat16_rn(x[r]);
             }
-#pragma unroll
-            for (int r = 0; r < kC; ++r)
-                *reinterpret_cast<__nv_bfloat16*>(sm + V_TB + sw128(r, jc >> 3) + (jc & 7) * 2) =
-                    __float2bfloat16_rn(x[r]);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // ---- W^T and U~^T (M=128 N=16 K=16, A MN-major)
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16_amn(128, 16);
-            const uint64_t tb = desc_sw128(smem_u32(sm + V_TB));
-            mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + V_BKG), 2048, 1024), tb, idesc, false);
-            mma_bf16(tbase + T_UT, desc_sw128_mn(smem_u32(sm + V_BV), 2048, 1024), tb, idesc, false);
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        if (warp < 4) {
-            float w[16];
-            tmem_ld16(tbase + tl + T_WT, w);
-            tmem_wait_ld();
-            const int c = 32 * warp + lane;
-#pragma unroll
-            for (int t = 0; t < kC; ++t)
-                *reinterpret_cast<__nv_bfloat16*>(sm + V_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
-                                                   (c & 7) * 2) = __float2bfloat16_rn(w[t]);
-        }
-        // ---- the state's bf16 copy S^T, row j (its loads have landed by now)
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-            uint4 r;
-            r.x = pack_bf16x2(st[8 * q8 + 0], st[8 * q8 + 1]);
-            r.y = pack_bf16x2(st[8 * q8 + 2], st[8 * q8 + 3]);
-            r.z = pack_bf16x2(st[8 * q8 + 4], st[8 * q8 + 5]);
-            r.w = pack_bf16x2(st[8 * q8 + 6], st[8 * q8 + 7]);
-            *reinterpret_cast<uint4*>(sm + V_ST + ch * 16384 + sw128(j, q8)) = r;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T (M=128 N=32 K=128)
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 32);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-                mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + V_ST + kb * 16384 + off)),
-                         desc_sw128(smem_u32(sm + V_SB + kb * 4096 + off)), idesc, ks > 0);
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // ---- W^T and U~^T (M=128 N=16 K=16, A MN-major)
+            if (tid == 0) {
+                const uint32_t idesc = idesc_bf16_amn(128, 16);
+                const uint64_t tb = desc_sw128(smem_u32(sm + V_TB));
+                mma_bf16(tbase + T_WT, desc_sw128_mn(smem_u32(sm + V_BKG), 2048, 1024), tb, idesc, false);
+                mma_bf16(tbase + T_UT, desc_sw128_mn(smem_u32(sm + V_BV), 2048, 1024), tb, idesc, false);
+                mma_commit(bar);
             }
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-        if (warp < 4) {
-            float ws_[16], ut[16];
-            tmem_ld16(tbase + tl + T_ST, ws_);
-            tmem_ld16(tbase + tl + T_UT, ut);
-            tmem_wait_ld();
+            if (!(ok = cta_wait(bar, phase))) break;
+            if (warp < 4) {
+                float w[16];
+                tmem_ld16(tbase + tl + T_WT, w);
+                tmem_wait_ld();
+                const int c = 32 * warp + lane;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+                for (int t = 0; t < kC; ++t)
+                    *reinterpret_cast<__nv_bfloat16*>(sm + V_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
+                                                       (c & 7) * 2) = __float2bfloat16_rn(w[t]);
+            }
+            // ---- the state's bf16 copy S^T, row j (its loads have landed by now)
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
                 uint4 r;
-                r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
-                r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
-                r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
-                r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
-                *reinterpret_cast<uint4*>(sm + V_UT + sw128(j, hh)) = r;
+                r.x = pack_bf16x2(st[8 * q8 + 0], st[8 * q8 + 1]);
+                r.y = pack_bf16x2(st[8 * q8 + 2], st[8 * q8 + 3]);
+                r.z = pack_bf16x2(st[8 * q8 + 4], st[8 * q8 + 5]);
+                r.w = pack_bf16x2(st[8 * q8 + 6], st[8 * q8 + 7]);
+                *reinterpret_cast<uint4*>(sm + V_ST + ch * 16384 + sw128(j, q8)) = r;
+            }
+            // the registers are free: the next pair's state starts now
+            if (next < n_pairs) fetch_state(next);
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // ---- [(W S)^T | (qE S)^T] = S^T [W ; qE]^T (M=128 N=32 K=128)
+            if (tid == 0) {
+                const uint32_t idesc = idesc_bf16(128, 32);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+                    mma_bf16(tbase + T_ST, desc_sw128(smem_u32(sm + V_ST + kb * 16384 + off)),
+                             desc_sw128(smem_u32(sm + V_SB + kb * 4096 + off)), idesc, ks > 0);
+                }
+                mma_commit(bar);
+            }
+            if (!(ok = cta_wait(bar, phase))) break;
+            if (warp < 4) {
+                float ws_[16], ut[16];
+                tmem_ld16(tbase + tl + T_ST, ws_);
+                tmem_ld16(tbase + tl + T_UT, ut);
+                tmem_wait_ld();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint4 r;
+                    r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
+                    r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
+                    r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
+                    r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
+                    *reinterpret_cast<uint4*>(sm + V_UT + sw128(j, hh)) = r;
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            // ---- O^T += U^T P^T (M=128 N=16 K=16)
+            if (tid == 0) {
+                mma_bf16(tbase + T_ST + 16, desc_sw128(smem_u32(sm + V_UT)), desc_sw128(smem_u32(sm + V_PB)),
+                         idesc_bf16(128, 16), true);
+                mma_commit(bar);
+            }
+            ok = cta_wait(bar, phase);
+        } while (false);
+
+        // ---- outputs o[b][t][h][j] (warps 0..3); NaN once a wait has given up
+        if (warp < 4) {
+            float ov[16];
+            if (ok) {
+                tmem_ld16(tbase + tl + T_ST + 16, ov);
+                tmem_wait_ld();
+            }
+            if (j < dv) {
+#pragma unroll
+                for (int t = 0; t < kC; ++t)
+                    if (t < Tn)
+                        o[(((size_t)b * Tn + t) * H + h) * dv + j] =
+                            __float2bfloat16_rn(ok ? ov[t] : __int_as_float(0x7fc00000));
             }
         }
-        fence_async_smem();
+        // this pair's TMEM reads are done before the next pair's products
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- O^T += U^T P^T (M=128 N=16 K=16)
-        if (tid == 0) {
-            mma_bf16(tbase + T_ST + 16, desc_sw128(smem_u32(sm + V_UT)), desc_sw128(smem_u32(sm + V_PB)),
-                     idesc_bf16(128, 16), true);
-            mma_commit(bar);
-        }
-        if (!(ok = cta_wait(bar, phase))) break;
-    } while (false);
-
-    // ---- outputs o[b][t][h][j] (warps 0..3); NaN if a wait gave up
-    if (warp < 4) {
-        float ov[16];
-        tmem_ld16(tbase + tl + T_ST + 16, ov);
-        tmem_wait_ld();
-        if (j < dv) {
-#pragma unroll
-            for (int t = 0; t < kC; ++t)
-                if (t < Tn)
-                    o[(((size_t)b * Tn + t) * H + h) * dv + j] = __float2bfloat16_rn(ok ? ov[t] : __int_as_float(0x7fc00000));
-        }
     }
+    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -930,11 +974,21 @@ cudaError_t run_spec_verify_tc(const void* q, const void* k, const void* v, cons
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
+    static int sm_count[kMaxDevices] = {};
+    if (sm_count[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t n_pairs = (int64_t)B * H;
+    if (n_pairs > INT32_MAX) return cudaErrorInvalidValue;
+    if (n_pairs == 0) return cudaSuccess;
+    // two persistent CTAs per SM walk the (b, h) pairs
+    const int64_t grid = n_pairs < 2LL * sm_count[dev] ? n_pairs : 2LL * sm_count[dev];
     using bf = __nv_bfloat16;
-    c16::spec_verify_kernel<<<(unsigned)((int64_t)B * H), c16::kVThreads, c16::V_SMEM, stream>>>(
+    c16::spec_verify_kernel<<<(unsigned)grid, c16::kVThreads, c16::V_SMEM, stream>>>(
         static_cast<const bf*>(q), static_cast<const bf*>(k), static_cast<const bf*>(v),
-        static_cast<const bf*>(z), static_cast<const bf*>(beta), A, state, static_cast<bf*>(o), Tn, H, dk,
-        dv);
+        static_cast<const bf*>(z), static_cast<const bf*>(beta), A, state, static_cast<bf*>(o),
+        (int)n_pairs, Tn, H, dk, dv);
     return cudaGetLastError();
 }
 
