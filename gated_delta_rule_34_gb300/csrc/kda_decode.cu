@@ -146,6 +146,9 @@ __device__ __forceinline__ void cp_async8_ca(void* dst_smem, const void* src) {
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst_smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(src) : "memory");
 }
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void cp_async_wait_all_own() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
             const T* __restrict__ z, const T* __restrict__ beta, const float* __restrict__ A,
             float* __restrict__ state, T* __restrict__ o, const int32_t* __restrict__ n_accept,
-            int Tn, int H, int dk, int dv) {
+            int Tn, int H, int dk, int dv, int pf_dist) {
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh % H;
     const int tid = threadIdx.x;
@@ -338,6 +341,20 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
         const int na = n_accept[b];
         n_steps = na < 0 ? 0 : (na > Tn ? Tn : na);
         if (n_steps == 0) return;                       // nothing accepted: S unchanged
+    }
+
+    // Verify asks L2 for the draft span of pair bh + pf_dist, which starts
+    // about one wave of CTAs later, so that its loads hit L2 instead of
+    // queueing behind the states being streamed: thread (part, tensor, token)
+    // takes one 128-byte line of one token row.  (In commit the same request
+    // costs more than it saves: the kernel has no registers to spare.)
+    if (kVerify && pf_dist > 0 && bh + pf_dist < (int)gridDim.x) {
+        const int p2 = bh + pf_dist, b2 = p2 / H, h2 = p2 - (p2 / H) * H;
+        const int t = tid & 15, which = (tid >> 4) & 3, part = tid >> 6;
+        const T* src = which == 0 ? k : which == 1 ? q : which == 2 ? v : z;
+        const int d = which == 2 ? dv : dk;
+        if (t < Tn && part * 128 < d * (int)sizeof(T))
+            prefetch_line_l2(reinterpret_cast<const char*>(src + ((size_t)(b2 * Tn + t) * H + h2) * d) + part * 128);
     }
 
     // The state read starts first: each thread copies its own 32 x 8 bytes into
@@ -490,13 +507,20 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
         }
     }
     if (!kVerify) {
+        // The row pointer is formed here, out of the compiler's sight, so that the
+        // 32 store addresses are not computed before the token loop and held
+        // through it (they would not fit in the registers left).
+        float* row = Sbh + (size_t)r0 * dv + j0;
+        asm volatile("mov.b64 %0, %0;" : "+l"(row));
 #pragma unroll
         for (int p = 0; p < 16; ++p) {
             const int r = r0 + 2 * p;
             const uint64_t g = f2_pack(s_gam[r & 127], s_gam[(r + 1) & 127]);
             const float2 a = f2_unpack(f2_mul(sp[p][0], g)), c = f2_unpack(f2_mul(sp[p][1], g));
-            if (col_ok && r < dk) __stcs(reinterpret_cast<float2*>(Sbh + (size_t)r * dv + j0), make_float2(a.x, c.x));
-            if (col_ok && r + 1 < dk) __stcs(reinterpret_cast<float2*>(Sbh + (size_t)(r + 1) * dv + j0), make_float2(a.y, c.y));
+            if (col_ok && r < dk) __stcs(reinterpret_cast<float2*>(row), make_float2(a.x, c.x));
+            row += dv;
+            if (col_ok && r + 1 < dk) __stcs(reinterpret_cast<float2*>(row), make_float2(a.y, c.y));
+            row += dv;
         }
     }
 }
@@ -507,10 +531,17 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
     const unsigned grid = (unsigned)((int64_t)B * H);
     constexpr int kMaxDevices = 64;
     static bool attr_done[kMaxDevices] = {};
+    static int sm_count[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (sm_count[dev] == 0) {
+        e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    // two CTAs per SM are resident: the pair one wave ahead
+    const int pf_dist = 2 * sm_count[dev];
     if (!attr_done[dev]) {
         const void* fns[4] = {(const void*)spec_kernel<__nv_bfloat16, true>,
                               (const void*)spec_kernel<__nv_bfloat16, false>,
@@ -530,10 +561,10 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
         auto kb = static_cast<const Tb*>(beta);
         if (verify)
             spec_kernel<Tb, true><<<grid, kDecodeThreads, kSpecStage, stream>>>(
-                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
+                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv, pf_dist);
         else
             spec_kernel<Tb, false><<<grid, kDecodeThreads, kSpecStage, stream>>>(
-                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv);
+                kq, kk, kv, kz, kb, A, state, static_cast<Tb*>(o), n_accept, Tn, H, dk, dv, pf_dist);
     } else {
         auto kq = static_cast<const float*>(q);
         auto kk = static_cast<const float*>(k);
@@ -542,10 +573,10 @@ cudaError_t run_spec(const void* q, const void* k, const void* v, const void* z,
         auto kb = static_cast<const float*>(beta);
         if (verify)
             spec_kernel<float, true><<<grid, kDecodeThreads, kSpecStage, stream>>>(
-                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
+                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv, pf_dist);
         else
             spec_kernel<float, false><<<grid, kDecodeThreads, kSpecStage, stream>>>(
-                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv);
+                kq, kk, kv, kz, kb, A, state, static_cast<float*>(o), n_accept, Tn, H, dk, dv, pf_dist);
     }
     return cudaGetLastError();
 }
