@@ -118,3 +118,19 @@ def test_full_size_verify_t16_all_pairs():
     torch.cuda.synchronize()
     ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
     assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "verify B=256 H=32 T=16 (all pairs)")
+
+
+def test_verify_tensor_cores_uneven_pairs_per_cta():
+    # 640 (b, h) pairs: more than the two resident CTAs per SM, so the persistent
+    # CTAs walk two or three pairs each and prefetch across pairs; T = 7 leaves
+    # nine empty token rows of the 16-token chunk, d_k = 64 and d_v = 48 leave
+    # channels of the 128-wide tiles empty.
+    w = replace(WORKLOADS[1], H=2, dk=64, dv=48, seed=97, initial_state=True)
+    x = make_inputs(w, B=320, T=7)
+    xc = cuda(x)
+    state = xc["S0"].clone()
+    o = kda.spec_verify(xc["q"], xc["k"], xc["v"], xc["z"], xc["beta"], xc["A"], state)
+    torch.cuda.synchronize()
+    assert torch.equal(state, xc["S0"])
+    ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
+    assert_parity(o.reshape(ro.shape), ro, torch.bfloat16, "verify B=320 H=2 T=7 dk=64 dv=48")
