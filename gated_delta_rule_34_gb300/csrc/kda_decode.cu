@@ -149,6 +149,11 @@ __device__ __forceinline__ void cp_async8_ca(void* dst_smem, const void* src) {
 __device__ __forceinline__ void prefetch_line_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// 16-byte async copy that fills the 16 - src_bytes bytes past the source with zeros.
+__device__ __forceinline__ void cp_async16_zfill(void* dst_smem, const void* src, uint32_t src_bytes) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst_smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all_own() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -317,7 +322,12 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
 namespace kda {
 
 constexpr int kSpecMaxT = 16;
-constexpr uint32_t kSpecStage = 32 * kDecodeThreads * 8;   // 64 KiB: the state, staged
+// The state staged row by row: rows of 128 floats, the four 32-row quarters 16
+// floats apart, so that a warp's row-pair reads (four quarters x 64 bytes) take
+// the two wavefronts 256 bytes need.
+constexpr int kStageQuarter = 32 * 128 + 16;                      // floats per quarter
+constexpr uint32_t kSpecStage = 4 * kStageQuarter * 4;            // 64.25 KiB
+__device__ __forceinline__ int stage_at(int r, int c) { return (r >> 5) * kStageQuarter + (r & 31) * 128 + c; }
 constexpr int kSpecPitch = 4 * 36;   // floats per token row: four 32-row quarters, each + 4 pad
 
 __device__ __forceinline__ int spec_row(int c) { return (c >> 5) * 36 + (c & 31); }
@@ -360,12 +370,16 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     // The state read starts first: each thread copies its own 32 x 8 bytes into
     // its own shared-memory slots (cp.async, no registers held), so the read
     // overlaps the per-token preparation below; rows past d_k read as zeros.
-    extern __shared__ float2 s_stage[];                 // [32][kDecodeThreads]
+    extern __shared__ __align__(16) float s_stage[];
+    {
+        // warp w copies rows w, w + 8, ...: 16 bytes a lane, one 512-byte row a warp
+        const int c4 = 4 * lane;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = r0 + i;
-        if (col_ok && r < dk) cp_async8_ca(&s_stage[i * kDecodeThreads + tid], Sbh + (size_t)r * dv + j0);
-        else s_stage[i * kDecodeThreads + tid] = make_float2(0.f, 0.f);
+        for (int i = 0; i < 16; ++i) {
+            const int r = warp + 8 * i;
+            const bool in = r < dk && c4 < dv;
+            cp_async16_zfill(&s_stage[stage_at(r, c4)], in ? Sbh + (size_t)r * dv + c4 : Sbh, in ? 16u : 0u);
+        }
     }
 
     // Per-token vectors: gam_t k, gam_t q, k / gam_t (rows skewed), v, beta, k^T q.
@@ -433,12 +447,15 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     }
     __syncthreads();
     // R = S on entry (gam_0 = 1), held as row pairs sp[p][u] = (R[r0 + 2p][j0 + u],
-    // R[r0 + 2p + 1][j0 + u]) on which packed two-lane FMAs run.
+    // R[r0 + 2p + 1][j0 + u]) on which packed two-lane FMAs run.  The rows were
+    // copied by other warps: every thread's copies land before any is read.
     cp_async_wait_all_own();
+    __syncthreads();
     uint64_t sp[16][2];
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
-        const float2 a = s_stage[(2 * p) * kDecodeThreads + tid], c = s_stage[(2 * p + 1) * kDecodeThreads + tid];
+        const float2 a = *reinterpret_cast<const float2*>(&s_stage[stage_at(r0 + 2 * p, j0)]);
+        const float2 c = *reinterpret_cast<const float2*>(&s_stage[stage_at(r0 + 2 * p + 1, j0)]);
         sp[p][0] = f2_pack(a.x, c.x);
         sp[p][1] = f2_pack(a.y, c.y);
     }
