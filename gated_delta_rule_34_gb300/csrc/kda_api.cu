@@ -518,8 +518,8 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
     kda::profile_event(0, stream);
     // bf16 heads with d_k and d_v multiples of 16 and more than 4 draft tokens:
     // the draft span is one 16-token chunk on the tensor cores; otherwise token
-    // by token in fp32 (up to 4 tokens that is faster: 0.126 against 0.203 ms at
-    // T = 1, 0.183 against 0.208 ms at T = 4, for B = 256, H = 32).
+    // by token in fp32 (up to 4 tokens that is faster: 0.128 against 0.203 ms at
+    // T = 1, 0.175 against 0.208 ms at T = 4, for B = 256, H = 32).
     const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0 && T > 4;
     const cudaError_t e =
         tc ? kda::run_spec_verify_tc(q, k, v, z, beta, A, state, o, B, T, H, d_k, d_v, stream)

@@ -332,6 +332,36 @@ constexpr int kSpecPitch = 4 * 36;   // floats per token row: four 32-row quarte
 
 __device__ __forceinline__ int spec_row(int c) { return (c >> 5) * 36 + (c & 31); }
 
+// src[0 .. n) as floats, zeros past n (n <= 8): one 16-byte load (bf16) or two
+// (fp32) when all eight are present and `vec` says the run is 16-byte aligned.
+__device__ __forceinline__ void load_run8(const __nv_bfloat16* __restrict__ src, int n, bool vec,
+                                          float (&f)[8]) {
+    if (vec && n == 8) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(src));
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(b2[e]);
+            f[2 * e] = x.x;
+            f[2 * e + 1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = e < n ? __bfloat162float(src[e]) : 0.f;
+    }
+}
+__device__ __forceinline__ void load_run8(const float* __restrict__ src, int n, bool vec, float (&f)[8]) {
+    if (vec && n == 8) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(src) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = e < n ? src[e] : 0.f;
+    }
+}
+
 template <typename T, bool kVerify>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
@@ -386,52 +416,63 @@ spec_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restric
     __shared__ __align__(16) float s_kg[kSpecMaxT][kSpecPitch], s_qg[kSpecMaxT][kSpecPitch];
     __shared__ __align__(16) float s_kh[kSpecMaxT][kSpecPitch];
     __shared__ __align__(16) float s_v[kSpecMaxT][128], s_L[kSpecMaxT][128];
-    __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_kqp[kSpecMaxT][4], s_gam[128];
-    // (a) every (token, channel) at once: raw k and q, v, the gate g, and k^T q
-    //     partial sums over each warp's 32 channels.  Thread (token
-    //     tid / 128 + 2 i, channel tid mod 128) issues all of its loads first,
-    //     so that one memory round trip covers the span.
-    constexpr int kPer = kSpecMaxT * 128 / kDecodeThreads;
-    const int ch = tid & 127;
-    T xk[kPer], xq[kPer], xz[kPer], xv[kPer];
-    const float eA = ch < dk ? A[(size_t)h * dk + ch] : 0.f;
+    __shared__ float s_b[kSpecMaxT], s_kq[kSpecMaxT], s_gam[128];
+    // (a) thread (token tt = tid / 16, channels 8 c8 .. 8 c8 + 7, c8 = tid % 16)
+    //     loads 16 bytes of each input row at once, so that the span takes one
+    //     round of wide loads: raw k and q, v, the gate g, and k^T q summed over
+    //     the token's 16 lanes.
+    {
+        const int tt = tid >> 4, c8 = tid & 15, cb = 8 * c8;
+        const bool live = tt < n_steps;
+        const size_t row = ((size_t)b * Tn + (live ? tt : 0)) * H + h;
+        const int nk = live ? (dk - cb < 0 ? 0 : (dk - cb > 8 ? 8 : dk - cb)) : 0;
+        const int nv = live ? (dv - cb < 0 ? 0 : (dv - cb > 8 ? 8 : dv - cb)) : 0;
+        constexpr int kVec = 16 / (int)sizeof(T);          // elements per 16 bytes
+        float kf[8], qf[8], zf[8], vf[8], af[8];
+        load_run8(k + row * dk + cb, nk, dk % kVec == 0, kf);
+        if (kVerify) load_run8(q + row * dk + cb, nk, dk % kVec == 0, qf);
+        else
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        const int t = (tid >> 7) + 2 * i;
-        const size_t row = ((size_t)b * Tn + (t < n_steps ? t : 0)) * H + h;
-        const bool live = t < n_steps;
-        xk[i] = (live && ch < dk) ? k[row * dk + ch] : from_f32<T>(0.f);
-        xq[i] = (kVerify && live && ch < dk) ? q[row * dk + ch] : from_f32<T>(0.f);
-        xz[i] = (live && ch < dk) ? z[row * dk + ch] : from_f32<T>(0.f);
-        xv[i] = (live && ch < dv) ? v[row * dv + ch] : from_f32<T>(0.f);
-    }
-    const float expA = expf(eA);
+            for (int e = 0; e < 8; ++e) qf[e] = 0.f;
+        load_run8(z + row * dk + cb, nk, dk % kVec == 0, zf);
+        load_run8(v + row * dv + cb, nv, dv % kVec == 0, vf);
+        load_run8(A + (size_t)h * dk + cb, nk, dk % 4 == 0, af);
+        if (live) {
+            float g[8];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        const int t = (tid >> 7) + 2 * i;
-        if (t >= n_steps) continue;                     // uniform per warp
-        const float kk = to_f32(xk[i]), qq = to_f32(xq[i]);
-        s_kh[t][spec_row(ch)] = kk;
-        s_qg[t][spec_row(ch)] = qq;
-        s_L[t][ch] = ch < dk ? gate_accurate(expA, to_f32(xz[i])) : 0.f;
-        s_v[t][ch] = to_f32(xv[i]);
+            for (int e = 0; e < 8; ++e) g[e] = e < nk ? gate_accurate(expf(af[e]), zf[e]) : 0.f;
+            // channels cb .. cb + 7 lie in one 32-channel quarter of the skewed rows
+            float4* kh4 = reinterpret_cast<float4*>(&s_kh[tt][spec_row(cb)]);
+            float4* qg4 = reinterpret_cast<float4*>(&s_qg[tt][spec_row(cb)]);
+            float4* l4 = reinterpret_cast<float4*>(&s_L[tt][cb]);
+            float4* v4 = reinterpret_cast<float4*>(&s_v[tt][cb]);
+            kh4[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
+            kh4[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
+            qg4[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
+            qg4[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
+            l4[0] = make_float4(g[0], g[1], g[2], g[3]);
+            l4[1] = make_float4(g[4], g[5], g[6], g[7]);
+            v4[0] = make_float4(vf[0], vf[1], vf[2], vf[3]);
+            v4[1] = make_float4(vf[4], vf[5], vf[6], vf[7]);
+        }
         if (kVerify) {
-            const float p = warp_sum(kk * qq);
-            if (lane == 0) s_kqp[t][ch >> 5] = p;
+            float p = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p = fmaf(kf[e], qf[e], p);
+#pragma unroll
+            for (int m = 1; m <= 8; m <<= 1) p += __shfl_xor_sync(0xffffffffu, p, m);
+            if (live && c8 == 0) s_kq[tt] = p;
         }
     }
     if (tid < n_steps) s_b[tid] = to_f32(beta[((size_t)b * Tn + tid) * H + h]);
     __syncthreads();
-    // (b) the running log-decay per channel, in place; k^T q per token
+    // (b) the running log-decay per channel, in place
     if (tid < 128) {
         float L = 0.f;
         for (int t = 0; t < n_steps; ++t) {
             L += s_L[t][tid];
             s_L[t][tid] = L;
         }
-    } else if (kVerify && tid < 128 + kSpecMaxT && tid - 128 < n_steps) {
-        const int t = tid - 128;
-        s_kq[t] = (s_kqp[t][0] + s_kqp[t][1]) + (s_kqp[t][2] + s_kqp[t][3]);
     }
     __syncthreads();
     // (c) the decay-scaled vectors, every (token, channel) at once
