@@ -113,6 +113,10 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
 #pragma unroll
         for (int c = 0; c < 4; ++c) ob[c] = from_f32<T>(fmaf(u[c], kq, pq[c]));
     }
+    // The row pointer is formed here, out of the compiler's sight, so that the
+    // 16 row addresses of the read are not held until the write.
+    float* row = Sbh + (size_t)rg * dv + j0;
+    asm volatile("mov.b64 %0, %0;" : "+l"(row));
 #pragma unroll
     for (int i = 0; i < kDecodeRows; ++i) {
         const int r = rg + 8 * i;
@@ -123,8 +127,9 @@ decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restr
             w.y = fmaf(kr, u[1], s[i].y);
             w.z = fmaf(kr, u[2], s[i].z);
             w.w = fmaf(kr, u[3], s[i].w);
-            __stcs(reinterpret_cast<float4*>(Sbh + (size_t)r * dv + j0), w);
+            __stcs(reinterpret_cast<float4*>(row), w);
         }
+        row += (size_t)8 * dv;
     }
 }
 
