@@ -258,6 +258,10 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
                        const void* beta, const float* A, float* state, void* o, int B, int H,
                        int dk, int dv, bool bf16, cudaStream_t stream) {
     const unsigned grid = (unsigned)((int64_t)B * H);
+    // Other head sizes: a warp per 16 columns of S, and at least four warps (thread
+    // c < 128 loads channel c of k, q, z); smaller CTAs let more pairs be resident.
+    const int col_warps = (dv + 15) / 16;
+    const int threads = 32 * (col_warps < 4 ? 4 : col_warps);
     if (dk == 128 && dv == 128) {
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -287,12 +291,12 @@ cudaError_t run_decode(const void* q, const void* k, const void* v, const void* 
     }
     if (bf16) {
         using T = __nv_bfloat16;
-        decode_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
+        decode_kernel<T><<<grid, threads, 0, stream>>>(
             static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
             static_cast<const T*>(z), static_cast<const T*>(beta), A, state,
             static_cast<T*>(o), H, dk, dv);
     } else {
-        decode_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+        decode_kernel<float><<<grid, threads, 0, stream>>>(
             static_cast<const float*>(q), static_cast<const float*>(k),
             static_cast<const float*>(v), static_cast<const float*>(z),
             static_cast<const float*>(beta), A, state, static_cast<float*>(o), H, dk, dv);

@@ -67,6 +67,24 @@ def test_decode_matches_oracle(B, H, d, dtype):
     assert rel_err(state, rS) < 1e-5
 
 
+@pytest.mark.parametrize("dk,dv", [(128, 48), (96, 64), (48, 96), (24, 128)])
+def test_decode_unequal_head_sizes(dk, dv):
+    # CTAs of a warp per 16 columns of S, at least four warps (which load all d_k
+    # channels): four warps for d_v <= 64, six for d_v = 96, eight for d_v = 128.
+    from dataclasses import replace
+    w = replace(WORKLOADS[3], H=3, dk=dk, dv=dv, dtype=torch.bfloat16, seed=dk + dv)
+    x = make_inputs(w, B=5)
+    S0 = x["S0"].clone()
+    xc = cuda(x)
+    state = xc["S0"].clone()
+    o = kda.decode_step(xc["q"], xc["k"], xc["v"], xc["z"], xc["beta"], xc["A"], state)
+    torch.cuda.synchronize()
+    ro, rS = oracle.recurrent(x["q"][:, None], x["k"][:, None], x["v"][:, None],
+                              x["z"][:, None], x["beta"][:, None], x["A"], S0=S0)
+    assert_parity(o, ro.reshape(5, 3, dv), torch.bfloat16, f"decode o dk={dk} dv={dv}")
+    assert rel_err(state, rS) < 1e-5
+
+
 def test_decode_full_workload():
     w = WORKLOADS[3]
     x = make_inputs(w)
