@@ -516,11 +516,12 @@ kda_status kda_spec_verify(const void* q, const void* k, const void* v, const vo
     KDA_REQUIRE_PTR(state);
     KDA_REQUIRE_PTR(o);
     kda::profile_event(0, stream);
-    // bf16 heads with d_k and d_v multiples of 16 and more than 4 draft tokens:
+    // bf16 heads with d_k and d_v multiples of 16 and more than 5 draft tokens:
     // the draft span is one 16-token chunk on the tensor cores; otherwise token
-    // by token in fp32 (up to 4 tokens that is faster: 0.128 against 0.203 ms at
-    // T = 1, 0.175 against 0.208 ms at T = 4, for B = 256, H = 32).
-    const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0 && T > 4;
+    // by token in fp32 (up to 5 tokens that is faster: 0.128 against 0.203 ms at
+    // T = 1, 0.175 against 0.208 ms at T = 4, 0.201 against 0.210 ms at T = 5,
+    // against 0.214 / 0.212 ms at T = 6, for B = 256, H = 32).
+    const bool tc = dtype == KDA_DTYPE_BF16 && d_k % 16 == 0 && d_v % 16 == 0 && T > 5;
     const cudaError_t e =
         tc ? kda::run_spec_verify_tc(q, k, v, z, beta, A, state, o, B, T, H, d_k, d_v, stream)
            : kda::run_spec(q, k, v, z, beta, A, const_cast<float*>(state), o, nullptr, B, T, H, d_k,

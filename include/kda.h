@@ -353,14 +353,15 @@ kda_status kda_static_workspace_status(uint32_t *status, cudaStream_t stream);
  *   n_accept device int32 [B]; values are clamped into [0, T]; 0 leaves the
  *   state untouched.
  * Both take 1 <= T <= 16, d_k <= 128, d_v <= 128 with d_v a multiple of 4.
- * Arithmetic: commit, verify of fp32 inputs and verify of at most 4 draft
+ * Arithmetic: commit, verify of fp32 inputs and verify of at most 5 draft
  * tokens run token by token in fp32 (commit with n_accept = T equals T decode
  * steps to fp32 rounding, so a state advanced by speculative decoding carries
- * no extra rounding).  verify of more than 4 bf16 tokens with d_k and d_v
+ * no extra rounding).  verify of more than 5 bf16 tokens with d_k and d_v
  * multiples of 16 takes the span as one 16-token chunk of the chunked form on
  * the tensor cores (the state's products in bf16, as in the tensor-core
  * prefill; outputs within the same bound, 2e-2 of max |o|); if one of its
- * bounded waits gives up, that (b, h)'s outputs are NaN.
+ * bounded waits gives up, the outputs of that (b, h) and of the other pairs
+ * its CTA has still to walk are NaN.
  */
 kda_status kda_spec_verify(const void *q, const void *k, const void *v, const void *z,
                            const void *beta, const float *A, const float *state, void *o, int B,

@@ -20,7 +20,8 @@ def _draft(B, T, H, d, dtype, seed):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("B,T,H,d", [(3, 1, 2, 128), (3, 4, 2, 128), (2, 16, 3, 128), (2, 5, 2, 64)])
+@pytest.mark.parametrize("B,T,H,d", [(3, 1, 2, 128), (3, 4, 2, 128), (2, 16, 3, 128), (2, 5, 2, 64),
+                                     (2, 6, 2, 64)])
 def test_verify_outputs_and_state_untouched(B, T, H, d, dtype):
     x = _draft(B, T, H, d, dtype, seed=B * 10 + T + d)
     xc = cuda(x)
@@ -29,13 +30,13 @@ def test_verify_outputs_and_state_untouched(B, T, H, d, dtype):
     torch.cuda.synchronize()
     assert torch.equal(state, xc["S0"]), "verify must not modify the state"
     ro, _ = oracle.recurrent(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], S0=x["S0"])
-    # fp32 inputs, and up to 4 bf16 tokens: token by token in fp32.  More bf16 tokens: the
+    # fp32 inputs, and up to 5 bf16 tokens: token by token in fp32.  More bf16 tokens: the
     # span as one 16-token chunk on the tensor cores, held to the layer's bf16 bound like
     # the tensor-core prefill.
     assert_parity(o.reshape(ro.shape), ro, dtype, f"verify B={B} T={T} d={d}")
     if dtype == torch.float32:
         assert rel_err(o.reshape(ro.shape), ro) < 1e-5
-    if dtype == torch.bfloat16 and T <= 4:
+    if dtype == torch.bfloat16 and T <= 5:
         # fp32 arithmetic: only the bf16 rounding of o itself remains
         assert rel_err(o.reshape(ro.shape), ro) < 5e-3
 
