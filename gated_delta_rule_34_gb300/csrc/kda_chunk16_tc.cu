@@ -821,14 +821,15 @@ spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                 mma_commit(bar);
             }
             if (!(ok = cta_wait(bar, phase))) break;
-            if (warp < 4) {
-                float w[16];
-                tmem_ld16(tbase + tl + T_WT, w);
+            {
+                // W rows: channel c = lane j of the warp's quadrant, tokens 8 th .. 8 th + 7
+                const int th = warp >> 2, c = j;
+                float w[8];
+                tmem_ld8(tbase + tl + T_WT + 8 * th, w);
                 tmem_wait_ld();
-                const int c = 32 * warp + lane;
 #pragma unroll
-                for (int t = 0; t < kC; ++t)
-                    *reinterpret_cast<__nv_bfloat16*>(sm + V_SB + (c >> 6) * 4096 + sw128(t, (c & 63) >> 3) +
+                for (int t = 0; t < 8; ++t)
+                    *reinterpret_cast<__nv_bfloat16*>(sm + V_SB + (c >> 6) * 4096 + sw128(8 * th + t, (c & 63) >> 3) +
                                                        (c & 7) * 2) = __float2bfloat16_rn(w[t]);
             }
             // ---- the state's bf16 copy S^T, row j (its loads have landed by now)
@@ -859,20 +860,19 @@ spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                 mma_commit(bar);
             }
             if (!(ok = cta_wait(bar, phase))) break;
-            if (warp < 4) {
-                float ws_[16], ut[16];
-                tmem_ld16(tbase + tl + T_ST, ws_);
-                tmem_ld16(tbase + tl + T_UT, ut);
+            {
+                // U^T row j, tokens 8 hh .. 8 hh + 7 (hh = warp half)
+                const int hh = warp >> 2;
+                float ws_[8], ut[8];
+                tmem_ld8(tbase + tl + T_ST + 8 * hh, ws_);
+                tmem_ld8(tbase + tl + T_UT + 8 * hh, ut);
                 tmem_wait_ld();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint4 r;
-                    r.x = pack_bf16x2(ut[8 * hh + 0] - ws_[8 * hh + 0], ut[8 * hh + 1] - ws_[8 * hh + 1]);
-                    r.y = pack_bf16x2(ut[8 * hh + 2] - ws_[8 * hh + 2], ut[8 * hh + 3] - ws_[8 * hh + 3]);
-                    r.z = pack_bf16x2(ut[8 * hh + 4] - ws_[8 * hh + 4], ut[8 * hh + 5] - ws_[8 * hh + 5]);
-                    r.w = pack_bf16x2(ut[8 * hh + 6] - ws_[8 * hh + 6], ut[8 * hh + 7] - ws_[8 * hh + 7]);
-                    *reinterpret_cast<uint4*>(sm + V_UT + sw128(j, hh)) = r;
-                }
+                uint4 r;
+                r.x = pack_bf16x2(ut[0] - ws_[0], ut[1] - ws_[1]);
+                r.y = pack_bf16x2(ut[2] - ws_[2], ut[3] - ws_[3]);
+                r.z = pack_bf16x2(ut[4] - ws_[4], ut[5] - ws_[5]);
+                r.w = pack_bf16x2(ut[6] - ws_[6], ut[7] - ws_[7]);
+                *reinterpret_cast<uint4*>(sm + V_UT + sw128(j, hh)) = r;
             }
             fence_async_smem();
             tc_fence_before();
@@ -887,19 +887,23 @@ spec_verify_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             ok = cta_wait(bar, phase);
         } while (false);
 
-        // ---- outputs o[b][t][h][j] (warps 0..3); NaN once a wait has given up
-        if (warp < 4) {
-            float ov[16];
+        // ---- outputs o[b][t][h][j], tokens 8 th .. 8 th + 7 (th = warp half); NaN
+        //      once a wait has given up
+        {
+            const int th = warp >> 2;
+            float ov[8];
             if (ok) {
-                tmem_ld16(tbase + tl + T_ST + 16, ov);
+                tmem_ld8(tbase + tl + T_ST + 16 + 8 * th, ov);
                 tmem_wait_ld();
             }
             if (j < dv) {
 #pragma unroll
-                for (int t = 0; t < kC; ++t)
+                for (int e = 0; e < 8; ++e) {
+                    const int t = 8 * th + e;
                     if (t < Tn)
                         o[(((size_t)b * Tn + t) * H + h) * dv + j] =
-                            __float2bfloat16_rn(ok ? ov[t] : __int_as_float(0x7fc00000));
+                            __float2bfloat16_rn(ok ? ov[e] : __int_as_float(0x7fc00000));
+                }
             }
         }
         // this pair's TMEM reads are done before the next pair's products
