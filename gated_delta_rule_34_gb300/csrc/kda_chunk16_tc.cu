@@ -610,6 +610,18 @@ constexpr uint32_t V_IN_Q = V_APA + 8192 + 4096;
 constexpr uint32_t V_IN_V = V_IN2;
 constexpr uint32_t V_IN_Z = V_IN2 + 4096;
 
+// 32 lanes x 32-bit, 8 consecutive columns: thread i of the warp receives TMEM
+// lane (lane field of taddr) + i, columns col .. col + 7.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t& phase) {
     const bool ok = mbar_wait(bar, phase);
     phase ^= 1u;
