@@ -22,16 +22,20 @@
 // 1e-4 bound for fp32 inputs).
 //
 // Columns of S evolve independently (column j only sees k, a, b and v[:, j]),
-// so the work splits over (sequence, head, 64-column group).  A CTA of eight
-// warps owns 64 columns; warp w owns 8 of them, lane (rq = lane / 4, cq =
-// lane mod 4) holds rows 16 rq .. 16 rq + 15 of columns 8 w + 2 cq and
-// 8 w + 2 cq + 1 (32 registers, as row pairs on which packed two-lane FMAs
-// run), so the d_k reductions are in-thread sums of 16 plus three
-// xor-shuffles (lane bits 2..4).  Tiles of 16 tokens are staged
+// so the work splits over (sequence, head, column group).  A CTA of eight
+// warps owns kCols = 64 or 32 columns; warp w owns kCols / 8 of them, lane
+// (rq = lane / kCq, cq = lane mod kCq, kCq = kCols / 16 column pairs) holds
+// 128 / (32 / kCq) rows (16 or 8) of columns kCols / 8 w + 2 cq, + 1 (row pairs
+// on which packed two-lane FMAs run), so the d_k reductions are in-thread sums
+// plus xor-shuffles over the row-group lane bits.  The 32-column form doubles
+// the CTAs where 64-column ones would leave most SMs idle (narrow heads, few
+// sequences); each CTA repeats the per-token preparation of its tile.  Tiles of 16 tokens are staged
 // in shared memory; the next tile's raw inputs are loaded into registers while
 // the current tile's tokens run.  The per-row vectors sit in rows whose
 // 16-channel groups are 20 floats apart, so the eight row groups of a warp
 // read them as conflict-free 16-byte loads.
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -40,12 +44,11 @@ namespace kda {
 constexpr int kRecThreads = 256;
 constexpr int kRecTile = 16;     // tokens staged per shared-memory tile
 constexpr int kRecRun = 8;       // tokens per factoring run (gam >= e^{-5 kRecRun})
-constexpr int kRecCols = 64;     // state columns per CTA (8 per warp)
 constexpr int kRecPitch = 160;   // floats per token row of the scaled vectors: 8 groups of 16 + 4
 
 __device__ __forceinline__ int rec_idx(int c) { return (c >> 4) * 20 + (c & 15); }
 
-template <typename T>
+template <typename T, int kCols>
 __global__ void __launch_bounds__(kRecThreads)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const T* __restrict__ z, const T* __restrict__ beta,
@@ -53,17 +56,21 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  const float* __restrict__ S0, float* __restrict__ S1,
                  const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H,
                  int dk, int dv, CheckpointSpec ck) {
+    static_assert(kCols == 64 || kCols == 32, "column group");
+    constexpr int kCq = kCols / 16;                   // column pairs per warp (lanes along columns)
+    constexpr int kRows = 128 / (32 / kCq);           // rows per lane: 16 or 8
+    constexpr int kPairs = kRows / 2;                 // row pairs per lane
     const int cgrp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rq = lane >> 2, cq = lane & 3;
-    const int col0 = cgrp * kRecCols;                 // first column of this CTA
-    const int lcol = 8 * warp + 2 * cq;               // this lane's first column, CTA-local
-    const int r0 = 16 * rq;                           // this lane's first row
+    const int rq = lane / kCq, cq = lane % kCq;
+    const int col0 = cgrp * kCols;                    // first column of this CTA
+    const int lcol = (kCols / 8) * warp + 2 * cq;     // this lane's first column, CTA-local
+    const int r0 = kRows * rq;                        // this lane's first row
 
     // s_kg holds g, then the running log-decay L, before gam k
     __shared__ __align__(16) float s_kg[kRecTile * kRecPitch], s_qg[kRecTile * kRecPitch];
     __shared__ __align__(16) float s_kh[kRecTile * kRecPitch];
-    __shared__ __align__(16) float s_v[kRecTile][kRecCols], s_o[kRecTile][kRecCols];
+    __shared__ __align__(16) float s_v[kRecTile][kCols], s_o[kRecTile][kCols];
     __shared__ __align__(16) float s_glast[kRecTile / kRecRun][kRecPitch];   // gam at each run's end
     __shared__ float s_b[kRecTile], s_kq[kRecTile], s_kqp[kRecTile][4], s_expA[128];
 
@@ -75,11 +82,11 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
     // State registers: st[p][u] = (S[r0 + 2p][j], S[r0 + 2p + 1][j]) with
     // j = col0 + lcol + u (R inside a run).
-    uint64_t st[8][2];
+    uint64_t st[kPairs][2];
     const size_t sbase = ((size_t)n * H + h) * dk * dv;
     const bool okc[2] = {col0 + lcol < dv, col0 + lcol + 1 < dv};
 #pragma unroll
-    for (int p2 = 0; p2 < 8; ++p2) {
+    for (int p2 = 0; p2 < kPairs; ++p2) {
         const int r = r0 + 2 * p2;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -89,7 +96,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     }
     auto store_state = [&](float* mat) {      // mat: [d_k][d_v] of (n, h)
 #pragma unroll
-        for (int p2 = 0; p2 < 8; ++p2) {
+        for (int p2 = 0; p2 < kPairs; ++p2) {
             const int r = r0 + 2 * p2;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -105,7 +112,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     // tile's tokens run: thread (row tt = tid / 128 + 2 i, channel c = tid mod
     // 128) for q, k, z; (tt, column) pairs idx = tid + 256 i for v; beta by
     // threads < 16.
-    constexpr int kVPer = kRecTile * kRecCols / kRecThreads;
+    constexpr int kVPer = kRecTile * kCols / kRecThreads;
     float rq_[kRecTile / 2], rk_[kRecTile / 2], rz_[kRecTile / 2], rv_[kVPer];
     float rb_ = 0.f;
     auto fetch = [&](int64_t t0) {
@@ -124,7 +131,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         }
 #pragma unroll
         for (int i = 0; i < kVPer; ++i) {
-            const int idx = tid + kRecThreads * i, tt = idx / kRecCols, j = col0 + idx % kRecCols;
+            const int idx = tid + kRecThreads * i, tt = idx / kCols, j = col0 + idx % kCols;
             rv_[i] = (tt < nt && j < dv) ? to_f32(v[((size_t)(t0 + tt) * H + h) * dv + j]) : 0.f;
         }
         if (tid < kRecTile) rb_ = tid < nt ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
@@ -149,7 +156,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 #pragma unroll
             for (int i = 0; i < kVPer; ++i) {
                 const int idx = tid + kRecThreads * i;
-                s_v[idx / kRecCols][idx % kRecCols] = rv_[i];
+                s_v[idx / kCols][idx % kCols] = rv_[i];
             }
             if (tid < kRecTile) s_b[tid] = rb_;
         }
@@ -192,12 +199,12 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         if (t0 + kRecTile < eos) fetch(t0 + kRecTile);
 
         for (int tt = 0; tt < nt; ++tt) {
-            const int base = tt * kRecPitch + rq * 20;
+            const int base = tt * kRecPitch + rec_idx(r0);
             // S'^T k and S'^T q on this lane's 16 rows: row pairs on packed
             // FMAs, two accumulators per column and vector
             uint64_t pk[2][2] = {{0ull, 0ull}, {0ull, 0ull}}, pq[2][2] = {{0ull, 0ull}, {0ull, 0ull}};
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
+            for (int x = 0; x < kPairs / 2; ++x) {
                 const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&s_kg[base + 4 * x]);
                 const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(&s_qg[base + 4 * x]);
 #pragma unroll
@@ -217,7 +224,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                 sq[u] = (q0.x + q0.y) + (q1.x + q1.y);
             }
 #pragma unroll
-            for (int m = 4; m <= 16; m <<= 1) {
+            for (int m = kCq; m <= 16; m <<= 1) {
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], m);
@@ -231,7 +238,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                 *reinterpret_cast<float2*>(&s_o[tt][lcol]) = make_float2(fmaf(u0, kq, sq[0]), fmaf(u1, kq, sq[1]));
             const uint64_t uu[2] = {f2_pack(u0, u0), f2_pack(u1, u1)};
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
+            for (int x = 0; x < kPairs / 2; ++x) {
                 const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(&s_kh[base + 4 * x]);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -241,9 +248,9 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
             }
             // end of a run: back from R to S
             if ((tt & (kRecRun - 1)) == kRecRun - 1 || tt == nt - 1) {
-                const float* gl = &s_glast[tt / kRecRun][rq * 20];
+                const float* gl = &s_glast[tt / kRecRun][rec_idx(r0)];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
+                for (int x = 0; x < kPairs / 2; ++x) {
                     const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(gl + 4 * x);
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -254,8 +261,8 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
             }
         }
         __syncthreads();
-        for (int idx = tid; idx < nt * kRecCols; idx += kRecThreads) {
-            const int tt = idx / kRecCols, jj = idx % kRecCols;
+        for (int idx = tid; idx < nt * kCols; idx += kRecThreads) {
+            const int tt = idx / kCols, jj = idx % kCols;
             const int j = col0 + jj;
             if (j < dv) o[((size_t)(t0 + tt) * H + h) * dv + j] = from_f32<T>(s_o[tt][jj]);
         }
@@ -273,19 +280,31 @@ cudaError_t run_recurrent(const void* q, const void* k, const void* v, const voi
                           const int32_t* cu, int n_seqs, int64_t T, int64_t T_total, int H,
                           int dk, int dv, bool bf16, const CheckpointSpec& ck,
                           cudaStream_t stream) {
-    dim3 grid((unsigned)((dv + kRecCols - 1) / kRecCols), (unsigned)H, (unsigned)n_seqs);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // 32-column CTAs where 64-column ones would not cover the SMs
+    const int64_t ctas64 = (int64_t)((dv + 63) / 64) * H * n_seqs;
+    const bool narrow = ctas64 < sms;
+    const int cols = narrow ? 32 : 64;
+    dim3 grid((unsigned)((dv + cols - 1) / cols), (unsigned)H, (unsigned)n_seqs);
+    auto launch = [&](auto tag, auto cols_tag) {
+        using TT = decltype(tag);
+        constexpr int C = decltype(cols_tag)::value;
+        recurrent_kernel<TT, C><<<grid, kRecThreads, 0, stream>>>(
+            static_cast<const TT*>(q), static_cast<const TT*>(k), static_cast<const TT*>(v),
+            static_cast<const TT*>(z), static_cast<const TT*>(beta), A, static_cast<TT*>(o), S0,
+            S1, cu, T, T_total, H, dk, dv, ck);
+    };
+    using C32 = std::integral_constant<int, 32>;
+    using C64 = std::integral_constant<int, 64>;
     if (bf16) {
-        using Tb = __nv_bfloat16;
-        recurrent_kernel<Tb><<<grid, kRecThreads, 0, stream>>>(
-            static_cast<const Tb*>(q), static_cast<const Tb*>(k), static_cast<const Tb*>(v),
-            static_cast<const Tb*>(z), static_cast<const Tb*>(beta), A, static_cast<Tb*>(o),
-            S0, S1, cu, T, T_total, H, dk, dv, ck);
+        if (narrow) launch(__nv_bfloat16{}, C32{});
+        else launch(__nv_bfloat16{}, C64{});
     } else {
-        recurrent_kernel<float><<<grid, kRecThreads, 0, stream>>>(
-            static_cast<const float*>(q), static_cast<const float*>(k),
-            static_cast<const float*>(v), static_cast<const float*>(z),
-            static_cast<const float*>(beta), A, static_cast<float*>(o), S0, S1, cu, T, T_total,
-            H, dk, dv, ck);
+        if (narrow) launch(float{}, C32{});
+        else launch(float{}, C64{});
     }
     return cudaGetLastError();
 }
