@@ -72,7 +72,8 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     __shared__ __align__(16) float s_kh[kRecTile * kRecPitch];
     __shared__ __align__(16) float s_v[kRecTile][kCols], s_o[kRecTile][kCols];
     __shared__ __align__(16) float s_glast[kRecTile / kRecRun][kRecPitch];   // gam at each run's end
-    __shared__ float s_b[kRecTile], s_kq[kRecTile], s_kqp[kRecTile][4], s_expA[128];
+    __shared__ float s_b[kRecTile], s_kq[kRecTile];
+    __shared__ __align__(16) float s_expA[128];
 
     int64_t bos, eos;
     seq_bounds(cu, n, T_len, T_total, bos, eos);
@@ -109,25 +110,43 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     };
 
     // The next tile's raw inputs, loaded into registers while the current
-    // tile's tokens run: thread (row tt = tid / 128 + 2 i, channel c = tid mod
-    // 128) for q, k, z; (tt, column) pairs idx = tid + 256 i for v; beta by
-    // threads < 16.
+    // tile's tokens run: warp w takes tokens w and w + 8, lane l channels
+    // 4 l .. 4 l + 3 of q, k, z (one 16-byte load each for fp32, 8 bytes for
+    // bf16, where the rows allow); (tt, column) pairs idx = tid + 256 i for v;
+    // beta by threads < 16.
     constexpr int kVPer = kRecTile * kCols / kRecThreads;
-    float rq_[kRecTile / 2], rk_[kRecTile / 2], rz_[kRecTile / 2], rv_[kVPer];
+    constexpr int kVec = 4 * (int)sizeof(T) <= 16 && (16 % (4 * (int)sizeof(T)) == 0) ? 4 : 1;
+    const int c4 = 4 * lane;                          // this lane's first channel in the row passes
+    float rq_[2][4], rk_[2][4], rz_[2][4], rv_[kVPer];
     float rb_ = 0.f;
+    auto load4 = [&](const T* __restrict__ src, int n, float (&f)[4]) {
+        // src[0 .. n) as floats, zeros past n (n <= 4); one vector load when all four are
+        // present and the row is aligned for it
+        if (n == 4 && (dk % 4) == 0 && kVec == 4) {
+            if constexpr (sizeof(T) == 4) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+                f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+            } else {
+                const uint2 x = __ldg(reinterpret_cast<const uint2*>(src));
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+                const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+                f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = e < n ? to_f32(src[e]) : 0.f;
+        }
+    };
     auto fetch = [&](int64_t t0) {
         const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
-        const int c = tid & 127;
 #pragma unroll
-        for (int i = 0; i < kRecTile / 2; ++i) {
-            const int tt = (tid >> 7) + 2 * i;
-            rq_[i] = rk_[i] = rz_[i] = 0.f;
-            if (tt < nt && c < dk) {
-                const size_t e = ((size_t)(t0 + tt) * H + h) * dk + c;
-                rq_[i] = to_f32(q[e]);
-                rk_[i] = to_f32(k[e]);
-                rz_[i] = to_f32(z[e]);
-            }
+        for (int i = 0; i < 2; ++i) {
+            const int tt = warp + 8 * i;
+            const int n = tt < nt ? (dk - c4 < 0 ? 0 : (dk - c4 > 4 ? 4 : dk - c4)) : 0;
+            const size_t e = ((size_t)(t0 + (tt < nt ? tt : 0)) * H + h) * dk + c4;
+            load4(q + e, n, rq_[i]);
+            load4(k + e, n, rk_[i]);
+            load4(z + e, n, rz_[i]);
         }
 #pragma unroll
         for (int i = 0; i < kVPer; ++i) {
@@ -141,17 +160,23 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     for (int64_t t0 = bos; t0 < eos; t0 += kRecTile) {
         const int nt = (int)((eos - t0) < kRecTile ? (eos - t0) : kRecTile);
         __syncthreads();   // previous tile fully consumed; s_expA visible
-        // Thread (token tt = tid / 128 + 2 i, channel c = tid mod 128) keeps its
-        // raw k and q in registers: g goes to s_kg, and the warp's 32 channels
-        // of k^T q to s_kqp.
+        // Warp w (tokens w, w + 8) keeps the raw k and q of channels 4 l .. 4 l + 3
+        // in registers: g goes to s_kg, and k^T q is one warp sum per token.
         {
-            const int c = tid & 127;
+            const float4 ea = *reinterpret_cast<const float4*>(&s_expA[c4]);
+            const float eav[4] = {ea.x, ea.y, ea.z, ea.w};
 #pragma unroll
-            for (int i = 0; i < kRecTile / 2; ++i) {
-                const int tt = (tid >> 7) + 2 * i;
-                s_kg[tt * kRecPitch + rec_idx(c)] = (tt < nt && c < dk) ? gate_fast(s_expA[c], rz_[i]) : 0.f;
-                const float p = warp_sum(rk_[i] * rq_[i]);
-                if (lane == 0) s_kqp[tt][(tid >> 5) & 3] = p;
+            for (int i = 0; i < 2; ++i) {
+                const int tt = warp + 8 * i;
+                float g[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) g[e] = (tt < nt && c4 + e < dk) ? gate_fast(eav[e], rz_[i][e]) : 0.f;
+                *reinterpret_cast<float4*>(&s_kg[tt * kRecPitch + rec_idx(c4)]) = make_float4(g[0], g[1], g[2], g[3]);
+                float p = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) p = fmaf(rk_[i][e], rq_[i][e], p);
+                p = warp_sum(p);
+                if (lane == 0) s_kq[tt] = p;
             }
 #pragma unroll
             for (int i = 0; i < kVPer; ++i) {
@@ -175,23 +200,26 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                 }
                 s_glast[run][rec_idx(tid)] = __expf(L);
             }
-        } else if (tid < 128 + kRecTile) {
-            const int tt = tid - 128;
-            s_kq[tt] = (s_kqp[tt][0] + s_kqp[tt][1]) + (s_kqp[tt][2] + s_kqp[tt][3]);
         }
         __syncthreads();
         // gam k (over L in place), gam q and k / gam for every (token, channel)
         {
-            const int c = tid & 127;
 #pragma unroll
-            for (int i = 0; i < kRecTile / 2; ++i) {
-                const int tt = (tid >> 7) + 2 * i;
-                const int ix = tt * kRecPitch + rec_idx(c);
-                const float L = s_kg[ix];
-                const float g = __expf(L), ig = __expf(-L);
-                s_kg[ix] = g * rk_[i];
-                s_qg[ix] = g * rq_[i];
-                s_kh[ix] = ig * rk_[i];
+            for (int i = 0; i < 2; ++i) {
+                const int ix = (warp + 8 * i) * kRecPitch + rec_idx(c4);
+                const float4 L = *reinterpret_cast<const float4*>(&s_kg[ix]);
+                const float Lv[4] = {L.x, L.y, L.z, L.w};
+                float kg[4], qg[4], kh[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float g = __expf(Lv[e]), ig = __expf(-Lv[e]);
+                    kg[e] = g * rk_[i][e];
+                    qg[e] = g * rq_[i][e];
+                    kh[e] = ig * rk_[i][e];
+                }
+                *reinterpret_cast<float4*>(&s_kg[ix]) = make_float4(kg[0], kg[1], kg[2], kg[3]);
+                *reinterpret_cast<float4*>(&s_qg[ix]) = make_float4(qg[0], qg[1], qg[2], qg[3]);
+                *reinterpret_cast<float4*>(&s_kh[ix]) = make_float4(kh[0], kh[1], kh[2], kh[3]);
             }
         }
         __syncthreads();
