@@ -29,7 +29,8 @@
 // on which packed two-lane FMAs run), so the d_k reductions are in-thread sums
 // plus xor-shuffles over the row-group lane bits.  The 32-column form doubles
 // the CTAs where 64-column ones would leave most SMs idle (narrow heads, few
-// sequences); each CTA repeats the per-token preparation of its tile.  Tiles of 16 tokens are staged
+// sequences); each CTA repeats the per-token preparation of its tile.  Heads
+// with d_k <= 64 hold only kDk = 64 rows, so their lanes own half as many.  Tiles of 16 tokens are staged
 // in shared memory; the next tile's raw inputs are loaded into registers while
 // the current tile's tokens run.  The per-row vectors sit in rows whose
 // 16-channel groups are 20 floats apart, so the eight row groups of a warp
@@ -48,7 +49,7 @@ constexpr int kRecPitch = 160;   // floats per token row of the scaled vectors: 
 
 __device__ __forceinline__ int rec_idx(int c) { return (c >> 4) * 20 + (c & 15); }
 
-template <typename T, int kCols>
+template <typename T, int kCols, int kDk>
 __global__ void __launch_bounds__(kRecThreads)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const T* __restrict__ z, const T* __restrict__ beta,
@@ -57,8 +58,9 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                  const int32_t* __restrict__ cu, int64_t T_len, int64_t T_total, int H,
                  int dk, int dv, CheckpointSpec ck) {
     static_assert(kCols == 64 || kCols == 32, "column group");
+    static_assert(kDk == 128 || kDk == 64, "rows held");
     constexpr int kCq = kCols / 16;                   // column pairs per warp (lanes along columns)
-    constexpr int kRows = 128 / (32 / kCq);           // rows per lane: 16 or 8
+    constexpr int kRows = kDk / (32 / kCq);           // rows per lane: 16, 8 or 4
     constexpr int kPairs = kRows / 2;                 // row pairs per lane
     const int cgrp = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -317,22 +319,30 @@ cudaError_t run_recurrent(const void* q, const void* k, const void* v, const voi
     const bool narrow = ctas64 < sms;
     const int cols = narrow ? 32 : 64;
     dim3 grid((unsigned)((dv + cols - 1) / cols), (unsigned)H, (unsigned)n_seqs);
-    auto launch = [&](auto tag, auto cols_tag) {
+    const bool rows64 = dk <= 64;
+    auto launch = [&](auto tag, auto cols_tag, auto rows_tag) {
         using TT = decltype(tag);
         constexpr int C = decltype(cols_tag)::value;
-        recurrent_kernel<TT, C><<<grid, kRecThreads, 0, stream>>>(
+        constexpr int R = decltype(rows_tag)::value;
+        recurrent_kernel<TT, C, R><<<grid, kRecThreads, 0, stream>>>(
             static_cast<const TT*>(q), static_cast<const TT*>(k), static_cast<const TT*>(v),
             static_cast<const TT*>(z), static_cast<const TT*>(beta), A, static_cast<TT*>(o), S0,
             S1, cu, T, T_total, H, dk, dv, ck);
     };
     using C32 = std::integral_constant<int, 32>;
     using C64 = std::integral_constant<int, 64>;
+    using R64 = std::integral_constant<int, 64>;
+    using R128 = std::integral_constant<int, 128>;
+    auto by_rows = [&](auto tag, auto cols_tag) {
+        if (rows64) launch(tag, cols_tag, R64{});
+        else launch(tag, cols_tag, R128{});
+    };
     if (bf16) {
-        if (narrow) launch(__nv_bfloat16{}, C32{});
-        else launch(__nv_bfloat16{}, C64{});
+        if (narrow) by_rows(__nv_bfloat16{}, C32{});
+        else by_rows(__nv_bfloat16{}, C64{});
     } else {
-        if (narrow) launch(float{}, C32{});
-        else launch(float{}, C64{});
+        if (narrow) by_rows(float{}, C32{});
+        else by_rows(float{}, C64{});
     }
     return cudaGetLastError();
 }
