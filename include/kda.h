@@ -125,6 +125,9 @@ kda_status kda_gate(const void *z, const float *A, float *g, int64_t n_tokens, i
  *                  run waits that long) sets a nonzero bit there and returns
  *                  instead of hanging.  Read it after the stream has finished:
  *                  nonzero means o and the states of that call are not valid.
+ *                  The fp32 SIMT recurrence needs no workspace: if one of its
+ *                  bounded waits gives up, o from that point of the sequence
+ *                  and that sequence's final state are NaN instead.
  * T == 0 (or every sequence empty) writes only the final states (copies of the
  * initial ones, or zeros).
  * A fixed-length batch whose (sequence, head) chains would leave most SMs idle
