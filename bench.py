@@ -609,6 +609,7 @@ def run_ncu_case(case: str) -> int:
     chunk16:   the 16-token path, B=1, H=32, T=4096, two calls.
     segmented: B=1, H=1, T=65536 with automatic segments, two calls.
     spec:      verify + commit of 16 draft tokens, B=256, H=32, twice.
+    recurrent: the fp32 recurrence, B=1, H=32, T=4096, d=64 (fp32 inputs), two calls.
     """
     import torch
     import gated_delta_rule_34_gb300 as kda
@@ -648,6 +649,14 @@ def run_ncu_case(case: str) -> int:
         for _ in range(2):
             kda.spec_verify(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"], st)
             kda.spec_commit(x["k"], x["v"], x["z"], x["beta"], x["A"], st, n_acc)
+    elif case == "recurrent":
+        # the fp32 recurrence on B=1, H=32, T=4096, d=64 with fp32 inputs, two calls
+        from dataclasses import replace
+        w = replace(WORKLOADS[2], dk=64, dv=64, seed=110)
+        x = make_inputs(w, device="cuda", T=4096)
+        a = tuple(x[n].float() for n in ("q", "k", "v", "z", "beta")) + (x["A"],)
+        for _ in range(2):
+            kda.chunk_prefill(*a, initial_state=x["S0"], chunk=16)
     else:
         w = WORKLOADS[3]
         x = make_inputs(w, device="cuda")
@@ -669,7 +678,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the speculative-decoding and checkpoint timings")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "chunk16", "segmented", "spec"],
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "chunk16", "segmented", "spec", "recurrent"],
                     help="run a short fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
     if args.ncu_case:
